@@ -1,0 +1,285 @@
+"""CPU oracle for the int4 weight-streaming GEMV (test infrastructure only).
+
+This package is the plain, slow, obviously correct restatement of what the
+GPU library computes.  Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (and its ``--impl reference`` arm) may import it;
+the product path never does, and it shares no code with the CUDA library.
+
+The arithmetic lives in ``q4_oracle.c`` (plain C99, binary64 accumulation);
+this module only compiles it with ``gcc`` and marshals numpy arrays into it.
+
+Array conventions (all C-contiguous numpy arrays):
+
+* ``codes``  uint8  [N, K/2]          two 4-bit codes per byte, even k low
+* ``scales`` uint16 [N, K/g]          fp16 bit patterns
+* ``zeros``  uint8  [N, ceil(K/g/2)]  two 4-bit zero points per byte, even
+                                      group low; ``None`` = symmetric (8)
+* ``x``      float32 [M, K];  ``a_bf16`` uint16 [M, K] (bfloat16 bits)
+* results    float32 [M, N] plus the binary64 bound sum_k |w*x| [M, N]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle_q4.so")
+# A test may point the wrapper at a separately compiled copy of the oracle
+# (the planted-mistake tests compile altered copies to show the pins catch
+# them); the environment variable names that shared object.
+_LIB_OVERRIDE = os.environ.get("Q4_ORACLE_LIB")
+
+# ISO C mode and -ffp-contract=off: the products and sums are rounded exactly
+# as written (no fused multiply-add contraction on either host architecture).
+_CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_lib = None
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64 = ctypes.c_int64
+
+
+def build(force: bool = False, src: str = _SRC, out: str = _LIB_PATH) -> str:
+    """Compile ``q4_oracle.c`` into ``liboracle_q4.so`` next to it."""
+    stale = (not os.path.exists(out)
+             or os.path.getmtime(out) < os.path.getmtime(src))
+    if force or stale:
+        tmp = out + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *_CFLAGS, src, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, out)
+    return out
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _LIB_OVERRIDE:
+                L = ctypes.CDLL(_LIB_OVERRIDE)
+            else:
+                build()
+                L = ctypes.CDLL(_LIB_PATH)
+            L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_f16_to_f32.restype = ctypes.c_float
+            L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_bf16_to_f32.restype = ctypes.c_float
+            L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+            L.orc_f32_to_bf16.restype = ctypes.c_uint16
+            L.orc_q4_code.argtypes = [_u8p, _i64, _i64, _i64]
+            L.orc_q4_code.restype = ctypes.c_int
+            L.orc_q4_zero.argtypes = [_u8p, _i64, _i64, _i64]
+            L.orc_q4_zero.restype = ctypes.c_int
+            L.orc_q4_dequant.argtypes = [_u8p, _u16p, _u8p, _i64, _i64, _i64, _f32p]
+            L.orc_q4_dequant.restype = None
+            L.orc_q4_dequant_bf16.argtypes = [_u8p, _u16p, _u8p, _i64, _i64, _i64, _u16p]
+            L.orc_q4_dequant_bf16.restype = None
+            L.orc_q4_gemv.argtypes = [_u8p, _u16p, _u8p, _f32p, _i64, _i64, _i64,
+                                      _i64, _f32p, _f64p]
+            L.orc_q4_gemv.restype = None
+            L.orc_q4_gemm.argtypes = [_u8p, _u16p, _u8p, _u16p, _i64, _i64, _i64,
+                                      _i64, _f32p, _f64p]
+            L.orc_q4_gemm.restype = None
+            L.orc_f32_gemv.argtypes = [_f32p, _f32p, _i64, _i64, _i64, _f32p, _f64p]
+            L.orc_f32_gemv.restype = None
+            L.orc_sum_f32.argtypes = [_f32p, _i64]
+            L.orc_sum_f32.restype = ctypes.c_double
+            _lib = L
+        return _lib
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+
+def _ptr(a, ctype, offset_elems: int = 0):
+    if a is None:
+        return ctypes.cast(None, ctype)
+    assert a.flags.c_contiguous
+    return ctypes.cast(a.ctypes.data + offset_elems * a.itemsize, ctype)
+
+
+def _check_q4(codes, scales, zeros, K, g):
+    N = codes.shape[0]
+    nb = K // g
+    assert codes.dtype == np.uint8 and codes.shape == (N, K // 2)
+    assert scales.dtype == np.uint16 and scales.shape == (N, nb)
+    if zeros is not None:
+        assert zeros.dtype == np.uint8 and zeros.shape == (N, (nb + 1) // 2)
+    return N, nb
+
+
+def f16_to_f32(h: int) -> float:
+    return lib().orc_f16_to_f32(int(h))
+
+
+def bf16_to_f32(b: int) -> float:
+    return lib().orc_bf16_to_f32(int(b))
+
+
+def f32_to_bf16(f: float) -> int:
+    return lib().orc_f32_to_bf16(ctypes.c_float(float(f)))
+
+
+def q4_code(codes, K: int, n: int, k: int) -> int:
+    return lib().orc_q4_code(_ptr(codes, _u8p), K, n, k)
+
+
+def q4_dequant(codes, scales, zeros, K: int, g: int) -> np.ndarray:
+    N, _ = _check_q4(codes, scales, zeros, K, g)
+    w = np.empty((N, K), np.float32)
+    lib().orc_q4_dequant(_ptr(codes, _u8p), _ptr(scales, _u16p), _ptr(zeros, _u8p),
+                         N, K, g, _ptr(w, _f32p))
+    return w
+
+
+def q4_dequant_bf16(codes, scales, zeros, K: int, g: int) -> np.ndarray:
+    N, _ = _check_q4(codes, scales, zeros, K, g)
+    w = np.empty((N, K), np.uint16)
+    lib().orc_q4_dequant_bf16(_ptr(codes, _u8p), _ptr(scales, _u16p), _ptr(zeros, _u8p),
+                              N, K, g, _ptr(w, _u16p))
+    return w
+
+
+def q4_gemv(codes, scales, zeros, x, g: int):
+    """y[M,N] (float32) and bound[M,N] (float64) for x[M,K] float32."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    N, _ = _check_q4(codes, scales, zeros, K, g)
+    y = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    lib().orc_q4_gemv(_ptr(codes, _u8p), _ptr(scales, _u16p), _ptr(zeros, _u8p),
+                      _ptr(x, _f32p), M, N, K, g, _ptr(y, _f32p), _ptr(b, _f64p))
+    return y, b
+
+
+def q4_gemv_rows(codes, scales, zeros, x, g: int, rows):
+    """The oracle on selected output rows only: y[M, len(rows)], bound."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    N, nb = _check_q4(codes, scales, zeros, K, g)
+    rows = [int(r) for r in rows]
+    y = np.empty((M, len(rows)), np.float32)
+    b = np.empty((M, len(rows)), np.float64)
+    yr = np.empty((M, 1), np.float32)
+    br = np.empty((M, 1), np.float64)
+    zrow = (nb + 1) // 2
+    for j, n in enumerate(rows):
+        lib().orc_q4_gemv(_ptr(codes, _u8p, n * (K // 2)), _ptr(scales, _u16p, n * nb),
+                          None if zeros is None else _ptr(zeros, _u8p, n * zrow),
+                          _ptr(x, _f32p), M, 1, K, g, _ptr(yr, _f32p), _ptr(br, _f64p))
+        y[:, j] = yr[:, 0]
+        b[:, j] = br[:, 0]
+    return y, b
+
+
+def q4_gemv_threaded(codes, scales, zeros, x, g: int, threads: int):
+    """The same oracle, run on `threads` contiguous row slices at once (the C
+    routine is called unchanged on each slice; ctypes releases the GIL)."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    N, nb = _check_q4(codes, scales, zeros, K, g)
+    zrow = (nb + 1) // 2
+    y = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    threads = max(1, min(threads, N))
+    bounds = [N * t // threads for t in range(threads + 1)]
+    parts = [(bounds[t], bounds[t + 1]) for t in range(threads)]
+    outs = [(np.empty((M, n1 - n0), np.float32), np.empty((M, n1 - n0), np.float64))
+            for n0, n1 in parts]
+    L = lib()
+
+    def run(t):
+        n0, n1 = parts[t]
+        L.orc_q4_gemv(_ptr(codes, _u8p, n0 * (K // 2)), _ptr(scales, _u16p, n0 * nb),
+                      None if zeros is None else _ptr(zeros, _u8p, n0 * zrow),
+                      _ptr(x, _f32p), M, n1 - n0, K, g,
+                      _ptr(outs[t][0], _f32p), _ptr(outs[t][1], _f64p))
+
+    ths = [threading.Thread(target=run, args=(t,)) for t in range(threads)]
+    for th in ths:
+        th.start()
+    for th in ths:
+        th.join()
+    for (n0, n1), (yo, bo) in zip(parts, outs):
+        y[:, n0:n1] = yo
+        b[:, n0:n1] = bo
+    return y, b
+
+
+def q4_gemm(codes, scales, zeros, a_bf16, g: int):
+    a_bf16 = np.ascontiguousarray(a_bf16, np.uint16)
+    M, K = a_bf16.shape
+    N, _ = _check_q4(codes, scales, zeros, K, g)
+    c = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    lib().orc_q4_gemm(_ptr(codes, _u8p), _ptr(scales, _u16p), _ptr(zeros, _u8p),
+                      _ptr(a_bf16, _u16p), M, N, K, g, _ptr(c, _f32p), _ptr(b, _f64p))
+    return c, b
+
+
+def q4_gemm_rows(codes, scales, zeros, a_bf16, g: int, m_rows, n_cols):
+    """The oracle on a sample of output elements C[m, n] for m in m_rows and
+    n in n_cols: returns c[len(m_rows), len(n_cols)] and the bound."""
+    a_bf16 = np.ascontiguousarray(a_bf16, np.uint16)
+    M, K = a_bf16.shape
+    N, nb = _check_q4(codes, scales, zeros, K, g)
+    zrow = (nb + 1) // 2
+    c = np.empty((len(m_rows), len(n_cols)), np.float32)
+    b = np.empty((len(m_rows), len(n_cols)), np.float64)
+    cr = np.empty((1, 1), np.float32)
+    br = np.empty((1, 1), np.float64)
+    for i, m in enumerate(m_rows):
+        for j, n in enumerate(n_cols):
+            lib().orc_q4_gemm(_ptr(codes, _u8p, int(n) * (K // 2)),
+                              _ptr(scales, _u16p, int(n) * nb),
+                              None if zeros is None else _ptr(zeros, _u8p, int(n) * zrow),
+                              _ptr(a_bf16, _u16p, int(m) * K), 1, 1, K, g,
+                              _ptr(cr, _f32p), _ptr(br, _f64p))
+            c[i, j] = cr[0, 0]
+            b[i, j] = br[0, 0]
+    return c, b
+
+
+def f32_gemv(W, x):
+    W = np.ascontiguousarray(W, np.float32)
+    x = np.ascontiguousarray(x, np.float32)
+    N, K = W.shape
+    M = x.shape[0]
+    assert x.shape == (M, K)
+    y = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    lib().orc_f32_gemv(_ptr(W, _f32p), _ptr(x, _f32p), M, N, K, _ptr(y, _f32p),
+                       _ptr(b, _f64p))
+    return y, b
+
+
+def f32_gemv_rows(W, x, rows):
+    W = np.ascontiguousarray(W, np.float32)
+    x = np.ascontiguousarray(x, np.float32)
+    N, K = W.shape
+    M = x.shape[0]
+    y = np.empty((M, len(rows)), np.float32)
+    b = np.empty((M, len(rows)), np.float64)
+    yr = np.empty((M, 1), np.float32)
+    br = np.empty((M, 1), np.float64)
+    for j, n in enumerate(rows):
+        lib().orc_f32_gemv(_ptr(W, _f32p, int(n) * K), _ptr(x, _f32p), M, 1, K,
+                           _ptr(yr, _f32p), _ptr(br, _f64p))
+        y[:, j] = yr[:, 0]
+        b[:, j] = br[:, 0]
+    return y, b
+
+
+def sum_f32(buf) -> float:
+    buf = np.ascontiguousarray(buf, np.float32).reshape(-1)
+    return lib().orc_sum_f32(_ptr(buf, _f32p), buf.size)

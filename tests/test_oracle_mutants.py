@@ -1,0 +1,60 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Every mutant below is a plausible slip in the oracle (a swapped nibble, a
+wrong index, a dropped term, a transposed operand, a sign, a rounding rule).
+The test compiles an altered copy of the oracle source into a temporary
+directory, runs the pin suite against it in a child process and expects the
+suite to fail.  The committed oracle is never modified.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+MUTANTS = {
+    "code_nibble_order": ("return (k % 2 == 0) ? (byte & 0x0f) : (byte >> 4);\n}\n\n/* Zero point",
+                          "return (k % 2 == 1) ? (byte & 0x0f) : (byte >> 4);\n}\n\n/* Zero point"),
+    "zero_nibble_order": ("return (b % 2 == 0) ? (byte & 0x0f) : (byte >> 4);",
+                          "return (b % 2 == 1) ? (byte & 0x0f) : (byte >> 4);"),
+    "zero_row_pitch": ("int64_t row_bytes = (nb + 1) / 2;", "int64_t row_bytes = nb / 2 + 1;"),
+    "group_index": ("int64_t b = k / g;", "int64_t b = (k / g) % 2;"),
+    "scale_row": ("return orc_f16_to_f32(scales[n * nb + b]);", "return orc_f16_to_f32(scales[b]);"),
+    "sign": ("return (float)(q - z) * s;", "return (float)(z - q) * s;"),
+    "symmetric_zero": ("        return 8;", "        return 7;"),
+    "dropped_last_term": ("double p = w * (double)x[m * K + k];",
+                          "double p = (k == K - 1) ? 0.0 : w * (double)x[m * K + k];"),
+    "x_transposed": ("double p = w * (double)x[m * K + k];", "double p = w * (double)x[k * M + m];"),
+    "f16_bias": ("v = ldexp((double)(1024 + frac), expo - 25);",
+                 "v = ldexp((double)(1024 + frac), expo - 24);"),
+    "f16_subnormal": ("v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
+    "bf16_ties_away": ("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
+    "gemm_widen": ("double p = w * (double)orc_bf16_to_f32(a_bf16[m * K + k]);",
+                   "double p = w * (double)orc_bf16_to_f32(a_bf16[m * K + k] & 0xfffe);"),
+    "bound_signed": ("                mag += fabs(p);\n            }\n            y[m * N + n] = (float)acc;",
+                     "                mag += p;\n            }\n            y[m * N + n] = (float)acc;"),
+    "f32_control_index": ("double p = (double)W[n * K + k] * (double)x[m * K + k];",
+                          "double p = (double)W[k * N + n] * (double)x[m * K + k];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    src = open(os.path.join(ROOT, "oracle", "q4_oracle.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new, 1)
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated)
+    so_path = str(tmp_path / "libmutant.so")
+    oracle.build(force=True, src=str(c_path), out=so_path)
+    env = dict(os.environ, Q4_ORACLE_LIB=so_path)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

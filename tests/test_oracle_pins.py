@@ -1,0 +1,268 @@
+"""Pins for the CPU oracle, independent of the oracle itself (no GPU needed).
+
+Each test fixes the oracle to something it does not compute itself: the
+hand-worked fixtures under tests/golden/, numpy/torch library routines for the
+number formats and for dense matmul, invariants that follow from the
+definition (gerbil kernel reference, "3. MatMulInt4": value = (nibble - zero)
+* scale, lowest nibble first), and brute force on tiny inputs written from
+unpacked integer arrays.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from conftest import GOLDEN_FILES, golden_x, load_golden, pack_codes, pack_zeros
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# -------------------------------------------------------------- golden values
+
+@pytest.mark.parametrize("name", GOLDEN_FILES)
+def test_hand_worked_examples(name):
+    d = load_golden(name)
+    for kind, y_expect in d["cases"]:
+        x = golden_x(kind, d["K"])
+        y, _ = oracle.q4_gemv(d["codes"], d["scales"], d["zeros"], x, d["group"])
+        np.testing.assert_array_equal(y[0], y_expect)
+    if "dequant" in d:
+        w = oracle.q4_dequant(d["codes"], d["scales"], d["zeros"], d["K"], d["group"])
+        np.testing.assert_array_equal(w[0], d["dequant"])
+
+
+def test_hand_1x32_symmetric_is_zero8():
+    d = load_golden("hand_1x32_g32.txt")
+    for kind, y_expect in d["cases"]:
+        x = golden_x(kind, d["K"])
+        y, _ = oracle.q4_gemv(d["codes"], d["scales"], None, x, d["group"])
+        np.testing.assert_array_equal(y[0], y_expect)
+
+
+def test_hand_examples_through_bf16_matmul():
+    # x = 1 and x = k (k < 256) are exact in bfloat16, so the matmul form of the
+    # oracle must reproduce the same hand-worked values.
+    for name in GOLDEN_FILES:
+        d = load_golden(name)
+        for kind, y_expect in d["cases"]:
+            x = golden_x(kind, d["K"])
+            a = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            c, _ = oracle.q4_gemm(d["codes"], d["scales"], d["zeros"], a, d["group"])
+            np.testing.assert_array_equal(c[0], y_expect)
+
+
+# ------------------------------------------------------------- number formats
+
+def test_fp16_decode_all_patterns_against_numpy():
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = h.view(np.float16).astype(np.float32)
+    got = np.array([oracle.f16_to_f32(v) for v in h], np.float32)
+    finite = np.isfinite(ref)
+    np.testing.assert_array_equal(got[finite].view(np.uint32), ref[finite].view(np.uint32))
+    assert np.all(np.isnan(got[np.isnan(ref)]))
+    assert np.all(got[np.isinf(ref)] == ref[np.isinf(ref)])
+
+
+def test_bf16_rounding_against_torch():
+    r = np.random.default_rng(7)
+    vals = r.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** r.integers(-30, 30, 20000).astype(np.float32)
+    # exact ties at both parities, the largest finite values and zero signs
+    ties = np.array([0x3F808000, 0x3F818000, 0x3F80C000, 0x7F7FFFFF, 0x7F7F8000,
+                     0x00008000, 0x80018000, 0x00000000, 0x80000000, 0x3F7FFFFF],
+                    np.uint32).view(np.float32)
+    vals = np.concatenate([vals[np.isfinite(vals)], ties])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.f32_to_bf16(v) for v in vals], np.uint16)
+    np.testing.assert_array_equal(got, ref)
+    back = np.array([oracle.bf16_to_f32(v) for v in ref[:500]], np.float32)
+    np.testing.assert_array_equal(
+        back, torch.from_numpy(ref[:500].view(np.int16)).view(torch.bfloat16).float().numpy())
+
+
+# ------------------------------------------------ definition via numpy routines
+
+def _random_integer_problem(seed, N, K, g, symmetric):
+    r = np.random.default_rng(seed)
+    q = r.integers(0, 16, size=(N, K))
+    nb = K // g
+    z = np.full((N, nb), 8) if symmetric else r.integers(0, 16, size=(N, nb))
+    s16 = r.uniform(-0.05, 0.05, size=(N, nb)).astype(np.float16)
+    codes = pack_codes(q)
+    zeros = None if symmetric else pack_zeros(z)
+    scales = s16.view(np.uint16).copy()
+    # definition, written in numpy on the unpacked integers (binary64)
+    W = (q - np.repeat(z, g, axis=1)) * np.repeat(s16.astype(np.float64), g, axis=1)
+    return codes, scales, zeros, W
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("N,K_groups", [(1, 1), (3, 3), (5, 7), (17, 2)])
+def test_dequant_and_gemv_match_numpy_definition(g, symmetric, N, K_groups):
+    K = g * K_groups
+    codes, scales, zeros, W = _random_integer_problem(N * 1000 + K + g, N, K, g, symmetric)
+    w = oracle.q4_dequant(codes, scales, zeros, K, g)
+    # (q - z) * s is exact in binary32: the oracle's dequant must equal it bit for bit
+    np.testing.assert_array_equal(w, W.astype(np.float32))
+    assert np.all(W.astype(np.float32).astype(np.float64) == W)
+    x = np.random.default_rng(K).standard_normal((3, K)).astype(np.float32)
+    y, bound = oracle.q4_gemv(codes, scales, zeros, x, g)
+    ref = x.astype(np.float64) @ W.T               # numpy binary64 matmul
+    mag = np.abs(x.astype(np.float64)) @ np.abs(W.T)
+    # both are binary64 sums of the same exact products; after one rounding to
+    # binary32 they may differ by at most one unit in the last place
+    assert np.all(np.abs(y - ref) <= np.spacing(np.abs(ref).astype(np.float32)) + 1e-30)
+    np.testing.assert_allclose(bound, mag, rtol=1e-12, atol=0)
+
+
+def test_bf16_dequant_matches_torch_rounding():
+    codes, scales, zeros, W = _random_integer_problem(3, 4, 256, 64, False)
+    wb = oracle.q4_dequant_bf16(codes, scales, zeros, 256, 64)
+    ref = torch.from_numpy(W.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(wb, ref)
+
+
+def test_f32_gemv_matches_numpy():
+    W = synth.dense_f32(1, 37, 300)
+    x = synth.activations_f32(1, 2, 300)
+    y, bound = oracle.f32_gemv(W, x)
+    ref = x.astype(np.float64) @ W.astype(np.float64).T
+    assert np.all(np.abs(y - ref) <= np.spacing(np.abs(ref).astype(np.float32)) + 1e-30)
+    np.testing.assert_allclose(bound, np.abs(x.astype(np.float64)) @ np.abs(W.astype(np.float64)).T,
+                               rtol=1e-12)
+
+
+def test_sum_matches_fsum():
+    buf = synth.uniform_f32(3, 100003)
+    assert oracle.sum_f32(buf) == math.fsum(buf.astype(np.float64))
+
+
+# ---------------------------------------------------------------- invariants
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_codes_equal_to_zero_point_give_exact_zero(g):
+    r = np.random.default_rng(g)
+    N, K = 9, 5 * g
+    z = r.integers(0, 16, size=(N, K // g))
+    q = np.repeat(z, g, axis=1)
+    scales = r.uniform(0.001, 0.5, size=(N, K // g)).astype(np.float16).view(np.uint16)
+    x = r.standard_normal((2, K)).astype(np.float32) * 100
+    y, bound = oracle.q4_gemv(pack_codes(q), scales, pack_zeros(z), x, g)
+    assert np.all(y == 0.0) and np.all(bound == 0.0)
+
+
+def test_symmetric_equals_explicit_zero_eight():
+    w = synth.q4_weights(11, 19, 384, 64, symmetric=True)
+    z8 = pack_zeros(np.full((19, 6), 8))
+    x = synth.activations_f32(11, 2, 384)
+    y0, _ = oracle.q4_gemv(w.codes, w.scales, None, x, 64)
+    y1, _ = oracle.q4_gemv(w.codes, w.scales, z8, x, 64)
+    np.testing.assert_array_equal(y0, y1)
+
+
+def test_power_of_two_linearity():
+    w = synth.q4_weights(12, 7, 256, 32)
+    x = synth.activations_f32(12, 1, 256)
+    y, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, 32)
+    for j in (-3, 1, 5):
+        yj, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x * np.float32(2.0 ** j), 32)
+        np.testing.assert_array_equal(yj, y * np.float32(2.0 ** j))
+
+
+def test_one_hot_selects_a_column():
+    w = synth.q4_weights(13, 6, 192, 64)
+    W = oracle.q4_dequant(w.codes, w.scales, w.zeros, 192, 64)
+    for k in (0, 1, 63, 64, 127, 191):
+        x = np.zeros((1, 192), np.float32)
+        x[0, k] = 1.0
+        y, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, 64)
+        np.testing.assert_array_equal(y[0], W[:, k])
+
+
+def test_rows_of_x_are_independent():
+    w = synth.q4_weights(14, 10, 256, 128)
+    x = synth.activations_f32(14, 4, 256)
+    y, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, 128)
+    for m in range(4):
+        ym, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x[m:m + 1], 128)
+        np.testing.assert_array_equal(ym[0], y[m])
+
+
+def test_dense_equivalence_inside_the_oracle():
+    w = synth.q4_weights(15, 33, 640, 32)
+    x = synth.activations_f32(15, 3, 640)
+    y, b = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, 32)
+    W = oracle.q4_dequant(w.codes, w.scales, w.zeros, 640, 32)
+    y2, b2 = oracle.f32_gemv(W, x)
+    np.testing.assert_array_equal(y, y2)
+    np.testing.assert_array_equal(b, b2)
+
+
+def test_gemm_equals_gemv_on_widened_activations():
+    w = synth.q4_weights(16, 12, 256, 32)
+    a = synth.activations_bf16(16, 5, 256)
+    c, bc = oracle.q4_gemm(w.codes, w.scales, w.zeros, a, 32)
+    xa = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).float().numpy()
+    y, by = oracle.q4_gemv(w.codes, w.scales, w.zeros, xa, 32)
+    np.testing.assert_array_equal(c, y)
+    np.testing.assert_array_equal(bc, by)
+
+
+def test_sampled_rows_match_full():
+    w = synth.q4_weights(17, 50, 384, 128)
+    x = synth.activations_f32(17, 2, 384)
+    y, b = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, 128)
+    rows = [0, 7, 49]
+    yr, br = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, 128, rows)
+    np.testing.assert_array_equal(yr, y[:, rows])
+    yt, bt = oracle.q4_gemv_threaded(w.codes, w.scales, w.zeros, x, 128, 3)
+    np.testing.assert_array_equal(yt, y)
+    np.testing.assert_array_equal(bt, b)
+
+
+# ---------------------------------------------------------------- brute force
+
+def _naive_python(q, z, s, x, g):
+    """Pure-Python loops over unpacked integers and scale values."""
+    N, K = len(q), len(q[0])
+    out = []
+    for n in range(N):
+        acc = 0.0
+        for k in range(K):
+            acc += (q[n][k] - z[n][k // g]) * s[n][k // g] * x[k]
+        out.append(acc)
+    return out
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+def test_brute_force_every_code_and_zero(g):
+    r = np.random.default_rng(100 + g)
+    cases = [(N, mult) for N in (1, 2, 3) for mult in (1, 2, 3)] + [(1, 16)]
+    seen_q, seen_z = set(), set()
+    for N, mult in cases:
+        K = g * mult
+        q = (np.arange(N * K).reshape(N, K) * 7 + r.integers(0, 16)) % 16
+        if mult == 16:
+            z = np.arange(16).reshape(1, 16)          # every zero value once
+        else:
+            z = r.integers(0, 16, size=(N, mult))
+        seen_q |= set(q.ravel().tolist())
+        seen_z |= set(z.ravel().tolist())
+        s16 = r.uniform(-1, 1, size=(N, mult)).astype(np.float16)
+        x = r.integers(-4, 5, size=K).astype(np.float32)   # small integers
+        ref = _naive_python(q.tolist(), z.tolist(), s16.astype(np.float64).tolist(),
+                            x.astype(np.float64).tolist(), g)
+        y, _ = oracle.q4_gemv(pack_codes(q), s16.view(np.uint16).copy(), pack_zeros(z),
+                              x.reshape(1, K), g)
+        # binary64 sums of at most 2048 terms of size < 2^15 * 2^-24 granularity
+        # are exact, so both sides round the same real number once
+        np.testing.assert_array_equal(y[0], np.array(ref, np.float32))
+    assert seen_q == set(range(16)) and seen_z == set(range(16))
+
+
+def test_code_accessor_nibble_order():
+    codes = np.array([[0x21, 0x43]], np.uint8)
+    assert [oracle.q4_code(codes, 4, 0, k) for k in range(4)] == [1, 2, 3, 4]
