@@ -1,0 +1,200 @@
+"""Python binding of libq4gemv.so, the GB300 int4 weight-streaming GEMV library.
+
+The functions here carry the C ABI's names (include/q4gemv.h) and only
+marshal arguments: torch tensors (or raw integer device addresses) become
+pointers, sizes are read off the tensors when not given, and the current
+torch CUDA stream is passed unless another is named.  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback of any
+kind -- if the shared library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+__all__ = [
+    "Q4Error", "lib", "library_path", "exported_names",
+    "q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
+    "q4gemv_status_string", "q4gemv_last_cuda_error",
+    "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
+    "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
+    "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+HEADER = os.path.join(_ROOT, "include", "q4gemv.h")
+
+Q4_OK, Q4_ERR_INVALID_ARG, Q4_ERR_UNSUPPORTED, Q4_ERR_MISALIGNED, Q4_ERR_CUDA, Q4_ERR_TIMEOUT = range(6)
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libq4gemv.so")
+
+
+class Q4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {q4gemv_status_string(status)} (status {status})"
+        if status == Q4_ERR_CUDA:
+            msg += f" [{q4gemv_last_cuda_error()}]"
+        super().__init__(msg)
+
+
+class _PackInfo(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("k", ctypes.c_int64), ("group", ctypes.c_int32),
+                ("blocks_per_row", ctypes.c_int32), ("codes_row_bytes", ctypes.c_int64),
+                ("codes_bytes", ctypes.c_int64), ("scales_row_bytes", ctypes.c_int64),
+                ("scales_bytes", ctypes.c_int64), ("zeros_row_bytes", ctypes.c_int64),
+                ("zeros_bytes", ctypes.c_int64), ("base_alignment", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    """Load libq4gemv.so (built by gemm_decode_gb300.build); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise OSError(f"{path} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(path)
+            L.q4gemv_pack_info.argtypes = [_i64, _i64, _i32, ctypes.POINTER(_PackInfo)]
+            L.q4gemv_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
+            L.q4gemm_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
+            L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
+            L.q4gemv_status_string.argtypes = [ctypes.c_int]
+            L.q4gemv_status_string.restype = ctypes.c_char_p
+            L.q4gemv_last_cuda_error.argtypes = []
+            L.q4gemv_last_cuda_error.restype = ctypes.c_char_p
+            L.q4_dequant_f32_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]
+            L.q4_dequant_bf16_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]
+            L.vec4_read_probe_run.argtypes = [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32), _vp]
+            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
+                      "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run"):
+                getattr(L, f).restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def exported_names():
+    """Function names declared in include/q4gemv.h."""
+    text = open(HEADER).read()
+    return re.findall(r"^Q4_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _addr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != Q4_OK:
+        raise Q4Error(st, where)
+
+
+def q4gemv_status_string(status: int) -> str:
+    return lib().q4gemv_status_string(int(status)).decode()
+
+
+def q4gemv_last_cuda_error() -> str:
+    return lib().q4gemv_last_cuda_error().decode()
+
+
+def q4gemv_pack_info(N: int, K: int, group: int) -> dict:
+    info = _PackInfo()
+    _check(lib().q4gemv_pack_info(N, K, group, ctypes.byref(info)), "q4gemv_pack_info")
+    return {name: getattr(info, name) for name, _ in _PackInfo._fields_ if name != "reserved"}
+
+
+def _mnk_q4(codes, x, M, N, K):
+    if M is None:
+        M = x.shape[0]
+    if N is None:
+        N = codes.shape[0]
+    if K is None:
+        K = x.shape[1]
+    return int(M), int(N), int(K)
+
+
+def q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M=None, N=None, K=None, group=32,
+               stream=None, check=True) -> int:
+    M, N, K = _mnk_q4(codes, x, M, N, K)
+    st = lib().q4gemv_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(x),
+                          _addr(y), M, N, K, int(group), _stream(stream))
+    if check:
+        _check(st, "q4gemv_run")
+    return st
+
+
+def q4gemm_run(codes, scales_f16, zeros_u4_or_null, a_bf16, c, M=None, N=None, K=None, group=32,
+               stream=None, check=True) -> int:
+    M, N, K = _mnk_q4(codes, a_bf16, M, N, K)
+    st = lib().q4gemm_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(a_bf16),
+                          _addr(c), M, N, K, int(group), _stream(stream))
+    if check:
+        _check(st, "q4gemm_run")
+    return st
+
+
+def f32gemv_run(W, x, y, M=None, N=None, K=None, stream=None, check=True) -> int:
+    M = int(x.shape[0] if M is None else M)
+    N = int(W.shape[0] if N is None else N)
+    K = int(W.shape[1] if K is None else K)
+    st = lib().f32gemv_run(_addr(W), _addr(x), _addr(y), M, N, K, _stream(stream))
+    if check:
+        _check(st, "f32gemv_run")
+    return st
+
+
+def q4_dequant_f32_run(codes, scales_f16, zeros_u4_or_null, w, N=None, K=None, group=32,
+                       stream=None, check=True) -> int:
+    N = int(codes.shape[0] if N is None else N)
+    K = int(codes.shape[1] * 2 if K is None else K)
+    st = lib().q4_dequant_f32_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null),
+                                  _addr(w), N, K, int(group), _stream(stream))
+    if check:
+        _check(st, "q4_dequant_f32_run")
+    return st
+
+
+def q4_dequant_bf16_run(codes, scales_f16, zeros_u4_or_null, wb, N=None, K=None, group=32,
+                        stream=None, check=True) -> int:
+    N = int(codes.shape[0] if N is None else N)
+    K = int(codes.shape[1] * 2 if K is None else K)
+    st = lib().q4_dequant_bf16_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null),
+                                   _addr(wb), N, K, int(group), _stream(stream))
+    if check:
+        _check(st, "q4_dequant_bf16_run")
+    return st
+
+
+def vec4_read_probe_run(buf, nbytes, partial, blocks=0, stream=None, check=True):
+    used = _i32(0)
+    st = lib().vec4_read_probe_run(_addr(buf), int(nbytes), _addr(partial), int(blocks),
+                                   ctypes.byref(used), _stream(stream))
+    if check:
+        _check(st, "vec4_read_probe_run")
+    return used.value

@@ -1,0 +1,174 @@
+// api.cu -- the C ABI of libq4gemv.so: argument checks, status codes, device
+// caches, and dispatch to the kernel launchers.  Every check runs on the host
+// before any launch; a failed check launches nothing.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "q4_common.cuh"
+
+namespace q4 {
+
+namespace {
+thread_local char g_cuda_error[256] = "";
+}
+
+void set_cuda_error(cudaError_t e) {
+    std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+const DeviceInfo &device_info() {
+    static std::mutex mu;
+    static DeviceInfo infos[64];
+    static bool have[64] = {};
+    static DeviceInfo fallback;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fallback;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!have[dev]) {
+        DeviceInfo d;
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaGetLastError();
+        if (d.sms <= 0) d.sms = 1;
+        if (d.smem_optin <= 0) d.smem_optin = 48 * 1024;
+        infos[dev] = d;
+        have[dev] = true;
+    }
+    return infos[dev];
+}
+
+static bool valid_group(int32_t g) { return g == 32 || g == 64 || g == 128; }
+
+// Scalar checks shared by the packed-weight entry points.
+static int check_shape(int64_t M, int64_t N, int64_t K, int32_t group) {
+    if (M < 0 || N < 0 || K < 1 || !valid_group(group) || K % group != 0) return Q4_ERR_INVALID_ARG;
+    if (N > 0x7fffffffLL || K > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
+    return Q4_OK;
+}
+
+int check_q4_args(const void *codes, const void *scales, int64_t N, int64_t K, int32_t group) {
+    (void)N;
+    (void)K;
+    (void)group;
+    if (codes == nullptr || scales == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(codes, 16) || !aligned(scales, 2)) return Q4_ERR_MISALIGNED;
+    return Q4_OK;
+}
+
+}  // namespace q4
+
+using namespace q4;
+
+extern "C" {
+
+const char *q4gemv_status_string(int status) {
+    switch (status) {
+        case Q4_OK: return "ok";
+        case Q4_ERR_INVALID_ARG: return "invalid argument";
+        case Q4_ERR_UNSUPPORTED: return "unsupported size";
+        case Q4_ERR_MISALIGNED: return "misaligned pointer";
+        case Q4_ERR_CUDA: return "CUDA runtime error";
+        case Q4_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+const char *q4gemv_last_cuda_error(void) { return g_cuda_error; }
+
+int q4gemv_pack_info(int64_t N, int64_t K, int32_t group, q4gemv_pack_info_t *out) {
+    if (out == nullptr || N < 0 || K < 1 || !valid_group(group) || K % group != 0) return Q4_ERR_INVALID_ARG;
+    const int64_t nb = K / group;
+    std::memset(out, 0, sizeof *out);
+    out->n = N;
+    out->k = K;
+    out->group = group;
+    out->blocks_per_row = static_cast<int32_t>(nb);
+    out->codes_row_bytes = K / 2;
+    out->codes_bytes = N * (K / 2);
+    out->scales_row_bytes = 2 * nb;
+    out->scales_bytes = N * 2 * nb;
+    out->zeros_row_bytes = (nb + 1) / 2;
+    out->zeros_bytes = N * ((nb + 1) / 2);
+    out->base_alignment = 16;
+    return Q4_OK;
+}
+
+int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const float *x,
+               float *y, int32_t M, int64_t N, int64_t K, int32_t group, void *stream) {
+    int st = check_shape(M, N, K, group);
+    if (st != Q4_OK) return st;
+    if (M == 0 || N == 0) return Q4_OK;
+    if (M > 16) return Q4_ERR_UNSUPPORTED;
+    if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
+    if (x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    return launch_q4gemv(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
+                         static_cast<const uint8_t *>(zeros_u4_or_null), x, y, M, N, static_cast<int>(K), group,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const void *a_bf16,
+               float *c, int32_t M, int64_t N, int64_t K, int32_t group, void *stream) {
+    int st = check_shape(M, N, K, group);
+    if (st != Q4_OK) return st;
+    if (M == 0 || N == 0) return Q4_OK;
+    if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
+    if (a_bf16 == nullptr || c == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(a_bf16, 16) || !aligned(c, 4)) return Q4_ERR_MISALIGNED;
+    return launch_q4gemm(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
+                         static_cast<const uint8_t *>(zeros_u4_or_null), static_cast<const uint16_t *>(a_bf16), c,
+                         M, N, static_cast<int>(K), group, static_cast<cudaStream_t>(stream));
+}
+
+int f32gemv_run(const float *W, const float *x, float *y, int32_t M, int64_t N, int64_t K, void *stream) {
+    if (M < 0 || N < 0 || K < 1) return Q4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return Q4_OK;
+    if (M > 16 || K % 4 != 0 || N > 0x7fffffffLL || K > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
+    if (W == nullptr || x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    return launch_f32gemv(W, x, y, M, N, static_cast<int>(K), static_cast<cudaStream_t>(stream));
+}
+
+int q4_dequant_f32_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, float *w,
+                       int64_t N, int64_t K, int32_t group, void *stream) {
+    int st = check_shape(1, N, K, group);
+    if (st != Q4_OK) return st;
+    if (N == 0) return Q4_OK;
+    if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
+    if (w == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(w, 16)) return Q4_ERR_MISALIGNED;
+    return launch_dequant(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
+                          static_cast<const uint8_t *>(zeros_u4_or_null), w, false, N, static_cast<int>(K), group,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int q4_dequant_bf16_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, uint16_t *wb,
+                        int64_t N, int64_t K, int32_t group, void *stream) {
+    int st = check_shape(1, N, K, group);
+    if (st != Q4_OK) return st;
+    if (N == 0) return Q4_OK;
+    if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
+    if (wb == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(wb, 16)) return Q4_ERR_MISALIGNED;
+    return launch_dequant(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
+                          static_cast<const uint8_t *>(zeros_u4_or_null), wb, true, N, static_cast<int>(K), group,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t blocks, int32_t *blocks_used,
+                        void *stream) {
+    if (buf == nullptr || partial == nullptr || bytes <= 0 || bytes % 16 != 0) return Q4_ERR_INVALID_ARG;
+    if (!aligned(buf, 16) || !aligned(partial, 4)) return Q4_ERR_MISALIGNED;
+    if (blocks <= 0) blocks = device_info().sms * 8;
+    if (blocks_used) *blocks_used = blocks;
+    return launch_read_probe(static_cast<const float4 *>(buf), bytes / 16, partial, blocks,
+                             static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// q4gemv.cu -- host planner for the decode GEMV: picks the M tile, lanes per
+// row, split-K factor and shared-memory size, then launches one kernel.
+#include "q4gemv_kernel.cuh"
+#include "q4gemv_xreg.cuh"
+
+namespace q4 {
+
+template <int MT>
+int launch_q4gemv_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
+extern template int launch_q4gemv_mt<1>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_mt<4>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_mt<8>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_mt<16>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+
+static int rows_per_cta(int MT, int L) {
+    const int R = (MT <= 2) ? 2 : 1;
+    return kGemvWarps * R * (32 / L);
+}
+
+// Plan a launch.  Returns Q4_OK or Q4_ERR_UNSUPPORTED (x slice does not fit).
+//  - M tile MT: M rounded up to a power of two (rows of x beyond M are zero).
+//  - L (lanes per row): as few as keep >= 16 warps per SM busy, since a slot's
+//    lanes broadcast-share each x value read from shared memory.
+//  - S (split-K over a cluster): when even L = 32 leaves fewer than 8 warps
+//    per SM, or when the x slice of the whole row would not fit in shared
+//    memory (large M x K).
+static int plan_gemv(int M, int64_t N, int K, bool asym, GemvPlan &p) {
+    const DeviceInfo &d = device_info();
+    int MT = 1;
+    while (MT < M) MT <<= 1;
+    const int R = (MT <= 2) ? 2 : 1;
+    const int C = K / 32;
+    const int64_t target = static_cast<int64_t>(d.sms) * 16;
+    int L = 4;
+    while (L < 32 && (N * L) / (32 * R) < target) L <<= 1;
+    const int64_t warps = (N * L + 32 * R - 1) / (32 * R);
+    int S = 1;
+    if (warps < target / 2) {
+        int64_t want = (target + warps - 1) / warps;
+        S = static_cast<int>(want < 8 ? want : 8);
+        const int by_len = C / L;  // every split keeps at least L chunks
+        if (S > by_len) S = by_len > 1 ? by_len : 1;
+    }
+    const size_t budget = static_cast<size_t>(d.smem_optin) - 1024;
+    const int rpc = rows_per_cta(MT, L);
+    int CS = 0;
+    size_t smem = 0;
+    for (;;) {
+        CS = (C + S - 1) / S;
+        smem = static_cast<size_t>(MT) * CS * kChunkFloats * sizeof(float) +
+               (S > 1 ? static_cast<size_t>(rpc) * MT * sizeof(float) : 0);
+        if (smem <= budget) break;
+        if (S >= 8) return Q4_ERR_UNSUPPORTED;
+        ++S;
+    }
+    S = (C + CS - 1) / CS;  // drop empty trailing splits
+    smem = static_cast<size_t>(MT) * CS * kChunkFloats * sizeof(float) +
+           (S > 1 ? static_cast<size_t>(rpc) * MT * sizeof(float) : 0);
+    p.MT = MT;
+    p.L = L;
+    p.S = S;
+    p.CS = CS;
+    p.asym = asym;
+    p.smem = smem;
+    p.row_blocks = static_cast<int>((N + rpc - 1) / rpc);
+    return Q4_OK;
+}
+
+int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
+                  const float *x, float *y, int M, int64_t N, int K, int group,
+                  cudaStream_t stream) {
+    {
+        XregPlan xp;
+        XregArgs xa;
+        if (plan_q4gemv_xreg(M, N, K, group, scales, zeros, xp, xa)) {
+            xa.codes = codes;
+            xa.scales = scales;
+            xa.zeros = zeros;
+            xa.x = x;
+            xa.y = y;
+            return launch_q4gemv_xreg(xp, xa, stream);
+        }
+    }
+    GemvPlan p;
+    int st = plan_gemv(M, N, K, zeros != nullptr, p);
+    if (st != Q4_OK) return st;
+    GemvArgs a;
+    a.codes = codes;
+    a.scales = scales;
+    a.zeros = zeros;
+    a.x = x;
+    a.y = y;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.K = K;
+    a.C = K / 32;
+    a.nb = K / group;
+    a.zrow = (a.nb + 1) / 2;
+    a.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
+    a.CS = p.CS;
+    switch (p.MT) {
+        case 1: return launch_q4gemv_mt<1>(p, a, stream);
+        case 2: return launch_q4gemv_mt<2>(p, a, stream);
+        case 4: return launch_q4gemv_mt<4>(p, a, stream);
+        case 8: return launch_q4gemv_mt<8>(p, a, stream);
+        case 16: return launch_q4gemv_mt<16>(p, a, stream);
+        default: return Q4_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace q4

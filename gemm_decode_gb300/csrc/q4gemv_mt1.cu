@@ -1,0 +1,6 @@
+// GEMV kernel instantiations for an M tile of 1 row(s) of x.
+#include "q4gemv_launch.cuh"
+
+namespace q4 {
+template int launch_q4gemv_mt<1>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+}  // namespace q4

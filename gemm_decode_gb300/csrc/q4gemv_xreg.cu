@@ -1,0 +1,494 @@
+// q4gemv_xreg.cu -- the streaming int4 GEMV for 1 <= M <= 2 on CUDA cores.
+//
+// Computes y[m][n] = sum_k (q[n][k] - z[n][k/g]) * s[n][k/g] * x[m][k]
+// (gerbil GPU-engine kernel reference, "3. MatMulInt4": "Computes",
+// "Dequantization"; MatMulNBits layout per the Refractometer page's
+// "b) q4 GEMV" sweep).
+//
+// Work decomposition.  A row of codes is C = K/32 chunks of 16 bytes (32
+// codes, inside one group).  Every thread owns ONE chunk position c for the
+// whole launch and keeps the matching 32 values of x in registers; rows stream
+// past it.  A CTA has CTp threads per row (CTp = the chunk positions of this
+// CTA's K-slice, rounded up to a warp multiple when at least 32) times RG rows,
+// so one "row group" of RG rows is covered by one pass of all threads, and an
+// iteration covers U row groups.  Each thread copies its own 16-byte code
+// chunk, scale word and zero-point word of future iterations into a private
+// shared-memory ring with cp.async (D slots), so loads run far ahead of the
+// arithmetic without holding registers and without CTA-wide barriers.  The
+// per-row partial sums go to shared memory and are reduced every RB
+// iterations.  Long rows are split over S CTAs of a thread-block cluster whose
+// partials are added in rank order through distributed shared memory.
+//
+// Arithmetic.  x is represented per 32-element chunk as 24-bit integers
+// m_k = round(x_k * 2^(22-E)) with E the exponent of the chunk's largest |x|
+// (|m_k| <= 2^22), split into three byte planes.  With the codes unpacked to
+// bytes (even k, odd k), dp4a forms sum_k q_k * plane_b(k) exactly in int32 for
+// each plane b; the zero point enters exactly as - z * sum_k plane_b(k).  The
+// three plane sums are combined in binary32 and scaled once by s * 2^(E-22).
+// Every integer step is exact; the only approximations are x's 24-bit chunk
+// representation (absolute error <= 2^-23 * 2^E per element) and binary32
+// rounding of the per-chunk and per-row sums.  Codes equal to their zero point
+// contribute exactly 0.
+#include <cooperative_groups.h>
+
+#include "q4_common.cuh"
+#include "q4gemv_xreg.cuh"
+
+namespace q4 {
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int kPlaneWords = 28;  // 24 plane words + S_lo + S_hi + (unused) + chunk scale 2^(E-22)
+
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// Encode one 32-element chunk of x (one warp, lane i holds element i) into the
+// plane layout: for word w (elements 8w..8w+7) and plane b, word 6w+2b holds
+// the b-th byte of m for the even elements 8w, 8w+2, 8w+4, 8w+6 and word
+// 6w+2b+1 that of the odd elements.  Plane 2 is the signed top byte.
+__device__ void encode_chunk(float v, uint32_t *pw, int lane) {
+    float mx = fabsf(v);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // mx in [2^(E-1), 2^E): E from the binary32 exponent field; tiny chunks clamp.
+    int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 126;
+    if (E < -100) E = -100;
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + 22 - E) << 23);   // 2^(22-E)
+    const int m = __float2int_rn(v * up);                                          // |m| <= 2^22
+    const int b0 = m & 0xFF, b1 = (m >> 8) & 0xFF, b2 = m >> 16;                   // b2 signed
+    const int w = lane >> 3, q = (lane & 7) >> 1, odd = lane & 1;
+    // gather the four bytes of each plane word with shuffles: word (w, parity) takes
+    // lanes 8w + 2q + parity for q = 0..3.
+    uint32_t out0 = 0, out1 = 0, out2 = 0;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const int src = (lane & ~7) + 2 * qq + odd;
+        out0 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b0, src) & 0xFF) << (8 * qq);
+        out1 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b1, src) & 0xFF) << (8 * qq);
+        out2 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b2, src) & 0xFF) << (8 * qq);
+    }
+    if (q == 0) {  // lanes 8w and 8w+1 write the even/odd words of word w
+        pw[6 * w + 0 + odd] = out0;
+        pw[6 * w + 2 + odd] = out1;
+        pw[6 * w + 4 + odd] = out2;
+    }
+    int s0 = b0, s1 = b1, s2 = b2;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    if (lane == 0) {
+        pw[24] = static_cast<uint32_t>(s1 * 256 + s0);
+        pw[25] = static_cast<uint32_t>(s2);
+        pw[26] = 0u;
+        pw[27] = __float_as_uint(__uint_as_float(static_cast<uint32_t>(127 + E - 22) << 23));  // 2^(E-22)
+    }
+}
+
+struct Planes {
+    uint32_t p[24];
+    int s_lo, s_hi;
+    float f;
+};
+
+// Exact integer dot product of one 16-byte chunk with one x chunk, minus the
+// zero-point term, returned as the binary32 value sum_k (q_k - z) m_k.
+__device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes &P) {
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    int a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu;          // codes of even k, one per byte
+        const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;   // codes of odd k
+        a0 = dp4a_uu(lo, P.p[6 * w + 0], a0);
+        a0 = dp4a_uu(hi, P.p[6 * w + 1], a0);
+        a1 = dp4a_uu(lo, P.p[6 * w + 2], a1);
+        a1 = dp4a_uu(hi, P.p[6 * w + 3], a1);
+        a2 = dp4a_us(lo, P.p[6 * w + 4], a2);
+        a2 = dp4a_us(hi, P.p[6 * w + 5], a2);
+    }
+    const int lo = a1 * 256 + a0 - z * P.s_lo;   // planes 0 and 1: |lo| < 2^31
+    const int hi = a2 - z * P.s_hi;               // plane 2
+    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
+}
+
+}  // namespace
+
+template <int MT, int U, int D, bool ASYM, bool WARPRED>
+__global__ void __launch_bounds__(512)
+q4gemv_xreg_kernel(const XregArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int T = blockDim.x;
+    const int tid = threadIdx.x;
+    const int CTp = a.CTp;
+    const int r = tid / CTp;            // row within a row group
+    const int cl = tid - r * CTp;       // chunk position within this CTA's K-slice
+    const int split = static_cast<int>(blockIdx.y);
+    const int c = split * a.CT + cl;    // chunk position in the row
+    const bool active = (cl < a.CT) && (c < a.C);
+    const int RG = a.RG;
+    const int rows_it = U * RG;         // rows per iteration
+    const int RB = a.RB;
+
+    // shared memory carve-up
+    uint32_t *planes = reinterpret_cast<uint32_t *>(smem);                       // [MT][CTp][28]
+    float *red = reinterpret_cast<float *>(smem + a.off_red);                    // [rows_b][MT][red_ld]
+    unsigned char *ring = smem + a.off_ring;                                     // [D][slot]
+    float *ysum = reinterpret_cast<float *>(smem + a.off_ysum);                  // [rows_b][MT] (split only)
+
+    // ---- this CTA's super groups (contiguous) ----
+    const int gsz = static_cast<int>(gridDim.x);
+    const int g_begin = static_cast<int>(static_cast<int64_t>(a.nsuper) * blockIdx.x / gsz);
+    const int g_end = static_cast<int>(static_cast<int64_t>(a.nsuper) * (blockIdx.x + 1) / gsz);
+    const int ng = g_end - g_begin;
+
+    // ---- per-thread streams ----
+    const int grp = c >> a.gshift;
+    const int64_t row0 = static_cast<int64_t>(g_begin) * rows_it + r;
+    const int64_t pitch = a.K / 2;
+    const unsigned char *gc = a.codes + row0 * pitch + static_cast<int64_t>(c) * 16;
+    const int64_t se = row0 * a.nb + grp;                       // scale element index
+    const unsigned char *gs = reinterpret_cast<const unsigned char *>(a.scales) + (se & ~1LL) * 2;
+    const int ssh = static_cast<int>(se & 1) * 16;              // same for every row of this thread
+    const int64_t ze = row0 * a.zrow + (grp >> 1);              // zero-point byte index
+    const unsigned char *gz = a.zeros + (ASYM ? (ze & ~3LL) : 0);
+    const int zsh = static_cast<int>(ze & 3) * 8 + (grp & 1) * 4;
+    const int64_t step_c = static_cast<int64_t>(rows_it) * pitch;
+    const int64_t step_s = static_cast<int64_t>(rows_it) * a.nb * 2;
+    const int64_t step_z = static_cast<int64_t>(rows_it) * a.zrow;
+    const int64_t rg_c = static_cast<int64_t>(RG) * pitch, rg_s = static_cast<int64_t>(RG) * a.nb * 2,
+                  rg_z = static_cast<int64_t>(RG) * a.zrow;
+    const uint32_t slot_bytes = static_cast<uint32_t>(U * T * (ASYM ? 24 : 20));
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t my_c = ring_s + tid * 16;
+    const uint32_t my_s = ring_s + U * T * 16 + tid * 4;
+    const uint32_t my_z = my_s + U * T * 4;
+
+    int issued = 0;
+    auto issue_next = [&]() {
+        if (active) {
+            const uint32_t so = static_cast<uint32_t>(issued % D) * slot_bytes;
+            const int64_t rb = static_cast<int64_t>(g_begin + issued) * rows_it;   // first row of the iteration
+            if (rb + rows_it <= a.N) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    cp_async16(my_c + so + u * T * 16, gc + u * rg_c);
+                    cp_async4(my_s + so + u * T * 4, gs + u * rg_s);
+                    if (ASYM) cp_async4(my_z + so + u * T * 4, gz + u * rg_z);
+                }
+            } else {
+                // Tail: a row past N reads row n - RG*k <= N-1 instead (same alignment
+                // class, so the per-thread shifts stay valid); its result is discarded.
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    int64_t n = rb + u * RG + r;
+                    int64_t back = 0;
+                    if (n >= a.N) back = (n - (a.N - 1) + RG - 1) / RG;
+                    const int64_t j = u - back;   // row groups from this iteration's first (may be < 0)
+                    cp_async16(my_c + so + u * T * 16, gc + j * rg_c);
+                    cp_async4(my_s + so + u * T * 4, gs + j * rg_s);
+                    if (ASYM) cp_async4(my_z + so + u * T * 4, gz + j * rg_z);
+                }
+            }
+        }
+        gc += step_c;
+        gs += step_s;
+        gz += ASYM ? step_z : 0;
+        ++issued;
+    };
+
+#pragma unroll 1
+    for (int p = 0; p < D - 1; ++p) {
+        if (p < ng) issue_next();
+        cp_commit();
+    }
+
+    // ---- encode this CTA's x slice into planes (one warp per chunk and row of x) ----
+    {
+        const int warp = tid >> 5, lane = tid & 31, nwarps = T >> 5;
+        for (int i = warp; i < MT * CTp; i += nwarps) {
+            const int m = i / CTp, ci = i - m * CTp;
+            const int cc = split * a.CT + ci;
+            float v = 0.0f;
+            if (m < a.M && ci < a.CT && cc < a.C) v = a.x[static_cast<int64_t>(m) * a.K + cc * 32 + lane];
+            encode_chunk(v, planes + (m * CTp + ci) * kPlaneWords, lane);
+        }
+    }
+    __syncthreads();
+    Planes P[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        const uint32_t *pw = planes + (m * CTp + cl) * kPlaneWords;
+#pragma unroll
+        for (int i = 0; i < 24; ++i) P[m].p[i] = pw[i];
+        P[m].s_lo = static_cast<int>(pw[24]);
+        P[m].s_hi = static_cast<int>(pw[25]);
+        P[m].f = __uint_as_float(pw[27]);
+    }
+
+    const int red_ld = a.red_ld;
+    const uint4 *rc_t = reinterpret_cast<const uint4 *>(ring) + tid;
+    const uint32_t *rs_t = reinterpret_cast<const uint32_t *>(ring + U * T * 16) + tid;
+    const uint32_t *rz_t = rs_t + U * T;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int nsplit = static_cast<int>(gridDim.y);
+
+    for (int b0 = 0; b0 < ng; b0 += RB) {
+        const int nbat = min(RB, ng - b0);
+#pragma unroll 1
+        for (int bi = 0; bi < nbat; ++bi) {
+            if (issued < ng) issue_next();
+            cp_commit();
+            cp_wait<D - 1>();
+            const uint32_t so = static_cast<uint32_t>((b0 + bi) % D) * slot_bytes;
+            const uint4 *rc = reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(rc_t) + so);
+            const uint32_t *rs = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rs_t) + so);
+            const uint32_t *rz = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rz_t) + so);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float part[MT];
+                if (active) {
+                    const uint4 cw = rc[u * T];
+                    const uint32_t sw = rs[u * T];
+                    const int z = ASYM ? static_cast<int>((rz[u * T] >> zsh) & 0xFu) : 8;
+                    const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sw >> ssh)));
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) part[m] = (s * P[m].f) * chunk_dot(cw, z, P[m]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) part[m] = 0.0f;
+                }
+                const int row_b = (bi * U + u) * RG + r;
+                if (WARPRED) {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) {
+                        float v = part[m];
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                        if ((cl & 31) == 0) red[(row_b * MT + m) * red_ld + (cl >> 5)] = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) red[(row_b * MT + m) * red_ld + cl] = part[m];
+                }
+            }
+        }
+        __syncthreads();
+        // ---- per-row sums of this batch ----
+        const int nrows = nbat * rows_it;
+        const int nterms = WARPRED ? (CTp >> 5) : CTp;
+        const int64_t first_row = static_cast<int64_t>(g_begin + b0) * rows_it;
+        for (int i = tid; i < nrows * MT; i += T) {
+            const float *src = red + i * red_ld;
+            float v = 0.0f;
+            for (int q = 0; q < nterms; ++q) v += src[q];
+            const int rr = i / MT, m = i - rr * MT;
+            if (nsplit == 1) {
+                const int64_t n = first_row + rr;
+                if (n < a.N && m < a.M) a.y[static_cast<int64_t>(m) * a.N + n] = v;
+            } else {
+                ysum[i] = v;
+            }
+        }
+        if (nsplit > 1) {
+            // add the K-slices of the cluster in rank order
+            cluster.sync();
+            const int rank = static_cast<int>(cluster.block_rank());
+            for (int i = rank * T + tid; i < nrows * MT; i += nsplit * T) {
+                float v = 0.0f;
+                for (int q = 0; q < nsplit; ++q) v += cluster.map_shared_rank(ysum, q)[i];
+                const int rr = i / MT, m = i - rr * MT;
+                const int64_t n = first_row + rr;
+                if (n < a.N && m < a.M) a.y[static_cast<int64_t>(m) * a.N + n] = v;
+            }
+            cluster.sync();
+        } else {
+            __syncthreads();
+        }
+    }
+    cp_wait<0>();
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int MT, int U, int D, bool ASYM, bool WARPRED>
+static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
+    auto kern = q4gemv_xreg_kernel<MT, U, D, ASYM, WARPRED>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             device_info().smem_optin);
+        if (e == cudaSuccess && p.S > 1)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.S > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(p.S);
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    // Persistent grid: as many CTAs (clusters) as can be resident at once.
+    int resident = 0;
+    if (p.S > 1) {
+        cfg.gridDim = dim3(1, static_cast<unsigned>(p.S), 1);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+    } else {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, p.threads, p.smem);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        resident = per_sm * device_info().sms;
+    }
+    if (resident < 1) return Q4_ERR_UNSUPPORTED;
+    const int grid_x = resident < a.nsuper ? resident : a.nsuper;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(p.S), 1);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+template <int MT, int U, int D>
+static int launch_flags(const XregPlan &p, const XregArgs &a, cudaStream_t s) {
+    if (p.asym)
+        return p.warpred ? launch_one<MT, U, D, true, true>(p, a, s) : launch_one<MT, U, D, true, false>(p, a, s);
+    return p.warpred ? launch_one<MT, U, D, false, true>(p, a, s) : launch_one<MT, U, D, false, false>(p, a, s);
+}
+
+int launch_q4gemv_xreg(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
+    if (p.MT == 1) return launch_flags<1, kXregU, kXregD>(p, a, stream);
+    if (p.MT == 2) return launch_flags<2, kXregU, kXregD>(p, a, stream);
+    return Q4_ERR_UNSUPPORTED;
+}
+
+// Plan: threads per row CTp, rows per group RG, split S, batch RB, persistent grid.
+// Returns false when the shape does not suit this kernel (the caller then uses the
+// general kernel).
+bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, const void *zeros,
+                      XregPlan &p, XregArgs &a) {
+    if (M < 1 || M > 2) return false;
+    const int C = K / 32;
+    const int nb = K / group;
+    const int zrow = (nb + 1) / 2;
+    const bool asym = zeros != nullptr;
+    // word-granular scale / zero-point reads: 4-byte aligned bases, no word past the end
+    if (!aligned(scales, 4) || (asym && !aligned(zeros, 4))) return false;
+    if ((N * nb) % 2 != 0) return false;
+    if (asym && (N * zrow) % 4 != 0) return false;
+    const DeviceInfo &d = device_info();
+    const int MT = M;
+    // K-slices: at most 256 chunk positions per CTA
+    int S = (C + 255) / 256;
+    if (S > 8) return false;
+    int CT = (C + S - 1) / S;
+    int CTp, RG;
+    if (CT >= 32) {
+        CTp = (CT + 31) / 32 * 32;
+        RG = 4;
+        while (CTp * RG > 512 && RG > 1) RG >>= 1;
+    } else {
+        // rows straddle warps: CTp * RG must be a warp multiple
+        CTp = CT;
+        RG = 4;
+        while ((CTp * RG) % 32 != 0) RG += 4;
+        if (CTp * RG > 512) return false;
+    }
+    // the per-thread shift constants need RG rows to advance whole 4-byte words
+    if (asym && (static_cast<int64_t>(RG) * zrow) % 4 != 0) return false;
+    if ((static_cast<int64_t>(RG) * nb) % 2 != 0) return false;
+    const int T = CTp * RG;
+    const int rows_it = kXregU * RG;
+    if (N < rows_it) return false;
+    const bool warpred = CTp >= 32;
+    const int red_ld = warpred ? CTp / 32 : CTp + 1;
+    // batch size: about 128 rows per reduction, within shared memory
+    int RB = 128 / rows_it;
+    if (RB < 1) RB = 1;
+    auto smem_for = [&](int rb) {
+        size_t planes_b = static_cast<size_t>(MT) * CTp * kPlaneWords * 4;
+        size_t off_red = (planes_b + 15) / 16 * 16;
+        size_t red_b = static_cast<size_t>(rb) * rows_it * MT * red_ld * 4;
+        size_t off_ring = (off_red + red_b + 15) / 16 * 16;
+        size_t ring_b = static_cast<size_t>(kXregD) * kXregU * T * (asym ? 24 : 20);
+        size_t off_ysum = off_ring + ring_b;
+        size_t ysum_b = S > 1 ? static_cast<size_t>(rb) * rows_it * MT * 4 : 0;
+        a.off_red = static_cast<int>(off_red);
+        a.off_ring = static_cast<int>(off_ring);
+        a.off_ysum = static_cast<int>(off_ysum);
+        return off_ysum + ysum_b;
+    };
+    size_t smem = smem_for(RB);
+    const size_t budget = static_cast<size_t>(d.smem_optin) - 1024;
+    while (smem > budget && RB > 1) smem = smem_for(--RB);
+    if (smem > budget) return false;
+    const int64_t nsuper = (N + rows_it - 1) / rows_it;
+    p.MT = MT;
+    p.S = S;
+    p.threads = T;
+    p.grid_x = 0;
+    p.smem = smem;
+    p.asym = asym;
+    p.warpred = warpred;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.K = K;
+    a.C = C;
+    a.nb = nb;
+    a.zrow = zrow;
+    a.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
+    a.CT = CT;
+    a.CTp = CTp;
+    a.RG = RG;
+    a.RB = RB;
+    a.red_ld = red_ld;
+    a.nsuper = static_cast<int>(nsuper);
+    return true;
+}
+
+}  // namespace q4

@@ -1,0 +1,140 @@
+/*
+ * q4gemv.h -- C ABI of the GB300 (sm_103a) int4 weight-streaming GEMV library
+ * (libq4gemv.so).
+ *
+ * The operation (gerbil GPU-engine kernel reference, docs/gpu-engine/kernels.md,
+ * section "3. MatMulInt4", "Computes" and "Dequantization"):
+ *
+ *     y[m][n] = sum_k  w[n][k] * x[m][k],     w[n][k] = (q[n][k] - z[n][k/g]) * s[n][k/g]
+ *
+ * in the MatMulNBits weight layout (Refractometer page, sweep "b) q4 GEMV"):
+ *
+ *   codes   uint8  [N][K/2]           4-bit codes q, two per byte; the even k is the
+ *                                     low nibble ("INT4 Packing": lowest nibble first)
+ *   scales  fp16   [N][K/g]           one scale per group of g consecutive k in a row
+ *   zeros   uint8  [N][ceil(K/g/2)]   4-bit zero points, two per byte, even group in the
+ *                                     low nibble; an odd group count leaves a pad nibble
+ *                                     (ignored).  NULL selects the symmetric variant,
+ *                                     zero = 8 for every group.
+ *
+ * Conventions for every call below:
+ *   - All arrays are row-major and contiguous.  Pointers marked "device" must point to
+ *     device memory (or memory the device can address); the library never dereferences
+ *     them on the host.  The caller allocates and owns every buffer; the library keeps
+ *     no pointer after a call returns and allocates no device memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Calls are asynchronous: they enqueue kernels and return; they never synchronise.
+ *   - Arguments are checked on the host before anything is launched.  A failed check
+ *     returns a status below and launches nothing.  Outputs are fully overwritten on
+ *     success (no accumulation into them, no memset needed).
+ *   - M == 0 or N == 0 is an empty problem: Q4_OK, nothing launched, pointers unused.
+ *   - Sizes: 1 <= K, K % g == 0, g in {32, 64, 128}.
+ *   - Alignment: codes, x, W, a_bf16 and probe buffers 16-byte aligned; scales 2-byte,
+ *     y / c 4-byte; otherwise Q4_ERR_MISALIGNED.
+ *   - A launch failure reported by the CUDA runtime returns Q4_ERR_CUDA (the runtime's
+ *     error string is available from q4gemv_last_cuda_error()).
+ */
+#ifndef Q4GEMV_H
+#define Q4GEMV_H
+
+#include <stdint.h>
+
+/* Symbols of this header are the library's only exported (default-visibility) names. */
+#if defined(__GNUC__)
+#define Q4_API __attribute__((visibility("default")))
+#else
+#define Q4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    Q4_OK = 0,
+    Q4_ERR_INVALID_ARG = 1, /* null pointer, non-positive K, bad group, K % g != 0 */
+    Q4_ERR_UNSUPPORTED = 2, /* valid but outside what a kernel serves (e.g. M > 16 in q4gemv_run) */
+    Q4_ERR_MISALIGNED = 3,  /* a pointer violates the alignment stated above */
+    Q4_ERR_CUDA = 4,        /* the CUDA runtime refused or failed a launch */
+    Q4_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (tensor-core path) */
+} q4_status;
+
+/* Byte sizes of one packed weight matrix (all byte counts). */
+typedef struct {
+    int64_t n, k;
+    int32_t group;
+    int32_t blocks_per_row;    /* nb = K / group                         */
+    int64_t codes_row_bytes;   /* K / 2                                  */
+    int64_t codes_bytes;       /* N * K / 2                              */
+    int64_t scales_row_bytes;  /* 2 * nb                                 */
+    int64_t scales_bytes;      /* N * 2 * nb                             */
+    int64_t zeros_row_bytes;   /* ceil(nb / 2)                           */
+    int64_t zeros_bytes;       /* N * ceil(nb / 2)                       */
+    int32_t base_alignment;    /* 16: required alignment of codes / x / A */
+    int32_t reserved;
+} q4gemv_pack_info_t;
+
+/* Fill *out with the packed sizes of an N x K matrix of group g.  Host only; no CUDA
+ * call.  Q4_ERR_INVALID_ARG for out == NULL, N < 0, K < 1, g not in {32,64,128} or
+ * K % g != 0. */
+Q4_API int q4gemv_pack_info(int64_t N, int64_t K, int32_t group, q4gemv_pack_info_t *out);
+
+/* Decode-time int4 GEMV on CUDA cores, 1 <= M <= 16 (M > 16: Q4_ERR_UNSUPPORTED).
+ *   codes, scales_f16, zeros_u4_or_null : device, layout above
+ *   x : device float [M][K];  y : device float [M][N] (written, not accumulated)
+ * Kernel: codes streamed with 128-bit loads, exact in-register nibble decode, x held in
+ * shared memory, f32 accumulation, warp-shuffle reduction, split-K over a thread-block
+ * cluster (distributed shared memory) for long K / few rows. */
+Q4_API int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+               const float *x, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
+               void *stream);
+
+/* Prefill-shaped int4 matmul on the tensor cores (tcgen05, bf16 operands, f32
+ * accumulate in tensor memory), any M >= 1 (tiles of 128 rows; a partial tile is
+ * padded and masked).
+ *   a_bf16 : device bfloat16 [M][K] activations;  c : device float [M][N]
+ * Each weight is dequantised exactly to f32 and rounded once to bf16 (nearest-even)
+ * before the MMA.  Q4_ERR_TIMEOUT if a bounded pipeline wait expired (the kernel then
+ * stops; c is unspecified). */
+Q4_API int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+               const void *a_bf16, float *c, int32_t M, int64_t N, int64_t K, int32_t group,
+               void *stream);
+
+/* Dense f32 GEMV control (cera wgpu_gemv_bench.rs, the F32 row kept in the table as the
+ * harness control): y[m][n] = sum_k W[n][k] * x[m][k], 1 <= M <= 16, K % 4 == 0.
+ *   W : device float [N][K];  x : device float [M][K];  y : device float [M][N] */
+Q4_API int f32gemv_run(const float *W, const float *x, float *y, int32_t M, int64_t N, int64_t K,
+                void *stream);
+
+/* Text for a status code (static storage, never NULL). */
+Q4_API const char *q4gemv_status_string(int status);
+
+/* The CUDA runtime's error string from the most recent Q4_ERR_CUDA on this thread, or
+ * "" (static/thread storage, never NULL). */
+Q4_API const char *q4gemv_last_cuda_error(void);
+
+/* ---- test and measurement exports (not part of the GEMV API proper) ---------------- */
+
+/* Write the dequantised matrix w[N][K] = (q - z) * s as float, with the same in-register
+ * decode the GEMV kernels use (exact, so it must equal the CPU definition bit for bit). */
+Q4_API int q4_dequant_f32_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                       float *w, int64_t N, int64_t K, int32_t group, void *stream);
+
+/* Write the bfloat16 weights wb[N][K] the tensor-core path feeds to its MMA
+ * (round-to-nearest-even of the exact f32 weight), as uint16 bit patterns. */
+Q4_API int q4_dequant_bf16_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                        uint16_t *wb, int64_t N, int64_t K, int32_t group, void *stream);
+
+/* Read-bandwidth probe (webgpu-bench README "read-bandwidth"; Refractometer
+ * "a) bandwidth"): `blocks` CTAs stream `bytes` (a multiple of 16, 16-byte aligned) of
+ * float data with 128-bit loads folded by addition; partial[b] receives CTA b's sum.
+ * blocks <= 0 picks one CTA per SM times the resident count.  Returns the CTA count
+ * used through *blocks_used (may be NULL). */
+Q4_API int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t blocks,
+                        int32_t *blocks_used, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4GEMV_H */

@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load, export every function include/q4gemv.h declares, size
+packed matrices correctly and reject bad arguments before any launch.  The
+rejected calls below fail a check that runs before the first CUDA call, so no
+pointer here is ever dereferenced.
+"""
+import ctypes
+import os
+
+import pytest
+
+import gemm_decode_gb300 as q4
+from gemm_decode_gb300 import build as q4build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    q4build.build()
+    return q4.lib()
+
+
+def test_library_exports_every_declared_function(L):
+    names = q4.exported_names()
+    assert set(names) >= {"q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
+                          "q4gemv_status_string"}
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in q4gemv.h but not exported"
+
+
+def test_only_declared_functions_are_exported(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", q4.library_path()],
+                         capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(q4.exported_names())
+
+
+def test_library_links_no_oracle():
+    import subprocess
+    out = subprocess.run(["nm", "-D", q4.library_path()], capture_output=True, text=True).stdout
+    assert "orc_" not in out
+
+
+def test_pack_info_sizes(L):
+    info = q4.q4gemv_pack_info(151936, 896, 32)
+    assert info["blocks_per_row"] == 28
+    assert info["codes_bytes"] == 151936 * 448 == 68067328
+    assert info["scales_bytes"] == 8508416
+    assert info["zeros_row_bytes"] == 14 and info["zeros_bytes"] == 2127104
+    assert info["base_alignment"] == 16
+    odd = q4.q4gemv_pack_info(4096, 896, 128)       # 7 groups: a pad nibble
+    assert odd["blocks_per_row"] == 7 and odd["zeros_row_bytes"] == 4
+    big = q4.q4gemv_pack_info(128256, 4096, 128)
+    assert big["codes_bytes"] + big["scales_bytes"] + big["zeros_bytes"] == 272928768
+
+
+@pytest.mark.parametrize("N,K,g", [(-1, 64, 32), (4, 0, 32), (4, 96, 48), (4, 80, 32), (4, 64, 16)])
+def test_pack_info_rejects(L, N, K, g):
+    info = q4._PackInfo()
+    assert L.q4gemv_pack_info(N, K, g, ctypes.byref(info)) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemv_pack_info(4, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+
+
+A = 0x100000  # an aligned address that is never dereferenced (every call fails first)
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert q4.q4gemv_status_string(s)
+    assert q4.q4gemv_status_string(99) == "unknown status"
+
+
+def test_gemv_argument_checks(L):
+    r = L.q4gemv_run
+    ok_shape = (4, 64, 64, 32)
+    # bad scalars
+    assert r(A, A, None, A, A, -1, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, 1, 64, 0, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, 1, 64, 96, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, 1, 64, 64, 48, None) == q4.Q4_ERR_INVALID_ARG
+    # empty problems are no-ops, whatever the pointers
+    assert r(None, None, None, None, None, 0, 64, 64, 32, None) == q4.Q4_OK
+    assert r(None, None, None, None, None, 3, 0, 64, 32, None) == q4.Q4_OK
+    # M beyond the CUDA-core kernel
+    assert r(A, A, None, A, A, 17, 64, 64, 32, None) == q4.Q4_ERR_UNSUPPORTED
+    # null and misaligned pointers
+    assert r(None, A, None, A, A, 1, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, None, None, A, A, 1, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, None, A, 1, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, None, 1, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A + 8, A, None, A, A, 1, 64, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert r(A, A + 1, None, A, A, 1, 64, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert r(A, A, None, A + 4, A, 1, 64, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert r(A, A, None, A, A + 2, 1, 64, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    del ok_shape
+
+
+def test_gemm_and_control_argument_checks(L):
+    g = L.q4gemm_run
+    assert g(A, A, None, A, A, 1, 64, 100, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert g(A, A, None, None, A, 128, 64, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert g(A, A, None, A + 2, A, 128, 64, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert g(None, None, None, None, None, 0, 64, 64, 32, None) == q4.Q4_OK
+    f = L.f32gemv_run
+    assert f(A, A, A, 17, 64, 64, None) == q4.Q4_ERR_UNSUPPORTED
+    assert f(A, A, A, 1, 64, 66, None) == q4.Q4_ERR_UNSUPPORTED
+    assert f(None, A, A, 1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert f(A + 4, A, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED
+    assert f(None, None, None, 0, 64, 64, None) == q4.Q4_OK
+    p = L.vec4_read_probe_run
+    assert p(A, 24, A, 1, None, None) == q4.Q4_ERR_INVALID_ARG
+    assert p(A + 8, 32, A, 1, None, None) == q4.Q4_ERR_MISALIGNED
+    d = L.q4_dequant_f32_run
+    assert d(A, A, None, A + 4, 4, 64, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert d(A, A, None, None, 4, 64, 32, None) == q4.Q4_ERR_INVALID_ARG
+
+
+def test_binding_raises_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(q4, "_lib", None)
+    monkeypatch.setattr(q4, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(OSError):
+        q4.lib()
