@@ -19,6 +19,7 @@ __all__ = [
     "q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
+    "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
     "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT",
 ]
@@ -78,8 +79,12 @@ def lib() -> ctypes.CDLL:
             L.q4_dequant_f32_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]
             L.q4_dequant_bf16_run.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i32, _vp]
             L.vec4_read_probe_run.argtypes = [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32), _vp]
+            L.q4gemv_device_status.argtypes = [_vp]
+            L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
-                      "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run"):
+                      "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
+    "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
+                      "q4gemv_device_status", "q4gemm_set_wait_timeout_ns"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -189,6 +194,15 @@ def q4_dequant_bf16_run(codes, scales_f16, zeros_u4_or_null, wb, N=None, K=None,
     if check:
         _check(st, "q4_dequant_bf16_run")
     return st
+
+
+def q4gemv_device_status(stream=None) -> int:
+    """Synchronise the stream; Q4_OK or Q4_ERR_TIMEOUT (clears the flag)."""
+    return lib().q4gemv_device_status(_stream(stream))
+
+
+def q4gemm_set_wait_timeout_ns(ns: int) -> int:
+    return lib().q4gemm_set_wait_timeout_ns(int(ns))
 
 
 def vec4_read_probe_run(buf, nbytes, partial, blocks=0, stream=None, check=True):

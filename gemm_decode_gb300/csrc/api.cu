@@ -161,6 +161,13 @@ int q4_dequant_bf16_run(const void *codes, const void *scales_f16, const void *z
                           static_cast<cudaStream_t>(stream));
 }
 
+int q4gemv_device_status(void *stream) { return read_device_status(static_cast<cudaStream_t>(stream)); }
+
+int q4gemm_set_wait_timeout_ns(uint64_t ns) {
+    set_gemm_wait_timeout_ns(ns);
+    return Q4_OK;
+}
+
 int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t blocks, int32_t *blocks_used,
                         void *stream) {
     if (buf == nullptr || partial == nullptr || bytes <= 0 || bytes % 16 != 0) return Q4_ERR_INVALID_ARG;

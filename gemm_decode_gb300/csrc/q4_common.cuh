@@ -47,6 +47,8 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
                   cudaStream_t stream);
 int launch_f32gemv(const float *W, const float *x, float *y, int M, int64_t N, int K,
                    cudaStream_t stream);
+void set_gemm_wait_timeout_ns(unsigned long long ns);
+int read_device_status(cudaStream_t stream);
 int launch_dequant(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
                    void *w, bool bf16, int64_t N, int K, int group, cudaStream_t stream);
 int launch_read_probe(const float4 *buf, int64_t n16, float *partial, int blocks,

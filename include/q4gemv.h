@@ -113,6 +113,18 @@ Q4_API const char *q4gemv_status_string(int status);
  * "" (static/thread storage, never NULL). */
 Q4_API const char *q4gemv_last_cuda_error(void);
 
+/* Synchronise `stream`, then report and clear the device status word that the
+ * tensor-core kernel raises when one of its bounded pipeline waits expires:
+ * Q4_OK, Q4_ERR_TIMEOUT (the affected q4gemm_run output is unspecified), or
+ * Q4_ERR_CUDA if synchronising failed.  Host-blocking. */
+Q4_API int q4gemv_device_status(void *stream);
+
+/* Upper bound, in nanoseconds, on each wait of the tensor-core pipeline for
+ * launches made after this call (default 1e9).  0 makes every wait that is not
+ * already satisfied give up at once, which exercises the timeout path without a
+ * fault.  Process-wide; not synchronised with launches in flight. */
+Q4_API int q4gemm_set_wait_timeout_ns(uint64_t ns);
+
 /* ---- test and measurement exports (not part of the GEMV API proper) ---------------- */
 
 /* Write the dequantised matrix w[N][K] = (q - z) * s as float, with the same in-register

@@ -1,0 +1,136 @@
+"""GPU parity of the tensor-core int4 matmul (q4gemm_run) against the CPU oracle.
+
+The tensor-core path feeds the MMA bf16 weights, each the exact binary32
+(q - z) * s rounded once to bfloat16, so a single term can be off by up to
+2^-9 of |w a|.  Checks:
+  * every case: against the oracle's own bf16-rounded weights multiplied in
+    binary64 (numpy) within 2e-6 * sum|w_bf16 a| + 1e-6 -- only binary32
+    accumulation differs -- and against the exact oracle within the bound that
+    follows from the arithmetic, 2^-9 * sum|w a| + 2e-6 * sum|w a| + 1e-6;
+  * the prefill workloads (K >= 2048): against the exact oracle within the
+    stated tolerance |c - c_ref| <= 1e-3 * sum_k |w_nk a_mk| + 1e-6.
+"""
+import numpy as np
+import pytest
+
+import gemm_decode_gb300 as q4
+import oracle
+import synth
+from conftest import GOLDEN_FILES, golden_x, load_golden
+from gpu_util import assert_within_bound, dev, host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_cuda()
+    q4.lib()
+    return t
+
+
+def bf16_to_f64(u16):
+    return (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def run_gemm(torch, w, a_bf16):
+    M, K = a_bf16.shape
+    c = torch.full((M, w.N), 7.0, dtype=torch.float32, device="cuda")
+    q4.q4gemm_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a_bf16, torch), c,
+                  M, w.N, K, w.group)
+    torch.cuda.synchronize()
+    assert q4.q4gemv_device_status() == q4.Q4_OK
+    return host(c)
+
+
+BF16_TERM = 2.0 ** -9
+
+
+def check_case(torch, w, a, stated_tolerance=False):
+    c = run_gemm(torch, w, a)
+    c_ref, bound = oracle.q4_gemm(w.codes, w.scales, w.zeros, a, w.group)
+    what = f"M={a.shape[0]} N={w.N} K={w.K} g={w.group}"
+    if stated_tolerance:
+        assert_within_bound(c, c_ref, bound, what)
+    err = np.abs(c.astype(np.float64) - c_ref.astype(np.float64))
+    assert np.all(err <= (BF16_TERM + 2e-6) * bound + 1e-6), what
+    wb = bf16_to_f64(oracle.q4_dequant_bf16(w.codes, w.scales, w.zeros, w.K, w.group))
+    af = bf16_to_f64(a)
+    ref_b = af @ wb.T
+    mag = np.abs(af) @ np.abs(wb).T
+    err = np.abs(c.astype(np.float64) - ref_b)
+    assert np.all(err <= 2e-6 * mag + 1e-6), f"max {np.max(err / (mag + 1e-30))}"
+
+
+@pytest.mark.parametrize("name", GOLDEN_FILES)
+def test_hand_worked_examples_exact(torch, name):
+    d = load_golden(name)
+    w = synth.Q4Weights(d["codes"], d["scales"], d["zeros"], d["N"], d["K"], d["group"])
+    for kind, y_expect in d["cases"]:
+        x = golden_x(kind, d["K"])
+        a = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        c = run_gemm(torch, w, a)
+        np.testing.assert_array_equal(c[0], y_expect)
+
+
+@pytest.mark.parametrize("g", [32, 64, 128])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_small_shapes(torch, g, symmetric):
+    for M, N, K in [(1, 128, 128), (7, 200, 256), (128, 128, 2 * 64), (130, 256, 384), (300, 136, 512),
+                    (64, 384, 1024 if g <= 64 else 1152)]:
+        if K % g:
+            continue
+        w = synth.q4_weights(M + N + K + g, N, K, g, symmetric=symmetric)
+        a = synth.activations_bf16(M + K, M, K)
+        check_case(torch, w, a)
+
+
+def test_k_tail_half_block(torch):
+    # K = 96: the last 64-wide K-block is half empty
+    w = synth.q4_weights(3, 256, 96, 32)
+    a = synth.activations_bf16(3, 128, 96)
+    check_case(torch, w, a)
+
+
+def test_prefill_gate_128_tokens(torch):
+    name, M, N, K = synth.PREFILL["shapes"][0]
+    w = synth.q4_weights(128, N, K, 32, tag=name)
+    a = synth.activations_bf16(128, M, K)
+    check_case(torch, w, a, stated_tolerance=True)
+
+
+def test_prefill_ffn_2048_tokens_sampled(torch):
+    name, M, N, K = synth.PREFILL["shapes"][1]
+    w = synth.q4_weights(2048, N, K, 32, tag=name)
+    a = synth.activations_bf16(2048, M, K)
+    c = run_gemm(torch, w, a)
+    r = np.random.default_rng(5)
+    ms = sorted(set(r.choice(M, 24, replace=False).tolist()) | {0, M - 1})
+    ns = sorted(set(r.choice(N, 24, replace=False).tolist()) | {0, N - 1})
+    c_ref, bound = oracle.q4_gemm_rows(w.codes, w.scales, w.zeros, a, 32, ms, ns)
+    assert_within_bound(c[np.ix_(ms, ns)], c_ref, bound, "2048x14336x4096 sampled")
+
+
+def test_deterministic(torch):
+    w = synth.q4_weights(9, 512, 2048, 32)
+    a = synth.activations_bf16(9, 256, 2048)
+    np.testing.assert_array_equal(run_gemm(torch, w, a), run_gemm(torch, w, a))
+
+
+def test_bounded_wait_reports_timeout_without_fault(torch):
+    # every pipeline wait that is not already satisfied gives up at once: the
+    # kernel must stop, drain what it issued, release tensor memory and raise the
+    # status flag -- and the context must stay usable afterwards
+    w = synth.q4_weights(4, 512, 2048, 32)
+    a = synth.activations_bf16(4, 256, 2048)
+    c = torch.zeros((256, 512), dtype=torch.float32, device="cuda")
+    try:
+        q4.q4gemm_set_wait_timeout_ns(0)
+        q4.q4gemm_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c,
+                      256, 512, 2048, 32)
+        st = q4.q4gemv_device_status()
+    finally:
+        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    assert st == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK          # flag cleared
+    check_case(torch, w, a)                                # and the next call is correct
