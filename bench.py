@@ -348,6 +348,7 @@ def run_gpu(args, rank, world, local_rank):
         "graph_steps": chunk, "event_mode": ev.mode}
     if args.controls and rank == 0:
         detail["controls"] = run_controls(args, torch, q4)
+        detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -507,6 +508,45 @@ def run_controls(args, torch, q4):
     }
 
 
+def load_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
+def run_prefill(args, torch, q4):
+    """The tensor-core int4 matmul on the prefill shapes: TFLOP/s against the
+    measured dense bf16 peak (2*M*N*K flops per call)."""
+    out = []
+    burst, sustained, src = load_bf16_peak()
+    for name, M, N, K in synth.PREFILL["shapes"]:
+        w = synth.q4_weights(7, N, K, 32, tag=name)
+        a = synth.activations_bf16(7, M, K)
+        dev = lambda x: None if x is None else torch.from_numpy(
+            np.ascontiguousarray(x.view(np.int16) if x.dtype == np.uint16 else x)).cuda()
+        cw, sw, zw, ad = dev(w.codes), dev(w.scales), dev(w.zeros), dev(a)
+        c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        n_it = 20 if M * N * K > 1e10 else 200
+        for _ in range(3):
+            q4.q4gemm_run(cw, sw, zw, ad, c, M, N, K, 32)
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(n_it):
+            q4.q4gemm_run(cw, sw, zw, ad, c, M, N, K, 32)
+        e0.record()
+        torch.cuda.synchronize()
+        assert q4.q4gemv_device_status() == q4.Q4_OK
+        us = s0.elapsed_time(e0) * 1e3 / n_it
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        out.append({"name": name, "M": M, "N": N, "K": K, "us": round(us, 2), "tflops": round(tf, 1),
+                    "frac_of_bf16_peak": round(tf / burst, 4), "peak": burst, "peak_source": src,
+                    "note": "back-to-back calls on one weight copy (W fits in L2)"})
+    return out
+
+
 # ----------------------------------------------------------------- CPU oracle
 
 def oracle_step(ws, xs_host, shapes, group, threads, row_fraction=1.0):
@@ -599,7 +639,8 @@ def parse_args(argv=None):
     p.add_argument("--ref-seconds", type=float, default=90.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--controls", type=int, default=1)
-    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "f32_lm_head"],
+    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "f32_lm_head",
+                                         "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--traffic-bytes", type=float, default=None,
@@ -625,6 +666,17 @@ def run_profile_case(args):
     import gemm_decode_gb300 as q4
     dev = lambda a: None if a is None else torch.from_numpy(
         np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).cuda()
+    if args.profile.startswith("gemm_"):
+        name, M, N, K = synth.PREFILL["shapes"][1 if args.profile == "gemm_ffn" else 0]
+        w = synth.q4_weights(7, N, K, 32, tag=name)
+        a = dev(synth.activations_bf16(7, M, K))
+        c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        cw, sw, zw = dev(w.codes), dev(w.scales), dev(w.zeros)
+        for _ in range(4):
+            q4.q4gemm_run(cw, sw, zw, a, c, M, N, K, 32)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": 4}))
+        return
     if args.profile == "f32_lm_head":
         N, K = 151936, 896
         Ws = [dev(synth.dense_f32(3, N, K)) for _ in range(2)]

@@ -243,8 +243,32 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
         const uint8_t *crow = g.codes + static_cast<int64_t>(n) * (g.K / 2);
         const uint16_t *srow = g.scales + static_cast<int64_t>(n) * g.nb;
         const uint8_t *zrow = g.zeros ? g.zeros + static_cast<int64_t>(n) * g.zrow : nullptr;
+        // codes / scale / zero point of K-block kb, fetched PF blocks ahead
+        constexpr int PF = 3;
+        struct Fetch {
+            uint4 cw;
+            uint32_t sc, zb;
+        };
+        auto fetch = [&](Fetch &f, int kb) {
+            const int k = kb * BK + half * 32;
+            if (kb < kblocks && k < g.K) {
+                const int grp = k >> (5 + g.gshift);
+                f.cw = ldg_stream(crow + k / 2);
+                f.sc = ldg_u16(srow + grp);
+                f.zb = zrow ? ldg_u8(zrow + (grp >> 1)) : 0u;
+            }
+        };
+        static_assert(PF == 3, "the fetch ring below rotates three registers sets");
+        Fetch f0, f1, f2;
+        fetch(f0, 0);
+        fetch(f1, 1);
+        fetch(f2, 2);
         for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
             const int s = kb % STAGES;
+            const Fetch cur = f0;   // rotate without dynamic indexing (stays in registers)
+            f0 = f1;
+            f1 = f2;
+            fetch(f2, kb + PF);
             if (kb >= STAGES && !mbar_wait(empty(s), ((kb / STAGES) - 1) & 1, limit)) {
                 fail();
                 break;
@@ -252,14 +276,11 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
             const int k = kb * BK + half * 32;     // first code of this thread's chunk
             uint32_t out[16];
             if (k < g.K) {
-                const uint4 cw = ldg_stream(crow + k / 2);
+                const uint4 cw = cur.cw;
                 const int grp = k >> (5 + g.gshift);
-                const float sc = half_bits_to_float(ldg_u16(srow + grp));
+                const float sc = half_bits_to_float(cur.sc);
                 uint32_t z = 8u;
-                if (zrow) {
-                    const uint32_t zb = ldg_u8(zrow + (grp >> 1));
-                    z = (grp & 1) ? (zb >> 4) : (zb & 0xFu);
-                }
+                if (zrow) z = (grp & 1) ? (cur.zb >> 4) : (cur.zb & 0xFu);
                 const ZeroTerms zt = zero_terms(z);
                 // s / e_p for the eight positions (exact power-of-two scalings of s)
                 const float2 f01 = make_float2(sc, sc * 0x1p-4f), f23 = make_float2(sc * 0x1p-8f, sc * 0x1p-12f);
