@@ -138,51 +138,59 @@ __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes 
 
 }  // namespace
 
-template <int MT, int U, int D, bool ASYM, bool WARPRED>
-__global__ void __launch_bounds__(512)
+// Compile-time geometry: KC = chunks per row and G = group size when known at
+// compile time (0 = read from the arguments); U rows groups per ring iteration
+// and D ring slots.
+template <int MT, bool ASYM, int CTP, int RG, int KC, int G, int U, int D>
+__global__ void __launch_bounds__(CTP * RG)
 q4gemv_xreg_kernel(const XregArgs a) {
+    constexpr int T = CTP * RG;
+    constexpr bool WARPRED = CTP >= 32;
+    constexpr int RED_LD = WARPRED ? CTP / 32 : CTP + 1;
+    constexpr int ROWS_IT = U * RG;                     // rows per ring iteration
+    constexpr int RB = (64 / ROWS_IT) > 0 ? (64 / ROWS_IT) : 1;     // iterations per reduction batch
+    constexpr int ROWS_B = RB * ROWS_IT;
+    constexpr int RED_FLOATS = ROWS_B * MT * RED_LD;
+    constexpr uint32_t SLOT = U * T * (ASYM ? 24 : 20);  // ring bytes per iteration
     extern __shared__ __align__(16) unsigned char smem[];
-    const int T = blockDim.x;
     const int tid = threadIdx.x;
-    const int CTp = a.CTp;
-    const int r = tid / CTp;            // row within a row group
-    const int cl = tid - r * CTp;       // chunk position within this CTA's K-slice
-    const int split = static_cast<int>(blockIdx.y);
-    const int c = split * a.CT + cl;    // chunk position in the row
-    const bool active = (cl < a.CT) && (c < a.C);
-    const int RG = a.RG;
-    const int rows_it = U * RG;         // rows per iteration
-    const int RB = a.RB;
+    const int r = tid / CTP;            // row within a row group
+    const int cl = tid - r * CTP;       // chunk position within this CTA's K-slice
+    const int split = KC ? 0 : static_cast<int>(blockIdx.y);
+    const int C = KC ? KC : a.C;
+    const int K = C * 32;
+    const int CT = KC ? KC : a.CT;
+    const int nb = G ? K / G : a.nb;
+    const int zrow = (nb + 1) / 2;
+    const int gshift = G ? (G == 32 ? 0 : (G == 64 ? 1 : 2)) : a.gshift;
+    const int c = split * CT + cl;      // chunk position in the row
+    // with compile-time geometry every thread holds a real chunk (KC == CTP)
+    const bool active = (KC == CTP) || ((cl < CT) && (c < C));
 
-    // shared memory carve-up
-    uint32_t *planes = reinterpret_cast<uint32_t *>(smem);                       // [MT][CTp][28]
-    float *red = reinterpret_cast<float *>(smem + a.off_red);                    // [rows_b][MT][red_ld]
-    unsigned char *ring = smem + a.off_ring;                                     // [D][slot]
-    float *ysum = reinterpret_cast<float *>(smem + a.off_ysum);                  // [rows_b][MT] (split only)
+    // shared memory: planes [MT][CTP][28] | red [2][ROWS_B][MT][RED_LD] | ring [D][SLOT] | ysum [ROWS_B][MT]
+    uint32_t *planes = reinterpret_cast<uint32_t *>(smem);
+    float *red0 = reinterpret_cast<float *>(smem + a.off_red);
+    unsigned char *ring = smem + a.off_ring;
+    float *ysum = reinterpret_cast<float *>(smem + a.off_ysum);
 
-    // ---- this CTA's super groups (contiguous) ----
     const int gsz = static_cast<int>(gridDim.x);
     const int g_begin = static_cast<int>(static_cast<int64_t>(a.nsuper) * blockIdx.x / gsz);
     const int g_end = static_cast<int>(static_cast<int64_t>(a.nsuper) * (blockIdx.x + 1) / gsz);
     const int ng = g_end - g_begin;
 
-    // ---- per-thread streams ----
-    const int grp = c >> a.gshift;
-    const int64_t row0 = static_cast<int64_t>(g_begin) * rows_it + r;
-    const int64_t pitch = a.K / 2;
+    // ---- per-thread streams (loop-carried pointers; per-thread constant shifts) ----
+    const int grp = c >> gshift;
+    const int64_t row0 = static_cast<int64_t>(g_begin) * ROWS_IT + r;
+    const int64_t pitch = K / 2;
     const unsigned char *gc = a.codes + row0 * pitch + static_cast<int64_t>(c) * 16;
-    const int64_t se = row0 * a.nb + grp;                       // scale element index
+    const int64_t se = row0 * nb + grp;                         // scale element index
     const unsigned char *gs = reinterpret_cast<const unsigned char *>(a.scales) + (se & ~1LL) * 2;
-    const int ssh = static_cast<int>(se & 1) * 16;              // same for every row of this thread
-    const int64_t ze = row0 * a.zrow + (grp >> 1);              // zero-point byte index
-    const unsigned char *gz = a.zeros + (ASYM ? (ze & ~3LL) : 0);
+    const int ssh = static_cast<int>(se & 1) * 16;
+    const int64_t ze = row0 * zrow + (grp >> 1);                // zero-point byte index
+    const unsigned char *gz = ASYM ? a.zeros + (ze & ~3LL) : nullptr;
     const int zsh = static_cast<int>(ze & 3) * 8 + (grp & 1) * 4;
-    const int64_t step_c = static_cast<int64_t>(rows_it) * pitch;
-    const int64_t step_s = static_cast<int64_t>(rows_it) * a.nb * 2;
-    const int64_t step_z = static_cast<int64_t>(rows_it) * a.zrow;
-    const int64_t rg_c = static_cast<int64_t>(RG) * pitch, rg_s = static_cast<int64_t>(RG) * a.nb * 2,
-                  rg_z = static_cast<int64_t>(RG) * a.zrow;
-    const uint32_t slot_bytes = static_cast<uint32_t>(U * T * (ASYM ? 24 : 20));
+    const int64_t rg_c = static_cast<int64_t>(RG) * pitch, rg_s = static_cast<int64_t>(RG) * nb * 2,
+                  rg_z = static_cast<int64_t>(RG) * zrow;
     const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
     const uint32_t my_c = ring_s + tid * 16;
     const uint32_t my_s = ring_s + U * T * 16 + tid * 4;
@@ -191,9 +199,9 @@ q4gemv_xreg_kernel(const XregArgs a) {
     int issued = 0;
     auto issue_next = [&]() {
         if (active) {
-            const uint32_t so = static_cast<uint32_t>(issued % D) * slot_bytes;
-            const int64_t rb = static_cast<int64_t>(g_begin + issued) * rows_it;   // first row of the iteration
-            if (rb + rows_it <= a.N) {
+            const uint32_t so = static_cast<uint32_t>(issued % D) * SLOT;
+            const int64_t rb = static_cast<int64_t>(g_begin + issued) * ROWS_IT;   // first row of the iteration
+            if (rb + ROWS_IT <= a.N) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     cp_async16(my_c + so + u * T * 16, gc + u * rg_c);
@@ -205,19 +213,19 @@ q4gemv_xreg_kernel(const XregArgs a) {
                 // class, so the per-thread shifts stay valid); its result is discarded.
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    int64_t n = rb + u * RG + r;
+                    const int64_t n = rb + u * RG + r;
                     int64_t back = 0;
                     if (n >= a.N) back = (n - (a.N - 1) + RG - 1) / RG;
-                    const int64_t j = u - back;   // row groups from this iteration's first (may be < 0)
+                    const int64_t j = u - back;
                     cp_async16(my_c + so + u * T * 16, gc + j * rg_c);
                     cp_async4(my_s + so + u * T * 4, gs + j * rg_s);
                     if (ASYM) cp_async4(my_z + so + u * T * 4, gz + j * rg_z);
                 }
             }
         }
-        gc += step_c;
-        gs += step_s;
-        gz += ASYM ? step_z : 0;
+        gc += U * rg_c;
+        gs += U * rg_s;
+        if (ASYM) gz += U * rg_z;
         ++issued;
     };
 
@@ -229,20 +237,21 @@ q4gemv_xreg_kernel(const XregArgs a) {
 
     // ---- encode this CTA's x slice into planes (one warp per chunk and row of x) ----
     {
-        const int warp = tid >> 5, lane = tid & 31, nwarps = T >> 5;
-        for (int i = warp; i < MT * CTp; i += nwarps) {
-            const int m = i / CTp, ci = i - m * CTp;
-            const int cc = split * a.CT + ci;
+        const int warp = tid >> 5, lane = tid & 31;
+        constexpr int NW = T / 32;
+        for (int i = warp; i < MT * CTP; i += NW) {
+            const int m = i / CTP, ci = i - m * CTP;
+            const int cc = split * CT + ci;
             float v = 0.0f;
-            if (m < a.M && ci < a.CT && cc < a.C) v = a.x[static_cast<int64_t>(m) * a.K + cc * 32 + lane];
-            encode_chunk(v, planes + (m * CTp + ci) * kPlaneWords, lane);
+            if (m < a.M && ci < CT && cc < C) v = a.x[static_cast<int64_t>(m) * K + cc * 32 + lane];
+            encode_chunk(v, planes + (m * CTP + ci) * kPlaneWords, lane);
         }
     }
     __syncthreads();
     Planes P[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const uint32_t *pw = planes + (m * CTp + cl) * kPlaneWords;
+        const uint32_t *pw = planes + (m * CTP + cl) * kPlaneWords;
 #pragma unroll
         for (int i = 0; i < 24; ++i) P[m].p[i] = pw[i];
         P[m].s_lo = static_cast<int>(pw[24]);
@@ -250,24 +259,28 @@ q4gemv_xreg_kernel(const XregArgs a) {
         P[m].f = __uint_as_float(pw[27]);
     }
 
-    const int red_ld = a.red_ld;
     const uint4 *rc_t = reinterpret_cast<const uint4 *>(ring) + tid;
     const uint32_t *rs_t = reinterpret_cast<const uint32_t *>(ring + U * T * 16) + tid;
     const uint32_t *rz_t = rs_t + U * T;
     cg::cluster_group cluster = cg::this_cluster();
     const int nsplit = static_cast<int>(gridDim.y);
+    // this thread's slot in a partial-sum buffer (row r of iteration bi, sub-row u)
+    const int red_col = WARPRED ? (cl >> 5) : cl;
 
-    for (int b0 = 0; b0 < ng; b0 += RB) {
+    int pp = 0;
+    for (int b0 = 0; b0 < ng; b0 += RB, pp ^= 1) {
         const int nbat = min(RB, ng - b0);
+        float *red = red0 + pp * RED_FLOATS;
 #pragma unroll 1
         for (int bi = 0; bi < nbat; ++bi) {
             if (issued < ng) issue_next();
             cp_commit();
             cp_wait<D - 1>();
-            const uint32_t so = static_cast<uint32_t>((b0 + bi) % D) * slot_bytes;
+            const uint32_t so = static_cast<uint32_t>((b0 + bi) % D) * SLOT;
             const uint4 *rc = reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(rc_t) + so);
             const uint32_t *rs = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rs_t) + so);
             const uint32_t *rz = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rz_t) + so);
+            float *rd = red + ((bi * U) * RG + r) * MT * RED_LD + red_col;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 float part[MT];
@@ -282,39 +295,43 @@ q4gemv_xreg_kernel(const XregArgs a) {
 #pragma unroll
                     for (int m = 0; m < MT; ++m) part[m] = 0.0f;
                 }
-                const int row_b = (bi * U + u) * RG + r;
-                if (WARPRED) {
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) {
-                        float v = part[m];
+                for (int m = 0; m < MT; ++m) {
+                    float v = part[m];
+                    if (WARPRED) {
 #pragma unroll
                         for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                        if ((cl & 31) == 0) red[(row_b * MT + m) * red_ld + (cl >> 5)] = v;
+                        if ((cl & 31) == 0) rd[(u * RG * MT + m) * RED_LD] = v;
+                    } else {
+                        rd[(u * RG * MT + m) * RED_LD] = v;
                     }
-                } else {
-#pragma unroll
-                    for (int m = 0; m < MT; ++m) red[(row_b * MT + m) * red_ld + cl] = part[m];
                 }
             }
         }
+        // One barrier per batch: the partial buffers alternate, and the next batch's
+        // barrier orders this batch's reads before the buffer is written again.
         __syncthreads();
-        // ---- per-row sums of this batch ----
-        const int nrows = nbat * rows_it;
-        const int nterms = WARPRED ? (CTp >> 5) : CTp;
-        const int64_t first_row = static_cast<int64_t>(g_begin + b0) * rows_it;
-        for (int i = tid; i < nrows * MT; i += T) {
-            const float *src = red + i * red_ld;
-            float v = 0.0f;
-            for (int q = 0; q < nterms; ++q) v += src[q];
-            const int rr = i / MT, m = i - rr * MT;
-            if (nsplit == 1) {
+        const int nrows = nbat * ROWS_IT;
+        constexpr int NTERMS = WARPRED ? CTP / 32 : CTP;
+        const int64_t first_row = static_cast<int64_t>(g_begin + b0) * ROWS_IT;
+        if (nsplit == 1) {
+            for (int i = tid; i < nrows * MT; i += T) {
+                const float *src = red + i * RED_LD;
+                float v = 0.0f;
+#pragma unroll
+                for (int q = 0; q < NTERMS; ++q) v += src[q];
+                const int rr = i / MT, m = i - rr * MT;
                 const int64_t n = first_row + rr;
                 if (n < a.N && m < a.M) a.y[static_cast<int64_t>(m) * a.N + n] = v;
-            } else {
+            }
+        } else {
+            for (int i = tid; i < nrows * MT; i += T) {
+                const float *src = red + i * RED_LD;
+                float v = 0.0f;
+#pragma unroll
+                for (int q = 0; q < NTERMS; ++q) v += src[q];
                 ysum[i] = v;
             }
-        }
-        if (nsplit > 1) {
             // add the K-slices of the cluster in rank order
             cluster.sync();
             const int rank = static_cast<int>(cluster.block_rank());
@@ -326,8 +343,6 @@ q4gemv_xreg_kernel(const XregArgs a) {
                 if (n < a.N && m < a.M) a.y[static_cast<int64_t>(m) * a.N + n] = v;
             }
             cluster.sync();
-        } else {
-            __syncthreads();
         }
     }
     cp_wait<0>();
@@ -335,17 +350,26 @@ q4gemv_xreg_kernel(const XregArgs a) {
 
 // ------------------------------------------------------------------ host side
 
-template <int MT, int U, int D, bool ASYM, bool WARPRED>
+// Supported (threads per row, rows per group) pairs.
+#define Q4_XREG_SHAPES(X) X(28, 8) X(32, 4) X(64, 4) X(96, 4) X(128, 4) X(160, 2) X(192, 2) X(224, 2) X(256, 2)
+
+static int rows_per_group(int ctp) {
+#define Q4_RG(C, R) if (ctp == C) return R;
+    Q4_XREG_SHAPES(Q4_RG)
+#undef Q4_RG
+    return 0;
+}
+
+template <int MT, bool ASYM, int CTP, int RG, int KC = 0, int G = 0, int U = kXregU, int D = kXregD>
 static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
-    auto kern = q4gemv_xreg_kernel<MT, U, D, ASYM, WARPRED>;
+    auto kern = q4gemv_xreg_kernel<MT, ASYM, CTP, RG, KC, G, U, D>;
+    constexpr int T = CTP * RG;
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              device_info().smem_optin);
-        if (e == cudaSuccess && p.S > 1)
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         if (e != cudaSuccess) {
             set_cuda_error(e);
             return Q4_ERR_CUDA;
@@ -353,7 +377,7 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
         configured[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.blockDim = dim3(T, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -376,7 +400,7 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
         }
     } else {
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, p.threads, p.smem);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, p.smem);
         if (e != cudaSuccess) {
             set_cuda_error(e);
             return Q4_ERR_CUDA;
@@ -384,9 +408,12 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
         resident = per_sm * device_info().sms;
     }
     if (resident < 1) return Q4_ERR_UNSUPPORTED;
-    const int grid_x = resident < a.nsuper ? resident : a.nsuper;
+    const int nsuper = static_cast<int>((a.N + U * RG - 1) / (U * RG));
+    XregArgs aa = a;
+    aa.nsuper = nsuper;
+    const int grid_x = resident < nsuper ? resident : nsuper;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(p.S), 1);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, aa);
     if (e != cudaSuccess) {
         set_cuda_error(e);
         return Q4_ERR_CUDA;
@@ -394,22 +421,50 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
     return launch_status();
 }
 
-template <int MT, int U, int D>
-static int launch_flags(const XregPlan &p, const XregArgs &a, cudaStream_t s) {
-    if (p.asym)
-        return p.warpred ? launch_one<MT, U, D, true, true>(p, a, s) : launch_one<MT, U, D, true, false>(p, a, s);
-    return p.warpred ? launch_one<MT, U, D, false, true>(p, a, s) : launch_one<MT, U, D, false, false>(p, a, s);
-}
-
-int launch_q4gemv_xreg(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
-    if (p.MT == 1) return launch_flags<1, kXregU, kXregD>(p, a, stream);
-    if (p.MT == 2) return launch_flags<2, kXregU, kXregD>(p, a, stream);
+template <int MT, bool ASYM>
+static int launch_shape(const XregPlan &p, const XregArgs &a, cudaStream_t s) {
+    // compile-time geometry for the long-N decode shapes (LM heads)
+    if (p.special) {
+        if (a.C == 28 && a.nb == 28) return launch_one<MT, ASYM, 28, 8, 28, 32, kXregUSpecial, kXregDSpecial>(p, a, s);
+        if (a.C == 128 && a.nb == 32) return launch_one<MT, ASYM, 128, 4, 128, 128, kXregUSpecial, kXregDSpecial>(p, a, s);
+    }
+#define Q4_CASE(C, R) \
+    if (a.CTp == C) return launch_one<MT, ASYM, C, R>(p, a, s);
+    Q4_XREG_SHAPES(Q4_CASE)
+#undef Q4_CASE
     return Q4_ERR_UNSUPPORTED;
 }
 
-// Plan: threads per row CTp, rows per group RG, split S, batch RB, persistent grid.
-// Returns false when the shape does not suit this kernel (the caller then uses the
-// general kernel).
+int launch_q4gemv_xreg(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
+    if (p.MT == 1) return p.asym ? launch_shape<1, true>(p, a, stream) : launch_shape<1, false>(p, a, stream);
+    if (p.MT == 2) return p.asym ? launch_shape<2, true>(p, a, stream) : launch_shape<2, false>(p, a, stream);
+    return Q4_ERR_UNSUPPORTED;
+}
+
+// Shared-memory layout of one instance (must match the carve-up in the kernel).
+static size_t xreg_smem(int MT, int CTp, int RG, int U, int D, int S, bool asym, XregArgs &a) {
+    const int T = CTp * RG;
+    const int rows_it = U * RG;
+    const bool warpred = CTp >= 32;
+    const int red_ld = warpred ? CTp / 32 : CTp + 1;
+    const int RB = (64 / rows_it) > 0 ? (64 / rows_it) : 1;
+    const size_t planes_b = static_cast<size_t>(MT) * CTp * kPlaneWords * 4;
+    const size_t off_red = (planes_b + 15) / 16 * 16;
+    const size_t red_b = 2 * static_cast<size_t>(RB) * rows_it * MT * red_ld * 4;
+    const size_t off_ring = (off_red + red_b + 15) / 16 * 16;
+    const size_t ring_b = static_cast<size_t>(D) * U * T * (asym ? 24 : 20);
+    const size_t off_ysum = off_ring + ring_b;
+    const size_t ysum_b = S > 1 ? static_cast<size_t>(RB) * rows_it * MT * 4 : 0;
+    a.red_ld = red_ld;
+    a.RB = RB;
+    a.off_red = static_cast<int>(off_red);
+    a.off_ring = static_cast<int>(off_ring);
+    a.off_ysum = static_cast<int>(off_ysum);
+    return off_ysum + ysum_b;
+}
+
+// Plan: K-slices S, threads per row CTp, rows per group RG.  Returns false when the
+// shape does not suit this kernel (the caller then uses the general kernel).
 bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, const void *zeros,
                       XregPlan &p, XregArgs &a) {
     if (M < 1 || M > 2) return false;
@@ -423,58 +478,32 @@ bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, co
     if (asym && (N * zrow) % 4 != 0) return false;
     const DeviceInfo &d = device_info();
     const int MT = M;
-    // K-slices: at most 256 chunk positions per CTA
     int S = (C + 255) / 256;
     if (S > 8) return false;
-    int CT = (C + S - 1) / S;
-    int CTp, RG;
-    if (CT >= 32) {
-        CTp = (CT + 31) / 32 * 32;
-        RG = 4;
-        while (CTp * RG > 512 && RG > 1) RG >>= 1;
-    } else {
-        // rows straddle warps: CTp * RG must be a warp multiple
-        CTp = CT;
-        RG = 4;
-        while ((CTp * RG) % 32 != 0) RG += 4;
-        if (CTp * RG > 512) return false;
-    }
-    // the per-thread shift constants need RG rows to advance whole 4-byte words
+    const int CT = (C + S - 1) / S;
+    const int CTp = CT >= 32 ? (CT + 31) / 32 * 32 : CT;
+    const int RG = rows_per_group(CTp);
+    if (RG == 0) return false;
+    // the per-thread shift constants need RG rows to advance whole words
     if (asym && (static_cast<int64_t>(RG) * zrow) % 4 != 0) return false;
     if ((static_cast<int64_t>(RG) * nb) % 2 != 0) return false;
+    // compile-time-geometry instances serve the long-N shapes they were built for
+    const bool special = S == 1 && ((C == 28 && group == 32) || (C == 128 && group == 128)) &&
+                         N >= 64 * kXregUSpecial * RG;
+    const int U = special ? kXregUSpecial : kXregU;
+    const int D = special ? kXregDSpecial : kXregD;
     const int T = CTp * RG;
-    const int rows_it = kXregU * RG;
-    if (N < rows_it) return false;
-    const bool warpred = CTp >= 32;
-    const int red_ld = warpred ? CTp / 32 : CTp + 1;
-    // batch size: about 128 rows per reduction, within shared memory
-    int RB = 128 / rows_it;
-    if (RB < 1) RB = 1;
-    auto smem_for = [&](int rb) {
-        size_t planes_b = static_cast<size_t>(MT) * CTp * kPlaneWords * 4;
-        size_t off_red = (planes_b + 15) / 16 * 16;
-        size_t red_b = static_cast<size_t>(rb) * rows_it * MT * red_ld * 4;
-        size_t off_ring = (off_red + red_b + 15) / 16 * 16;
-        size_t ring_b = static_cast<size_t>(kXregD) * kXregU * T * (asym ? 24 : 20);
-        size_t off_ysum = off_ring + ring_b;
-        size_t ysum_b = S > 1 ? static_cast<size_t>(rb) * rows_it * MT * 4 : 0;
-        a.off_red = static_cast<int>(off_red);
-        a.off_ring = static_cast<int>(off_ring);
-        a.off_ysum = static_cast<int>(off_ysum);
-        return off_ysum + ysum_b;
-    };
-    size_t smem = smem_for(RB);
-    const size_t budget = static_cast<size_t>(d.smem_optin) - 1024;
-    while (smem > budget && RB > 1) smem = smem_for(--RB);
-    if (smem > budget) return false;
-    const int64_t nsuper = (N + rows_it - 1) / rows_it;
+    if (N < 4 * U * RG) return false;
+    const size_t smem = xreg_smem(MT, CTp, RG, U, D, S, asym, a);
+    if (smem > static_cast<size_t>(d.smem_optin) - 1024) return false;
     p.MT = MT;
     p.S = S;
     p.threads = T;
     p.grid_x = 0;
     p.smem = smem;
     p.asym = asym;
-    p.warpred = warpred;
+    p.warpred = CTp >= 32;
+    p.special = special;
     a.M = M;
     a.N = static_cast<int>(N);
     a.K = K;
@@ -485,9 +514,7 @@ bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, co
     a.CT = CT;
     a.CTp = CTp;
     a.RG = RG;
-    a.RB = RB;
-    a.red_ld = red_ld;
-    a.nsuper = static_cast<int>(nsuper);
+    a.nsuper = static_cast<int>((N + U * RG - 1) / (U * RG));
     return true;
 }
 

@@ -7,6 +7,9 @@ namespace q4 {
 
 constexpr int kXregU = 2;   // row groups per ring iteration
 constexpr int kXregD = 4;   // cp.async ring slots (iterations in flight + 1)
+// compile-time-geometry instances (K = 896 with groups of 32, K = 4096 with groups of 128)
+constexpr int kXregUSpecial = 4;
+constexpr int kXregDSpecial = 2;
 
 struct XregArgs {
     const uint8_t *codes;
@@ -32,6 +35,7 @@ struct XregPlan {
     int MT, S, threads, grid_x;
     size_t smem;
     bool asym, warpred;
+    bool special;   // use the compile-time-geometry instance
 };
 
 bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, const void *zeros,
