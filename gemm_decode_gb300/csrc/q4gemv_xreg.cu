@@ -64,44 +64,61 @@ __device__ __forceinline__ void cp_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N));
 }
 
-// Encode one 32-element chunk of x (one warp, lane i holds element i) into the
-// plane layout: for word w (elements 8w..8w+7) and plane b, word 6w+2b holds
-// the b-th byte of m for the even elements 8w, 8w+2, 8w+4, 8w+6 and word
-// 6w+2b+1 that of the odd elements.  Plane 2 is the signed top byte.
-__device__ void encode_chunk(float v, uint32_t *pw, int lane) {
-    float mx = fabsf(v);
+// Encode one 32-element chunk of x into the plane layout, four threads per chunk
+// (the four consecutive lanes 4j..4j+3 of a warp; thread q owns elements
+// 8q..8q+7, i.e. code word q).  For word w (elements 8w..8w+7) and plane b,
+// word 6w+2b holds the b-th byte of m for the even elements 8w, 8w+2, 8w+4,
+// 8w+6 and word 6w+2b+1 that of the odd elements; plane 2 is the signed top
+// byte.  Words 24/25 hold the plane sums (planes 0+1 combined as s0 + 256 s1,
+// plane 2), word 27 the chunk scale 2^(E-22).  `valid` false encodes zeros;
+// `store` false skips the stores (the shuffles still run: all lanes take part).
+__device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool store, uint32_t *pw, int q) {
+    float v[8];
+    if (valid) {
+        const float4 a = reinterpret_cast<const float4 *>(xc)[2 * q];
+        const float4 b = reinterpret_cast<const float4 *>(xc)[2 * q + 1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     // mx in [2^(E-1), 2^E): E from the binary32 exponent field; tiny chunks clamp.
     int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 126;
     if (E < -100) E = -100;
     const float up = __uint_as_float(static_cast<uint32_t>(127 + 22 - E) << 23);   // 2^(22-E)
-    const int m = __float2int_rn(v * up);                                          // |m| <= 2^22
-    const int b0 = m & 0xFF, b1 = (m >> 8) & 0xFF, b2 = m >> 16;                   // b2 signed
-    const int w = lane >> 3, q = (lane & 7) >> 1, odd = lane & 1;
-    // gather the four bytes of each plane word with shuffles: word (w, parity) takes
-    // lanes 8w + 2q + parity for q = 0..3.
-    uint32_t out0 = 0, out1 = 0, out2 = 0;
+    int m[8];
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-        const int src = (lane & ~7) + 2 * qq + odd;
-        out0 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b0, src) & 0xFF) << (8 * qq);
-        out1 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b1, src) & 0xFF) << (8 * qq);
-        out2 |= static_cast<uint32_t>(__shfl_sync(0xffffffffu, b2, src) & 0xFF) << (8 * qq);
-    }
-    if (q == 0) {  // lanes 8w and 8w+1 write the even/odd words of word w
-        pw[6 * w + 0 + odd] = out0;
-        pw[6 * w + 2 + odd] = out1;
-        pw[6 * w + 4 + odd] = out2;
-    }
-    int s0 = b0, s1 = b1, s2 = b2;
+    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * up);                  // |m| <= 2^22
+    // byte b of the four even (odd) elements -> one word, via byte permutes
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int par = 0; par < 2; ++par) {
+#pragma unroll
+        for (int b = 0; b < 3; ++b) {
+            const uint32_t sel_lo = 0x0040u | (b) | ((4 + b) << 4);   // {m[i].byte b, m[i+2].byte b}
+            const uint32_t t01 = __byte_perm(m[par], m[par + 2], sel_lo);
+            const uint32_t t23 = __byte_perm(m[par + 4], m[par + 6], sel_lo);
+            if (store) pw[6 * q + 2 * b + par] = __byte_perm(t01, t23, 0x5410u);
+        }
+    }
+    int s0 = 0, s1 = 0, s2 = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        s0 += m[i] & 0xFF;
+        s1 += (m[i] >> 8) & 0xFF;
+        s2 += m[i] >> 16;   // arithmetic shift: the signed top byte
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
         s0 += __shfl_xor_sync(0xffffffffu, s0, o);
         s1 += __shfl_xor_sync(0xffffffffu, s1, o);
         s2 += __shfl_xor_sync(0xffffffffu, s2, o);
     }
-    if (lane == 0) {
+    if (store && q == 0) {
         pw[24] = static_cast<uint32_t>(s1 * 256 + s0);
         pw[25] = static_cast<uint32_t>(s2);
         pw[26] = 0u;
@@ -235,28 +252,36 @@ q4gemv_xreg_kernel(const XregArgs a) {
         cp_commit();
     }
 
-    // ---- encode this CTA's x slice into planes (one warp per chunk and row of x) ----
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        constexpr int NW = T / 32;
-        for (int i = warp; i < MT * CTP; i += NW) {
-            const int m = i / CTP, ci = i - m * CTP;
-            const int cc = split * CT + ci;
-            float v = 0.0f;
-            if (m < a.M && ci < CT && cc < C) v = a.x[static_cast<int64_t>(m) * K + cc * 32 + lane];
-            encode_chunk(v, planes + (m * CTP + ci) * kPlaneWords, lane);
-        }
+    // ---- encode this CTA's x slice into planes (four threads per chunk and row of x) ----
+    // (the round count is the same for every thread, so every lane reaches the shuffles)
+    for (int base = 0; base < MT * CTP; base += T / 4) {
+        const int i = base + (tid >> 2);
+        const bool in_range = i < MT * CTP;
+        const int ii = in_range ? i : 0;
+        const int m = ii / CTP, ci = ii - m * CTP;
+        const int cc = split * CT + ci;
+        const bool valid = in_range && m < a.M && ci < CT && cc < C;
+        encode_chunk4(a.x + static_cast<int64_t>(valid ? m : 0) * K + (valid ? cc : 0) * 32, valid, in_range,
+                      planes + (m * CTP + ci) * kPlaneWords, tid & 3);
     }
     __syncthreads();
+    // Load this thread's planes once.  The loads are volatile asm so the compiler
+    // keeps the values in registers instead of re-reading shared memory at each use.
     Planes P[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        const uint32_t *pw = planes + (m * CTP + cl) * kPlaneWords;
+        const uint32_t pa = static_cast<uint32_t>(__cvta_generic_to_shared(planes + (m * CTP + cl) * kPlaneWords));
+        uint32_t w[28];
 #pragma unroll
-        for (int i = 0; i < 24; ++i) P[m].p[i] = pw[i];
-        P[m].s_lo = static_cast<int>(pw[24]);
-        P[m].s_hi = static_cast<int>(pw[25]);
-        P[m].f = __uint_as_float(pw[27]);
+        for (int i = 0; i < 7; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                         : "r"(pa + 16 * i));
+#pragma unroll
+        for (int i = 0; i < 24; ++i) P[m].p[i] = w[i];
+        P[m].s_lo = static_cast<int>(w[24]);
+        P[m].s_hi = static_cast<int>(w[25]);
+        P[m].f = __uint_as_float(w[27]);
     }
 
     const uint4 *rc_t = reinterpret_cast<const uint4 *>(ring) + tid;
@@ -281,31 +306,66 @@ q4gemv_xreg_kernel(const XregArgs a) {
             const uint32_t *rs = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rs_t) + so);
             const uint32_t *rz = reinterpret_cast<const uint32_t *>(reinterpret_cast<const unsigned char *>(rz_t) + so);
             float *rd = red + ((bi * U) * RG + r) * MT * RED_LD + red_col;
+            float part[U][MT];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                float part[MT];
                 if (active) {
                     const uint4 cw = rc[u * T];
                     const uint32_t sw = rs[u * T];
                     const int z = ASYM ? static_cast<int>((rz[u * T] >> zsh) & 0xFu) : 8;
                     const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(sw >> ssh)));
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) part[m] = (s * P[m].f) * chunk_dot(cw, z, P[m]);
+                    for (int m = 0; m < MT; ++m) part[u][m] = (s * P[m].f) * chunk_dot(cw, z, P[m]);
                 } else {
 #pragma unroll
-                    for (int m = 0; m < MT; ++m) part[m] = 0.0f;
+                    for (int m = 0; m < MT; ++m) part[u][m] = 0.0f;
                 }
+            }
+            if (WARPRED) {
+                // Sum the U*MT values over the warp's 32 lanes by recursive halving: each
+                // round halves the number of values a lane carries while doubling the lanes
+                // it covers, then plain butterflies finish (U*MT - 1 + log2 of the rest
+                // shuffles instead of 5 per value).  Lane l ends with value index
+                // (l >> (5 - log2(U*MT))) summed over all 32 lanes.
+                constexpr int NV = U * MT;
+                float v[NV];
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    float v = part[m];
-                    if (WARPRED) {
+                for (int u = 0; u < U; ++u)
 #pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                        if ((cl & 31) == 0) rd[(u * RG * MT + m) * RED_LD] = v;
-                    } else {
-                        rd[(u * RG * MT + m) * RED_LD] = v;
+                    for (int m = 0; m < MT; ++m) v[u * MT + m] = part[u][m];
+                const int lane = tid & 31;
+                int width = NV;
+                int off = 16;
+#pragma unroll
+                for (int round = 0; (NV >> round) > 1; ++round) {
+                    const int half = (NV >> round) / 2;
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        // keep the upper half of the values on lanes with the bit set
+                        const float send = upper ? v[i] : v[i + half];
+                        const float keep = upper ? v[i + half] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                     }
+                    off >>= 1;
+                    width >>= 1;
                 }
+                float t = v[0];
+#pragma unroll
+                for (int o = off; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                (void)width;
+                // lanes whose low bits are 0 write: value index = lane >> (log2(32/NV))
+                constexpr int SHIFT = (NV >= 32) ? 0 : (NV == 1 ? 5 : (NV == 2 ? 4 : (NV == 4 ? 3 : (NV == 8 ? 2 : 1))));
+                if ((lane & ((1 << SHIFT) - 1)) == 0) {
+                    const int idx = lane >> SHIFT;      // = u * MT + m
+                    const int u = idx / MT, m = idx - u * MT;
+                    rd[(u * RG * MT + m) * RED_LD] = t;
+                }
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int m = 0; m < MT; ++m) rd[(u * RG * MT + m) * RED_LD] = part[u][m];
             }
         }
         // One barrier per batch: the partial buffers alternate, and the next batch's
