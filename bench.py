@@ -51,6 +51,10 @@ WORKLOAD = "decode projection set of a 0.5B-class transformer, M=1, group=32"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
+# the instance below on the LM-head shape (see profiles/); None once the kernel changes.
+DOMINANT_KERNEL = "q4gemv_xreg_kernel<MT=1, ASYM, CTP=28, RG=8, KC=28, G=32, U=4, D=2>"
+DOMINANT_TRAFFIC_BYTES = 78_732_800 + 1_519_360
 
 
 def algorithmic_bytes(M, N, K, group, symmetric=False):
@@ -140,7 +144,7 @@ class ClockSampler:
                 continue
             rows.append((ts, parts))
         window = [p for ts, p in rows if (t0 is None or ts >= t0) and (t1 is None or ts <= t1)]
-        use = window if window else rows
+        use = window if window else [p for ts, p in rows]
         sm = [float(p[1]) for p in use if p[1].replace(".", "").isdigit()]
         smax = [float(p[2]) for p in use if p[2].replace(".", "").isdigit()]
         reasons = set()
@@ -351,11 +355,12 @@ def run_gpu(args, rank, world, local_rank):
     lm = len(shapes) - 1
     lm_bytes = algorithmic_bytes(1, shapes[lm][1], shapes[lm][2], group)
     achieved = lm_bytes / (lm_us * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "kernel": "q4gemv_xreg_kernel (M=1, asym) on lm_head 151936x896",
+    roofline = {"bound": "hbm", "kernel": DOMINANT_KERNEL + " on lm_head 151936x896",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_src,
                 "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
-                "traffic": args.traffic_bytes, "algorithmic_bytes_per_launch": lm_bytes}
+                "traffic": args.traffic_bytes if args.traffic_bytes is not None else DOMINANT_TRAFFIC_BYTES,
+                "algorithmic_bytes_per_launch": lm_bytes}
 
     # ---- end to end: pinned host x in, pinned host y out, through the same API ----
     e2e = run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dist)
