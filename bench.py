@@ -53,8 +53,8 @@ NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # the instance below on the LM-head shape (see profiles/); None once the kernel changes.
-DOMINANT_KERNEL = "q4gemv_xreg_kernel<MT=1, ASYM, CTP=28, RG=8, KC=28, G=32, U=4, D=2>"
-DOMINANT_TRAFFIC_BYTES = 78_732_800 + 1_519_360
+DOMINANT_KERNEL = "q4gemv_stream_kernel<C=28, RG=8, G=32, ASYM, U=4, D=3>"
+DOMINANT_TRAFFIC_BYTES = 78_732_032 + 772_352
 
 
 def algorithmic_bytes(M, N, K, group, symmetric=False):

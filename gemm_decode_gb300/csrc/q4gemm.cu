@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "q4_common.cuh"
+#include "q4gemv_stream.cuh"
 
 namespace q4 {
 
@@ -84,6 +85,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete, for at most limit_ns.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (mbar_try(bar, parity)) return true;
+    if (limit_ns == 0) return false;   // a zero bound means one attempt (the timer is coarse)
     const unsigned long long t0 = global_ns();
     for (;;) {
         if (mbar_try(bar, parity)) return true;
@@ -371,7 +373,10 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
 
 static unsigned long long g_timeout_ns = 1000ull * 1000 * 1000;   // 1 s per wait
 
-void set_gemm_wait_timeout_ns(unsigned long long ns) { g_timeout_ns = ns; }
+void set_gemm_wait_timeout_ns(unsigned long long ns) {
+    g_timeout_ns = ns;
+    set_stream_wait_timeout_ns(ns);
+}
 
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -441,18 +446,17 @@ int read_device_status(cudaStream_t stream) {
         set_cuda_error(e);
         return Q4_ERR_CUDA;
     }
-    unsigned int v = 0;
+    unsigned int v = 0, w = 0;
     e = cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof v);
-    if (e != cudaSuccess) {
-        set_cuda_error(e);
+    if (e != cudaSuccess || read_and_clear_stream_status(&w) != Q4_OK) {
+        set_cuda_error(e != cudaSuccess ? e : cudaGetLastError());
         return Q4_ERR_CUDA;
     }
     if (v != 0) {
         const unsigned int zero = 0;
         cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof zero);
-        return Q4_ERR_TIMEOUT;
     }
-    return Q4_OK;
+    return (v != 0 || w != 0) ? Q4_ERR_TIMEOUT : Q4_OK;
 }
 
 }  // namespace q4

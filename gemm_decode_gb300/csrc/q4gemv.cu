@@ -2,6 +2,7 @@
 // row, split-K factor and shared-memory size, then launches one kernel.
 #include "q4gemv_kernel.cuh"
 #include "q4gemv_xreg.cuh"
+#include "q4gemv_stream.cuh"
 
 namespace q4 {
 
@@ -70,6 +71,8 @@ static int plan_gemv(int M, int64_t N, int K, bool asym, GemvPlan &p) {
 int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
                   const float *x, float *y, int M, int64_t N, int K, int group,
                   cudaStream_t stream) {
+    if (stream_applies(M, N, K, group, codes, scales, zeros))
+        return launch_q4gemv_stream(codes, scales, zeros, x, y, N, K, group, stream);
     {
         XregPlan xp;
         XregArgs xa;

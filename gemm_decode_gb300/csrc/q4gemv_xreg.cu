@@ -33,127 +33,13 @@
 
 #include "q4_common.cuh"
 #include "q4gemv_xreg.cuh"
+#include "q4gemv_xplanes.cuh"
 
 namespace q4 {
 
 namespace cg = cooperative_groups;
+using namespace xp;
 
-namespace {
-
-constexpr int kPlaneWords = 28;  // 24 plane words + S_lo + S_hi + (unused) + chunk scale 2^(E-22)
-
-__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
-    int d;
-    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src));
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N));
-}
-
-// Encode one 32-element chunk of x into the plane layout, four threads per chunk
-// (the four consecutive lanes 4j..4j+3 of a warp; thread q owns elements
-// 8q..8q+7, i.e. code word q).  For word w (elements 8w..8w+7) and plane b,
-// word 6w+2b holds the b-th byte of m for the even elements 8w, 8w+2, 8w+4,
-// 8w+6 and word 6w+2b+1 that of the odd elements; plane 2 is the signed top
-// byte.  Words 24/25 hold the plane sums (planes 0+1 combined as s0 + 256 s1,
-// plane 2), word 27 the chunk scale 2^(E-22).  `valid` false encodes zeros;
-// `store` false skips the stores (the shuffles still run: all lanes take part).
-__device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool store, uint32_t *pw, int q) {
-    float v[8];
-    if (valid) {
-        const float4 a = reinterpret_cast<const float4 *>(xc)[2 * q];
-        const float4 b = reinterpret_cast<const float4 *>(xc)[2 * q + 1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-    }
-    float mx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    // mx in [2^(E-1), 2^E): E from the binary32 exponent field; tiny chunks clamp.
-    int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 126;
-    if (E < -100) E = -100;
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + 22 - E) << 23);   // 2^(22-E)
-    int m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * up);                  // |m| <= 2^22
-    // byte b of the four even (odd) elements -> one word, via byte permutes
-#pragma unroll
-    for (int par = 0; par < 2; ++par) {
-#pragma unroll
-        for (int b = 0; b < 3; ++b) {
-            const uint32_t sel_lo = 0x0040u | (b) | ((4 + b) << 4);   // {m[i].byte b, m[i+2].byte b}
-            const uint32_t t01 = __byte_perm(m[par], m[par + 2], sel_lo);
-            const uint32_t t23 = __byte_perm(m[par + 4], m[par + 6], sel_lo);
-            if (store) pw[6 * q + 2 * b + par] = __byte_perm(t01, t23, 0x5410u);
-        }
-    }
-    int s0 = 0, s1 = 0, s2 = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        s0 += m[i] & 0xFF;
-        s1 += (m[i] >> 8) & 0xFF;
-        s2 += m[i] >> 16;   // arithmetic shift: the signed top byte
-    }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    }
-    if (store && q == 0) {
-        pw[24] = static_cast<uint32_t>(s1 * 256 + s0);
-        pw[25] = static_cast<uint32_t>(s2);
-        pw[26] = 0u;
-        pw[27] = __float_as_uint(__uint_as_float(static_cast<uint32_t>(127 + E - 22) << 23));  // 2^(E-22)
-    }
-}
-
-struct Planes {
-    uint32_t p[24];
-    int s_lo, s_hi;
-    float f;
-};
-
-// Exact integer dot product of one 16-byte chunk with one x chunk, minus the
-// zero-point term, returned as the binary32 value sum_k (q_k - z) m_k.
-__device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes &P) {
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-    int a0 = 0, a1 = 0, a2 = 0;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const uint32_t lo = words[w] & 0x0F0F0F0Fu;          // codes of even k, one per byte
-        const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;   // codes of odd k
-        a0 = dp4a_uu(lo, P.p[6 * w + 0], a0);
-        a0 = dp4a_uu(hi, P.p[6 * w + 1], a0);
-        a1 = dp4a_uu(lo, P.p[6 * w + 2], a1);
-        a1 = dp4a_uu(hi, P.p[6 * w + 3], a1);
-        a2 = dp4a_us(lo, P.p[6 * w + 4], a2);
-        a2 = dp4a_us(hi, P.p[6 * w + 5], a2);
-    }
-    const int lo = a1 * 256 + a0 - z * P.s_lo;   // planes 0 and 1: |lo| < 2^31
-    const int hi = a2 - z * P.s_hi;               // plane 2
-    return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
-}
-
-}  // namespace
 
 // Compile-time geometry: KC = chunks per row and G = group size when known at
 // compile time (0 = read from the arguments); U rows groups per ring iteration

@@ -119,7 +119,8 @@ Q4_API const char *q4gemv_last_cuda_error(void);
  * Q4_ERR_CUDA if synchronising failed.  Host-blocking. */
 Q4_API int q4gemv_device_status(void *stream);
 
-/* Upper bound, in nanoseconds, on each wait of the tensor-core pipeline for
+/* Upper bound, in nanoseconds, on each wait of the tensor-core pipeline and of the
+ * TMA-streamed GEMV for
  * launches made after this call (default 1e9).  0 makes every wait that is not
  * already satisfied give up at once, which exercises the timeout path without a
  * fault.  Process-wide; not synchronised with launches in flight. */

@@ -191,3 +191,27 @@ def test_sweep_cells(torch, K, g):
             w = synth.q4_weights(K + N + g, N, K, g, symmetric=sym, tag="sweep")
             for M in synth.SWEEP["Ms"]:
                 _full_size_check(torch, w, M, K + M, count=16)
+
+
+def test_streamed_kernel_bounded_wait_reports_timeout_without_fault(torch):
+    # the TMA-streamed GEMV (long-N shapes) bounds every mbarrier wait the same way
+    # as the tensor-core path: with the bound at 0 it must stop, drain and report
+    # the LM-head shape: about ten row blocks per CTA, so consumers must wait for
+    # blocks the producer can only issue after a slot is released
+    N = 151936
+    w = synth.q4_weights(21, N, 896, 32)
+    x = synth.activations_f32(21, 1, 896)
+    y = torch.zeros((1, N), dtype=torch.float32, device="cuda")
+    try:
+        q4.q4gemm_set_wait_timeout_ns(0)
+        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                      1, N, 896, 32)
+        st = q4.q4gemv_device_status()
+    finally:
+        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    assert st == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK
+    y2 = run_gemv(torch, w, x)
+    rows = _sample_rows(N, 64, 3)
+    y_ref, bound = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, 32, rows)
+    assert_within_bound(y2[:, rows], y_ref, bound, "after timeout")
