@@ -14,8 +14,13 @@ Refractometer page):
   * every step uses the next of several weight replicas whose total is several
     times the 129 MB L2, so each step streams its weights from HBM;
   * W untimed warm-up steps run first;
-  * external event nodes inside the graph time every projection launch, which
-    gives the per-call microseconds and the dominant kernel's roofline figure;
+  * external event nodes inside the graph bracket the LM-head launch of every
+    n-th step (--event-stride), which gives the dominant kernel's duration for
+    its roofline figure; per-projection microseconds come from separate graphs
+    of back-to-back launches;
+  * by default the GEMVs are launched overlapped (programmatic dependent
+    launch: a kernel streams its weights while the previous one finishes and
+    waits for it before reading x); --overlap 0 serialises them;
   * SM clocks and throttle reasons are sampled with nvidia-smi during the
     timed region.
 
@@ -234,6 +239,7 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dist = dist_init(world, "nccl")
     q4.lib()
+    q4.q4gemv_set_overlapped_launch(bool(args.overlap))
     shapes = synth.DECODE_05B["shapes"]
     group = synth.DECODE_05B["group"]
     ws = make_weights(shapes, group, synth.DECODE_05B["scale"])
@@ -280,12 +286,17 @@ def run_gpu(args, rank, world, local_rank):
     reps_timed = args.steps // chunk
     tail = args.steps - reps_timed * chunk
     events = [[(ev.new(), ev.new()) for _ in shapes] for _ in range(chunk)]
+    # LM-head launches bracketed by event nodes: every stride-th step of the timed graph
+    # (an event node costs a bubble and breaks the launch overlap around it)
+    stride = max(1, min(args.event_stride, chunk))
+    sampled = list(range(0, chunk, stride))
 
     def capture(n, with_events, offset=0, only=LM):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                one_step((offset + i) % replicas, stream, events if with_events else None, i, only)
+                timed = with_events and i % stride == 0
+                one_step((offset + i) % replicas, stream, events if timed else None, i, only)
         return g
 
     g_main = capture(chunk, True)
@@ -326,7 +337,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # the dominant launch's duration: event nodes around each LM-head launch of the
     # last replay of the timed graph (the only event nodes in it)
-    lm_us = statistics.fmean(ev.elapsed_ms(events[i][LM][0], events[i][LM][1]) * 1e3 for i in range(chunk))
+    lm_us = statistics.fmean(ev.elapsed_ms(events[i][LM][0], events[i][LM][1]) * 1e3 for i in sampled)
     # per-projection microseconds per call: for each projection, one graph of back-to-back
     # launches over the rotating replicas, timed from outside (no event nodes between
     # launches; event nodes cost a bubble of about a microsecond or more each)
@@ -372,6 +383,7 @@ def run_gpu(args, rank, world, local_rank):
         "weight_replicas": replicas, "replica_bytes": per_step_weight_bytes,
         "graph_steps": chunk, "event_mode": ev.mode,
         "lm_head_us_in_timed_region": round(lm_us, 3),
+        "lm_head_event_samples": f"{len(sampled)} per {chunk}-step graph (every {stride}th step)",
         "us_per_call_note": "per projection: a graph of back-to-back launches over the rotating replicas, "
                             "timed from outside; the LM head's in-step time carries the event-node bubble"}
     if args.controls and rank == 0:
@@ -389,7 +401,9 @@ def run_gpu(args, rank, world, local_rank):
                    "bytes_per_step": bytes_per_step,
                    "l2_policy": f"inputs larger than L2: {replicas} rotating weight replicas "
                                 f"({replicas * per_step_weight_bytes / 1e6:.0f} MB > 129 MB L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "launch": ("overlapped: programmatic dependent launch, each GEMV waits for the "
+                              "previous kernel before reading x" if args.overlap else "serialised")},
         "clocks": clocks, "e2e": e2e, "gpu_launches": len(shapes) * args.steps,
         "roofline": roofline, "pct_of_8TBs_nominal": round(value / NOMINAL_HBM_GBS, 4),
         "detail": detail,
@@ -671,6 +685,10 @@ def parse_args(argv=None):
                                          "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
+    p.add_argument("--overlap", type=int, default=1,
+                   help="1: q4gemv_set_overlapped_launch(1) (programmatic dependent launch); 0: serialised")
+    p.add_argument("--event-stride", type=int, default=25,
+                   help="bracket the LM head of every n-th timed step with event nodes")
     p.add_argument("--traffic-bytes", type=float, default=None,
                    help="ncu dram bytes per launch of the dominant kernel, when measured")
     args = p.parse_args(argv)

@@ -19,7 +19,7 @@ __all__ = [
     "q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
-    "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
+    "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
     "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT",
 ]
@@ -81,10 +81,11 @@ def lib() -> ctypes.CDLL:
             L.vec4_read_probe_run.argtypes = [_vp, _i64, _vp, _i32, ctypes.POINTER(_i32), _vp]
             L.q4gemv_device_status.argtypes = [_vp]
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+            L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
-    "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
-                      "q4gemv_device_status", "q4gemm_set_wait_timeout_ns"):
+                      "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
+                      "q4gemv_set_overlapped_launch"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -203,6 +204,11 @@ def q4gemv_device_status(stream=None) -> int:
 
 def q4gemm_set_wait_timeout_ns(ns: int) -> int:
     return lib().q4gemm_set_wait_timeout_ns(int(ns))
+
+
+def q4gemv_set_overlapped_launch(enable: bool) -> int:
+    """Programmatic dependent launch for later q4gemv_run calls; returns the old setting."""
+    return lib().q4gemv_set_overlapped_launch(1 if enable else 0)
 
 
 def vec4_read_probe_run(buf, nbytes, partial, blocks=0, stream=None, check=True):

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI of libq4gemv.so: argument checks, status codes, device
 // caches, and dispatch to the kernel launchers.  Every check runs on the host
 // before any launch; a failed check launches nothing.
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -11,7 +12,11 @@ namespace q4 {
 
 namespace {
 thread_local char g_cuda_error[256] = "";
+std::atomic<bool> g_overlapped_launch{false};
 }
+
+bool set_overlapped_launch(bool on) { return g_overlapped_launch.exchange(on); }
+bool overlapped_launch() { return g_overlapped_launch.load(std::memory_order_relaxed); }
 
 void set_cuda_error(cudaError_t e) {
     std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -167,6 +172,8 @@ int q4gemm_set_wait_timeout_ns(uint64_t ns) {
     set_gemm_wait_timeout_ns(ns);
     return Q4_OK;
 }
+
+int q4gemv_set_overlapped_launch(int enable) { return set_overlapped_launch(enable != 0) ? 1 : 0; }
 
 int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t blocks, int32_t *blocks_used,
                         void *stream) {

@@ -35,6 +35,21 @@ inline int launch_status() {
     return Q4_OK;
 }
 
+// Overlapped (programmatic dependent) launch of the GEMV kernels: process-wide flag;
+// set_overlapped_launch returns the previous value.  add_overlap_attr appends the
+// programmatic-stream-serialisation attribute to cfg when the flag is set (attrs must
+// have a free entry at cfg.numAttrs).
+bool set_overlapped_launch(bool on);
+bool overlapped_launch();
+inline void add_overlap_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attrs) {
+    if (!overlapped_launch()) return;
+    cudaLaunchAttribute &at = attrs[cfg.numAttrs];
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attrs;
+    ++cfg.numAttrs;
+}
+
 // Common validation of the packed-weight arguments (codes / scales / zeros, K, g).
 int check_q4_args(const void *codes, const void *scales, int64_t N, int64_t K, int32_t group);
 
@@ -55,6 +70,13 @@ int launch_read_probe(const float4 *buf, int64_t n16, float *partial, int blocks
                       cudaStream_t stream);
 
 // ---------------------------------------------------------------- device side
+
+// Programmatic dependent launch.  wait_prior_grid: block until the grid this one
+// depends on has completed and its memory writes are visible (a no-op when the
+// launch carried no programmatic dependency).  allow_next_grid: let the next grid
+// in the stream be scheduled once every CTA of this grid has executed it or exited.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // 2^23 as a binary32 bit pattern.  OR-ing an integer v < 2^23 into its fraction
 // field gives the float 2^23 + v exactly; subtracting two such floats is exact.

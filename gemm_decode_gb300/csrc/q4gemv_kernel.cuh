@@ -84,6 +84,8 @@ q4gemv_kernel(const GemvArgs a) {
     const int c_begin = split * a.CS;
     const int nchunks = min(a.C - c_begin, a.CS);
     const int tid = threadIdx.x;
+    allow_next_grid();
+    wait_prior_grid();   // x and y may belong to the kernel before this one in the stream
 
     // ---- stage x' = x / e_p for this CTA's chunk range (rows m >= M are zero) ----
     {

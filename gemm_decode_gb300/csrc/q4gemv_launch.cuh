@@ -28,7 +28,7 @@ static int launch_gemv_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t st
     cfg.blockDim = dim3(kGemvThreads, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     if (SPLIT) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
@@ -37,6 +37,7 @@ static int launch_gemv_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t st
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
+    add_overlap_attr(cfg, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) {
         set_cuda_error(e);

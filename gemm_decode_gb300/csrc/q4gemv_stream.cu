@@ -96,6 +96,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    allow_next_grid();
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -147,6 +148,9 @@ q4gemv_stream_kernel(const StreamArgs a) {
     }
 
     // ---------------------------------------------------------------- consumers
+    // x and y may belong to the kernel before this one in the stream; the producer
+    // streams only weights and needs no such wait.
+    wait_prior_grid();
     const int r = tid / C, c = tid - r * C;
     // encode x into planes (four consumer threads per chunk), then a consumer-only barrier
     for (int base = 0; base < C; base += Gm::TC / 4) {
@@ -270,7 +274,18 @@ static int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
     a.nblocks = static_cast<int>((a.N + Gm::ROWS - 1) / Gm::ROWS);
     int grid = per_sm * device_info().sms;
     if (grid > a.nblocks) grid = a.nblocks;
-    kern<<<grid, Gm::T, Gm::SMEM, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(Gm::T, 1, 1);
+    cfg.dynamicSmemBytes = Gm::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    add_overlap_attr(cfg, attr);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
     return launch_status();
 }
 

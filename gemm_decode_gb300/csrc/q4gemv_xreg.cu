@@ -137,6 +137,10 @@ q4gemv_xreg_kernel(const XregArgs a) {
         if (p < ng) issue_next();
         cp_commit();
     }
+    // The weights are already on their way; x (and the y this grid writes) may belong
+    // to the kernel before this one in the stream.
+    allow_next_grid();
+    wait_prior_grid();
 
     // ---- encode this CTA's x slice into planes (four threads per chunk and row of x) ----
     // (the round count is the same for every thread, so every lane reaches the shuffles)
@@ -326,7 +330,7 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
     cfg.blockDim = dim3(T, 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     if (p.S > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 1;
@@ -359,6 +363,7 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
     aa.nsuper = nsuper;
     const int grid_x = resident < nsuper ? resident : nsuper;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(p.S), 1);
+    add_overlap_attr(cfg, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, aa);
     if (e != cudaSuccess) {
         set_cuda_error(e);

@@ -126,6 +126,20 @@ Q4_API int q4gemv_device_status(void *stream);
  * fault.  Process-wide; not synchronised with launches in flight. */
 Q4_API int q4gemm_set_wait_timeout_ns(uint64_t ns);
 
+/* Overlapped launch of the M <= 2 GEMV kernels (programmatic dependent launch).
+ * With enable != 0, every later q4gemv_run launch carries CUDA's programmatic
+ * stream serialisation attribute: the kernel may be scheduled while the kernel
+ * before it in the stream is still running, and it starts streaming codes, scales
+ * and zero points at once; before it reads x or writes y it waits (griddepcontrol.wait)
+ * until that kernel has completed and its writes are visible.  Chains of dependent
+ * GEMVs (y of one call is x of the next) stay correct; the launch gaps between them
+ * shrink.  The contract this adds: the weight arrays of a call must not be written by
+ * the kernel that immediately precedes it in the stream (copies and allocations are
+ * not affected).  The pages describe one launch per dispatch and have no counterpart;
+ * this is a launch policy of this implementation.  Default 0.  Process-wide; it
+ * applies to launches made after the call.  Returns the previous setting (0 or 1). */
+Q4_API int q4gemv_set_overlapped_launch(int enable);
+
 /* ---- test and measurement exports (not part of the GEMV API proper) ---------------- */
 
 /* Write the dequantised matrix w[N][K] = (q - z) * s as float, with the same in-register

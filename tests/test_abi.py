@@ -123,3 +123,11 @@ def test_binding_raises_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(q4, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(OSError):
         q4.lib()
+
+
+def test_overlapped_launch_setting_round_trips(L):
+    # host-only state: the call launches nothing
+    assert L.q4gemv_set_overlapped_launch(1) == 0
+    assert L.q4gemv_set_overlapped_launch(7) == 1
+    assert L.q4gemv_set_overlapped_launch(0) == 1
+    assert L.q4gemv_set_overlapped_launch(0) == 0
