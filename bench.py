@@ -685,6 +685,8 @@ def parse_args(argv=None):
                                          "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
+    p.add_argument("--sweep", action="store_true",
+                   help="time every cell of the shape sweep instead of the decode step")
     p.add_argument("--overlap", type=int, default=1,
                    help="1: q4gemv_set_overlapped_launch(1) (programmatic dependent launch); 0: serialised")
     p.add_argument("--event-stride", type=int, default=25,
@@ -743,11 +745,84 @@ def run_profile_case(args):
     print(json.dumps({"profile": args.profile, "launches": 7}))
 
 
+def run_sweep(args):
+    """Every cell of the shape sweep (M, K, N, group, symmetric): microseconds per
+    q4gemv_run call and achieved GB/s, from a CUDA graph of back-to-back launches over
+    rotating weight replicas (cold in HBM where the replicas exceed twice the L2).
+    Weights are drawn on the device (timing only; parity is the tests' job)."""
+    import torch
+    import gemm_decode_gb300 as q4
+    q4.lib()
+    q4.q4gemv_set_overlapped_launch(bool(args.overlap))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(1234)
+    stream = torch.cuda.Stream()
+    cells = []
+    sw = synth.SWEEP
+    for K in sw["Ks"]:
+        for N in sw["Ns"]:
+            for g in sw["groups"]:
+                nb = K // g
+                zrow = (nb + 1) // 2
+                for sym in sw["symmetric"]:
+                    wbytes = N * K // 2 + N * nb * 2 + (0 if sym else N * zrow)
+                    nrep = int(min(256, max(2, -(-6 * L2_BYTES // wbytes))))
+                    reps = []
+                    for _ in range(nrep):
+                        c = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+                        sc = torch.empty((N, nb), dtype=torch.float16, device="cuda").uniform_(
+                            *sw["scale"], generator=gen).view(torch.int16)
+                        z = None if sym else torch.randint(0, 256, (N, zrow), dtype=torch.uint8, device="cuda",
+                                                           generator=gen)
+                        reps.append((c, sc, z))
+                    for M in sw["Ms"]:
+                        x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
+                        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                        with torch.cuda.stream(stream):
+                            for r in reps[:2]:
+                                q4.q4gemv_run(*r, x, y, M, N, K, g, stream=stream)
+                        torch.cuda.synchronize()
+                        est_us = max(2.0, wbytes / 5e3)
+                        n = int(max(nrep, min(400, 20000 / est_us)))
+                        gr = torch.cuda.CUDAGraph()
+                        with torch.cuda.graph(gr, stream=stream):
+                            for i in range(n):
+                                q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream)
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        with torch.cuda.stream(stream):
+                            gr.replay()
+                            e0.record(stream)
+                            gr.replay()
+                            gr.replay()
+                            e1.record(stream)
+                        torch.cuda.synchronize()
+                        us = e0.elapsed_time(e1) * 1e3 / (2 * n)
+                        byts = algorithmic_bytes(M, N, K, g, symmetric=sym)
+                        cells.append({"M": M, "N": N, "K": K, "group": g, "symmetric": sym,
+                                      "us_per_call": round(us, 3), "gbs": round(byts / us / 1e3, 1),
+                                      "packed_weight_bytes": wbytes,
+                                      "cold": nrep * wbytes >= 2 * L2_BYTES})
+                        del gr
+                    del reps
+                    torch.cuda.empty_cache()
+    big = [c for c in cells if c["M"] == 1 and c["packed_weight_bytes"] >= 64e6]
+    peak, peak_src = load_peaks()
+    summary = {"cells_m1_ge_64MB": len(big),
+               "min_gbs_m1_ge_64MB": min(c["gbs"] for c in big) if big else None,
+               "median_gbs_m1_ge_64MB": statistics.median(c["gbs"] for c in big) if big else None,
+               "peak": peak, "peak_source": peak_src}
+    return {"metric": "int4 GEMV sweep: us/call and achieved GB/s per cell", "unit": "GB/s",
+            "launch": "overlapped" if args.overlap else "serialised", "summary": summary, "cells": cells}
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local_rank = dist_env()
     if args.profile != "none":
         run_profile_case(args)
+        return 0
+    if args.sweep:
+        print(json.dumps(run_sweep(args)), flush=True)
         return 0
     if args.impl == "reference":
         res = run_reference(args, rank, world)

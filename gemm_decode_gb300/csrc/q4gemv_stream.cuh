@@ -5,6 +5,60 @@
 
 namespace q4 {
 
+// Row-block geometry and shared-memory carve-up of one launch (all sizes in bytes).
+// Block = ROWS = U * RG consecutive rows, one ring slot: codes | fp16 scales |
+// zero-point bytes (asymmetric only), each a contiguous stretch of the arrays.
+struct StreamGeo {
+    int C;        // 32-code chunks per row (K / 32)
+    int RG;       // row groups: consumer thread (r, c), r < RG, c < C
+    int NB;       // groups per row
+    int ZROW;     // zero-point bytes per row
+    int GSHIFT;   // log2(g / 32): chunk >> GSHIFT = group
+    int ROWS;     // rows per block
+    int TC;       // consumer threads (C * RG, whole warps)
+    int NWC;      // consumer warps
+    int CODE_B, SC_B, Z_B, SLOT_B;
+    int WRED;     // 1: a row spans whole warps (C % 32 == 0), partials per warp
+    int PARTS;    // partials per row
+    int RED_LD;   // floats per row of a partial-sum buffer
+    int RED_B;    // bytes of one partial-sum buffer
+    int OFF_RED, OFF_RING, OFF_BAR, OFF_FLAG, SMEM;
+};
+
+constexpr int kStreamU = 8;       // rows per consumer thread and block
+constexpr int kStreamD = 2;       // ring slots
+constexpr int kStreamNRed = 2;    // partial-sum buffers
+constexpr int kStreamMaxTC = 608; // consumer threads per CTA, at most
+
+__host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 128 * 128; }
+
+__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, bool asym) {
+    StreamGeo g{};
+    g.C = K / 32;
+    g.RG = RG;
+    g.NB = K / G;
+    g.ZROW = (g.NB + 1) / 2;
+    g.GSHIFT = G == 32 ? 0 : (G == 64 ? 1 : 2);
+    g.ROWS = kStreamU * RG;
+    g.TC = g.C * RG;
+    g.NWC = g.TC / 32;
+    g.CODE_B = g.ROWS * g.C * 16;
+    g.SC_B = g.ROWS * g.NB * 2;
+    g.Z_B = asym ? g.ROWS * g.ZROW : 0;
+    g.SLOT_B = stream_round128(g.CODE_B + g.SC_B + g.Z_B);
+    g.WRED = g.C % 32 == 0 ? 1 : 0;
+    g.PARTS = g.WRED ? g.C / 32 : g.C;
+    g.RED_LD = g.PARTS + 1;
+    g.RED_B = g.ROWS * g.RED_LD * 4;
+    // shared memory: x planes | partial sums [kStreamNRed] | ring [kStreamD] | barriers | abort flag
+    g.OFF_RED = stream_round128(g.C * 28 * 4);
+    g.OFF_RING = stream_round128(g.OFF_RED + kStreamNRed * g.RED_B);
+    g.OFF_BAR = g.OFF_RING + kStreamD * g.SLOT_B;
+    g.OFF_FLAG = g.OFF_BAR + 8 * (2 * kStreamD + 2 * kStreamNRed);
+    g.SMEM = g.OFF_FLAG + 16;
+    return g;
+}
+
 struct StreamArgs {
     const uint8_t *codes;
     const uint16_t *scales;
@@ -14,10 +68,13 @@ struct StreamArgs {
     int64_t N;
     int nblocks;                     // blocks of rows (set by the launcher)
     unsigned long long timeout_ns;   // bound on every mbarrier wait
+    unsigned int *status;            // device status word, set to 1 when a wait expires
+    StreamGeo geo;                   // used when the instance does not fix K and g
 };
 
-// True when the streamed kernel serves this problem (M = 1, a compiled row
-// geometry, 16-byte aligned side arrays, enough rows).
+// True when the streamed kernel serves this problem (M = 1, enough rows, a row
+// geometry whose blocks are whole warps and 16-byte multiples, 16-byte aligned
+// arrays, and a carve-up that fits the shared memory of one CTA).
 bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const void *scales, const void *zeros);
 int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                          float *y, int64_t N, int K, int group, cudaStream_t stream);

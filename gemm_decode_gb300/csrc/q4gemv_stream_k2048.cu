@@ -1,0 +1,9 @@
+// q4gemv_stream_k2048.cu -- compile-time row geometry of the streamed M = 1 GEMV for
+// K = 2048 (8 row groups per block), groups 32, 64 and 128.
+#include "q4gemv_stream_kernel.cuh"
+
+namespace q4 {
+
+Q4_STREAM_K_LAUNCHER(2048, 8)
+
+}  // namespace q4

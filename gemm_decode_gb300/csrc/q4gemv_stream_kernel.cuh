@@ -1,0 +1,307 @@
+// q4gemv_stream_kernel.cuh -- the TMA-streamed M = 1 int4 GEMV kernel template and
+// its launcher template.  Each q4gemv_stream_k*.cu instantiates the compile-time
+// row geometries of one K (in parallel translation units); q4gemv_stream.cu holds
+// the runtime-geometry instance and the dispatch.
+#pragma once
+
+#include "q4_common.cuh"
+#include "q4gemv_xplanes.cuh"
+#include "q4gemv_stream.cuh"
+
+namespace q4 {
+
+using namespace xp;
+
+namespace {
+
+// The geometry an instance works with: compile-time when the instance fixes K, g
+// and RG (the tuned decode shapes), else the launcher's.
+template <int KC, int GC, int RGC, bool ASYM>
+__device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
+    if constexpr (KC != 0) {
+        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, ASYM);
+        return g;
+    } else {
+        return rt;
+    }
+}
+
+}  // namespace
+
+template <int KC, int GC, int RGC, bool ASYM>
+__global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
+q4gemv_stream_kernel(const StreamArgs a) {
+    constexpr int U = kStreamU, D = kStreamD, NRED = kStreamNRed;
+    const StreamGeo G = geo_of<KC, GC, RGC, ASYM>(a.geo);
+    const int C = G.C;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    const uint32_t s_planes = sbase;
+    const uint32_t s_red = sbase + G.OFF_RED;
+    const uint32_t s_ring = sbase + G.OFF_RING;
+    const uint32_t bar0 = sbase + G.OFF_BAR;
+    const uint32_t s_flag = sbase + G.OFF_FLAG;
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (D + s); };
+    auto redfull = [&](int b) { return bar0 + 8u * (2 * D + b); };
+    auto reddone = [&](int b) { return bar0 + 8u * (2 * D + NRED + b); };
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const unsigned long long limit = a.timeout_ns;
+
+    // blocks of this CTA (contiguous range)
+    const int gsz = static_cast<int>(gridDim.x);
+    const int b_begin = static_cast<int>(static_cast<int64_t>(a.nblocks) * blockIdx.x / gsz);
+    const int b_end = static_cast<int>(static_cast<int64_t>(a.nblocks) * (blockIdx.x + 1) / gsz);
+    const int nbk = b_end - b_begin;
+
+    if (tid == 0) {
+        for (int s = 0; s < D; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), G.NWC);
+        }
+        for (int b = 0; b < NRED; ++b) {
+            mbar_init(redfull(b), G.NWC);
+            mbar_init(reddone(b), 1);
+        }
+        sts_volatile_u32(s_flag, 0u);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    allow_next_grid();
+
+    auto aborted = [&]() { return lds_volatile_u32(s_flag) != 0u; };
+    auto fail = [&]() {
+        sts_volatile_u32(s_flag, 1u);
+        atomicOr(a.status, 1u);
+    };
+
+    if (warp == G.NWC) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int issued = 0;
+            int s = 0, ph = 0;   // slot and its wrap parity
+            for (int i = 0; i < nbk && !aborted(); ++i) {
+                if (i >= D && !mbar_wait(empty(s), ph ^ 1, limit)) {
+                    fail();
+                    break;
+                }
+                const int64_t row0 = static_cast<int64_t>(b_begin + i) * G.ROWS;
+                const int rows = static_cast<int>(a.N - row0 < G.ROWS ? a.N - row0 : G.ROWS);
+                const uint32_t dst = s_ring + s * G.SLOT_B;
+                const unsigned char *src_c = a.codes + row0 * (C * 16);
+                const unsigned char *src_s = reinterpret_cast<const unsigned char *>(a.scales) + row0 * (G.NB * 2);
+                const unsigned char *src_z = ASYM ? a.zeros + row0 * G.ZROW : nullptr;
+                if (rows == G.ROWS) {
+                    mbar_expect_tx(full(s), G.CODE_B + G.SC_B + G.Z_B);
+                    bulk_copy(dst, src_c, G.CODE_B, full(s));
+                    bulk_copy(dst + G.CODE_B, src_s, G.SC_B, full(s));
+                    if (ASYM) bulk_copy(dst + G.CODE_B + G.SC_B, src_z, G.Z_B, full(s));
+                } else {
+                    // last, partial block: codes by bulk copy (rows * C * 16 bytes), the
+                    // scale and zero-point bytes by plain copies (their size need not be a
+                    // multiple of 16); the arrive below publishes the plain stores
+                    const int sb = rows * G.NB * 2, zb = rows * G.ZROW;
+                    unsigned char *sl = smem + G.OFF_RING + s * G.SLOT_B;
+                    for (int j = 0; j < sb; ++j) sl[G.CODE_B + j] = src_s[j];
+                    if (ASYM)
+                        for (int j = 0; j < zb; ++j) sl[G.CODE_B + G.SC_B + j] = src_z[j];
+                    mbar_expect_tx(full(s), rows * C * 16);
+                    bulk_copy(dst, src_c, rows * C * 16, full(s));
+                }
+                issued = i + 1;
+                if (++s == D) {
+                    s = 0;
+                    ph ^= 1;
+                }
+            }
+            if (aborted()) {
+                // drain (bounded): every issued copy lands before the CTA may exit
+                for (int i = issued - D > 0 ? issued - D : 0; i < issued; ++i)
+                    mbar_wait(full(i % D), (i / D) & 1, 50ull * 1000 * 1000);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // x and y may belong to the kernel before this one in the stream; the producer
+    // streams only weights and needs no such wait.
+    wait_prior_grid();
+    const int r = tid / C, c = tid - r * C;
+    // encode x into planes (four consumer threads per chunk), then a consumer-only barrier
+    uint32_t *planes = reinterpret_cast<uint32_t *>(smem);
+    for (int base = 0; base < C; base += G.TC / 4) {
+        const int i = base + (tid >> 2);
+        const bool in_range = i < C;
+        encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range, in_range, planes + (in_range ? i : 0) * kPlaneWords,
+                      tid & 3);
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
+    Planes P;
+    {
+        const uint32_t pa = s_planes + c * kPlaneWords * 4;
+        uint32_t w[28];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) {
+            const uint4 v = lds128(pa + 16 * i);
+            w[4 * i] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 24; ++i) P.p[i] = w[i];
+        P.s_lo = static_cast<int>(w[24]);
+        P.s_hi = static_cast<int>(w[25]);
+        P.f = __uint_as_float(w[27]);
+    }
+    const int grp = c >> G.GSHIFT;
+    // byte offsets of this thread's data inside a slot for sub-row u = 0, and the
+    // distance between sub-rows u and u + 1 (RG rows)
+    const uint32_t off_c = (r * C + c) * 16, str_c = G.RG * C * 16;
+    const uint32_t off_s = G.CODE_B + (r * G.NB + grp) * 2, str_s = G.RG * G.NB * 2;
+    const uint32_t off_z = G.CODE_B + G.SC_B + r * G.ZROW + (grp >> 1), str_z = G.RG * G.ZROW;
+    const int zsh = (grp & 1) * 4;
+    // where this thread's partial of sub-row u = 0 goes in a partial-sum buffer: with
+    // whole-warp rows, lane l of the warp holds the warp total of sub-row l >> NSH
+    constexpr int NSH = U == 1 ? 5 : (U == 2 ? 4 : (U == 4 ? 3 : (U == 8 ? 2 : (U == 16 ? 1 : 0))));
+    const bool red_writer = !G.WRED || (lane & ((1 << NSH) - 1)) == 0;
+    const int red_u = G.WRED ? (lane >> NSH) : 0;
+    const uint32_t red_off = G.WRED ? ((red_u * G.RG + r) * G.RED_LD + (c >> 5)) * 4 : (r * G.RED_LD + c) * 4;
+    const uint32_t str_red = G.RG * G.RED_LD * 4;
+
+    auto reduce_block = [&](int buf, int64_t row0) {
+        const uint32_t src = s_red + buf * G.RED_B;
+        for (int rho = lane; rho < G.ROWS; rho += 32) {
+            float acc = 0.0f;
+#pragma unroll 4
+            for (int q = 0; q < G.PARTS; ++q) acc += lds_f32(src + (rho * G.RED_LD + q) * 4);
+            if (row0 + rho < a.N) a.y[row0 + rho] = acc;
+        }
+    };
+
+    int s = 0, ph = 0;       // ring slot of block i and its wrap parity
+    int rb = 0, rph = 0;     // partial-sum buffer of block i and its wrap parity
+    int pb = 0, pph = 0;     // the same for block i - 1 (set at the end of each iteration)
+    for (int i = 0; i < nbk; ++i) {
+        if (aborted()) break;
+        if (!mbar_wait(full(s), ph, limit)) {
+            fail();
+            break;
+        }
+        if (i >= NRED && !mbar_wait(reddone(rb), rph ^ 1, limit)) {
+            fail();
+            break;
+        }
+        const uint32_t sl = s_ring + s * G.SLOT_B;
+        const uint32_t rd = s_red + rb * G.RED_B;
+        float v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint4 cw = lds128(sl + off_c + u * str_c);
+            const uint32_t sh = lds_u16(sl + off_s + u * str_s);
+            const int z = ASYM ? static_cast<int>((lds_u8(sl + off_z + u * str_z) >> zsh) & 0xFu) : 8;
+            const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sh)));
+            v[u] = (sc * P.f) * chunk_dot(cw, z, P);
+        }
+        if (G.WRED) {
+            const float t = warp_sum_many<U>(v, lane);
+            if (red_writer) sts_f32(rd + red_off, t);
+        } else {
+#pragma unroll
+            for (int u = 0; u < U; ++u) sts_f32(rd + red_off + u * str_red, v[u]);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(empty(s));      // slot s may be refilled
+            mbar_arrive(redfull(rb));   // this warp's partials of block i are written
+        }
+        // deferred reduction of block i-1 by one (rotating) consumer warp
+        if (i >= 1 && warp == (i - 1) % G.NWC) {
+            if (!mbar_wait(redfull(pb), pph, limit)) {
+                fail();
+                break;
+            }
+            reduce_block(pb, static_cast<int64_t>(b_begin + i - 1) * G.ROWS);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(reddone(pb));
+        }
+        pb = rb;
+        pph = rph;
+        if (++rb == NRED) {
+            rb = 0;
+            rph ^= 1;
+        }
+        if (++s == D) {
+            s = 0;
+            ph ^= 1;
+        }
+    }
+    // the last block's reduction
+    if (nbk > 0 && !aborted() && warp == (nbk - 1) % G.NWC) {
+        const int lb = (nbk - 1) % NRED;
+        if (!mbar_wait(redfull(lb), ((nbk - 1) / NRED) & 1, limit))
+            fail();
+        else
+            reduce_block(lb, static_cast<int64_t>(b_end - 1) * G.ROWS);
+    }
+}
+
+template <int KC, int GC, int RGC, bool ASYM>
+int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
+    auto kern = q4gemv_stream_kernel<KC, GC, RGC, ASYM>;
+    const StreamGeo &g = a0.geo;
+    const int T = g.TC + 32;
+    static int configured[64] = {};   // largest dynamic shared memory set so far, per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && configured[dev] < g.SMEM) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             device_info().smem_optin);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        configured[dev] = device_info().smem_optin;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, g.SMEM);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    if (per_sm < 1) return Q4_ERR_UNSUPPORTED;
+    StreamArgs a = a0;
+    a.nblocks = static_cast<int>((a.N + g.ROWS - 1) / g.ROWS);
+    int grid = per_sm * device_info().sms;
+    if (grid > a.nblocks) grid = a.nblocks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(T), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(g.SMEM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    add_overlap_attr(cfg, attr);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+
+// One translation unit per K instantiates the compile-time geometries of that K.
+#define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                          \
+    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, cudaStream_t s) {    \
+        switch (group) {                                                                    \
+            case 32: return asym ? launch_stream<KV, 32, RGV, true>(a, s) : launch_stream<KV, 32, RGV, false>(a, s);    \
+            case 64: return asym ? launch_stream<KV, 64, RGV, true>(a, s) : launch_stream<KV, 64, RGV, false>(a, s);    \
+            case 128: return asym ? launch_stream<KV, 128, RGV, true>(a, s) : launch_stream<KV, 128, RGV, false>(a, s); \
+            default: return Q4_ERR_UNSUPPORTED;                                             \
+        }                                                                                   \
+    }
+
+}  // namespace q4

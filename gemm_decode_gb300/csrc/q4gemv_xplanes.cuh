@@ -34,12 +34,17 @@ __device__ __forceinline__ void cp_wait() {
 
 // Encode one 32-element chunk of x into the plane layout, four threads per chunk
 // (the four consecutive lanes 4j..4j+3 of a warp; thread q owns elements
-// 8q..8q+7, i.e. code word q).  For word w (elements 8w..8w+7) and plane b,
-// word 6w+2b holds the b-th byte of m for the even elements 8w, 8w+2, 8w+4,
-// 8w+6 and word 6w+2b+1 that of the odd elements; plane 2 is the signed top
-// byte.  Words 24/25 hold the plane sums (planes 0+1 combined as s0 + 256 s1,
-// plane 2), word 27 the chunk scale 2^(E-22).  `valid` false encodes zeros;
-// `store` false skips the stores (the shuffles still run: all lanes take part).
+// 8q..8q+7, i.e. code word q).  With 2^E > max |x| over the chunk, an even
+// element k is held as m_k = rint(x_k 2^(22-E)) and an odd one as
+// m_k = rint(x_k 2^(18-E)): the odd (high-nibble) codes are used in place, as
+// 16 q, so the odd values carry a factor 16 less and 20 rather than 24 bits.
+// For word w (elements 8w..8w+7) and plane b, word 6w+2b holds the b-th byte of
+// m for the even elements 8w, 8w+2, 8w+4, 8w+6 and word 6w+2b+1 that of the
+// odd elements; plane 2 is the signed top byte.  Words 24/25 hold the plane
+// sums of the effective values (m for even, 16 m for odd: planes 0+1 combined
+// as sum of (byte0 + 256 byte1), plane 2), word 27 the chunk scale 2^(E-22).
+// `valid` false encodes zeros; `store` false skips the stores (the shuffles
+// still run: all lanes take part).
 __device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool store, uint32_t *pw, int q) {
     float v[8];
     if (valid) {
@@ -59,9 +64,10 @@ __device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool 
     int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 126;
     if (E < -100) E = -100;
     const float up = __uint_as_float(static_cast<uint32_t>(127 + 22 - E) << 23);   // 2^(22-E)
+    const float up_odd = __uint_as_float(static_cast<uint32_t>(127 + 18 - E) << 23);   // 2^(18-E)
     int m[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * up);                  // |m| <= 2^22
+    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * ((i & 1) ? up_odd : up));  // |m| <= 2^22
     // byte b of the four even (odd) elements -> one word, via byte permutes
 #pragma unroll
     for (int par = 0; par < 2; ++par) {
@@ -73,21 +79,21 @@ __device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool 
             if (store) pw[6 * q + 2 * b + par] = __byte_perm(t01, t23, 0x5410u);
         }
     }
-    int s0 = 0, s1 = 0, s2 = 0;
+    // plane sums of the effective values (odd elements count 16 times)
+    int s01 = 0, s2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        s0 += m[i] & 0xFF;
-        s1 += (m[i] >> 8) & 0xFF;
-        s2 += m[i] >> 16;   // arithmetic shift: the signed top byte
+        const int wgt = (i & 1) ? 16 : 1;
+        s01 += wgt * (m[i] & 0xFFFF);   // byte0 + 256 byte1
+        s2 += wgt * (m[i] >> 16);       // arithmetic shift: the signed top byte
     }
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s01 += __shfl_xor_sync(0xffffffffu, s01, o);
         s2 += __shfl_xor_sync(0xffffffffu, s2, o);
     }
     if (store && q == 0) {
-        pw[24] = static_cast<uint32_t>(s1 * 256 + s0);
+        pw[24] = static_cast<uint32_t>(s01);
         pw[25] = static_cast<uint32_t>(s2);
         pw[26] = 0u;
         pw[27] = __float_as_uint(__uint_as_float(static_cast<uint32_t>(127 + E - 22) << 23));  // 2^(E-22)
@@ -100,15 +106,17 @@ struct Planes {
     float f;
 };
 
-// Exact integer dot product of one 16-byte chunk with one x chunk, minus the
-// zero-point term, returned as the binary32 value sum_k (q_k - z) m_k.
+// Integer dot product of one 16-byte chunk with one x chunk, minus the
+// zero-point term: sum_k (q_k - z) m_eff_k (m_eff = m for even k, 16 m for odd k),
+// exact in int32 and returned as binary32 (the conversion of the planes-0/1 part,
+// |lo| < 2^30, may round once, by at most 2^-24 of it).
 __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes &P) {
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
     int a0 = 0, a1 = 0, a2 = 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const uint32_t lo = words[w] & 0x0F0F0F0Fu;          // codes of even k, one per byte
-        const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;   // codes of odd k
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu;   // codes of even k, one per byte
+        const uint32_t hi = words[w] & 0xF0F0F0F0u;   // 16 x codes of odd k, in place
         a0 = dp4a_uu(lo, P.p[6 * w + 0], a0);
         a0 = dp4a_uu(hi, P.p[6 * w + 1], a0);
         a1 = dp4a_uu(lo, P.p[6 * w + 2], a1);
@@ -116,7 +124,7 @@ __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes 
         a2 = dp4a_us(lo, P.p[6 * w + 4], a2);
         a2 = dp4a_us(hi, P.p[6 * w + 5], a2);
     }
-    const int lo = a1 * 256 + a0 - z * P.s_lo;   // planes 0 and 1: |lo| < 2^31
+    const int lo = a1 * 256 + a0 - z * P.s_lo;   // planes 0 and 1
     const int hi = a2 - z * P.s_hi;               // plane 2
     return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
 }
@@ -161,16 +169,88 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for the phase with the given parity to complete, for at most limit_ns.
+// try_wait with a suspend-time hint: the thread sleeps until the phase completes or
+// about hint_ns pass, instead of spinning through the issue slots of working warps.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete, for at most limit_ns
+// (checked between suspended tries of at most 20 us each).
 // A zero bound means one non-blocking test (the timer is too coarse to mean less).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (limit_ns == 0) return mbar_test(bar, parity);
-    if (mbar_try(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Explicit shared-memory accesses (32-bit shared-window addresses).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_volatile_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts_volatile_u32(uint32_t a, uint32_t v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Sum NV values per lane over the 32 lanes of a warp by recursive halving: each round
+// halves the values a lane carries while doubling the lanes it covers; butterflies
+// finish.  Returns the total of value index (lane >> (5 - log2 NV)) on every lane.
+template <int NV>
+__device__ __forceinline__ float warp_sum_many(float (&v)[NV], int lane) {
+    static_assert(NV == 1 || NV == 2 || NV == 4 || NV == 8 || NV == 16 || NV == 32, "NV must be a power of two <= 32");
+    int off = 16;
+#pragma unroll
+    for (int n = NV; n > 1; n >>= 1) {
+        const int half = n / 2;
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? v[i] : v[i + half];
+            const float keep = upper ? v[i + half] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+        off >>= 1;
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = off; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    return t;
 }
 // 1-D bulk copy global -> shared (TMA engine), completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_copy(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

@@ -215,3 +215,18 @@ def test_streamed_kernel_bounded_wait_reports_timeout_without_fault(torch):
     rows = _sample_rows(N, 64, 3)
     y_ref, bound = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, 32, rows)
     assert_within_bound(y2[:, rows], y_ref, bound, "after timeout")
+
+
+@pytest.mark.parametrize("K,g,N", [(896, 32, 9765), (896, 128, 9765), (2048, 64, 9777), (4096, 128, 4899),
+                                   (4096, 64, 4899), (8192, 32, 4103), (16384, 32, 4099),
+                                   (1152, 32, 9761), (14336, 128, 4101)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_streamed_kernel_ragged_last_block(torch, K, g, N, symmetric):
+    # M = 1 and many rows: the TMA-streamed kernel, with N not a multiple of its
+    # rows per block, so the last block is partial (codes by bulk copy, scales and
+    # zero points by plain copies); 1152 and 14336 take the runtime-geometry instance
+    w = synth.q4_weights(N + K + g, N, K, g, symmetric=symmetric, tag="ragged")
+    x = synth.activations_f32(N + g, 1, K)
+    y = run_gemv(torch, w, x)
+    y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, g)
+    assert_within_bound(y, y_ref, bound, f"N={N} K={K} g={g}")
