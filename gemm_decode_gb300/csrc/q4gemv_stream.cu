@@ -78,11 +78,12 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
     if (!aligned(codes, 16) || !aligned(scales, 16) || (zeros && !aligned(zeros, 16))) return false;
     const int rg = stream_rg(K);
     if (rg == 0) return false;
-    const StreamGeo g = make_stream_geo(K, group, rg, zeros != nullptr);
-    // at least one block of rows per SM; below that the register-resident kernel's
-    // finer row split keeps more SMs busy
-    if ((N + g.ROWS - 1) / g.ROWS < device_info().sms) return false;
-    return stream_geo_ok(g, zeros != nullptr);
+    const bool asym = zeros != nullptr;
+    const StreamGeo g = make_stream_geo(K, group, rg, stream_slots(K, group, rg, asym), asym);
+    // short rows (K < 2048): at least one block of rows per SM, below which the
+    // register-resident kernel's finer row split keeps more SMs busy
+    if (K < 2048 && (N + g.ROWS - 1) / g.ROWS < device_info().sms) return false;
+    return stream_geo_ok(g, asym);
 }
 
 static unsigned long long g_stream_timeout_ns = 1000ull * 1000 * 1000;
@@ -104,7 +105,7 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
     a.timeout_ns = g_stream_timeout_ns;
     a.status = stream_status_word();
     if (a.status == nullptr) return Q4_ERR_CUDA;
-    a.geo = make_stream_geo(K, group, rg, asym);
+    a.geo = make_stream_geo(K, group, rg, stream_slots(K, group, rg, asym), asym);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
     switch (K) {

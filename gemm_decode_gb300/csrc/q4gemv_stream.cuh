@@ -22,17 +22,19 @@ struct StreamGeo {
     int PARTS;    // partials per row
     int RED_LD;   // floats per row of a partial-sum buffer
     int RED_B;    // bytes of one partial-sum buffer
+    int D;        // ring slots
     int OFF_RED, OFF_RING, OFF_BAR, OFF_FLAG, SMEM;
 };
 
 constexpr int kStreamU = 8;       // rows per consumer thread and block
-constexpr int kStreamD = 2;       // ring slots
 constexpr int kStreamNRed = 2;    // partial-sum buffers
 constexpr int kStreamMaxTC = 608; // consumer threads per CTA, at most
+constexpr int kStreamSmemBudget = 227 * 1024;   // opt-in shared memory per CTA on this GPU
+constexpr int kStreamSmemPerSM = 228 * 1024;    // shared memory per SM (1 KB of it reserved per CTA)
 
 __host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 128 * 128; }
 
-__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, bool asym) {
+__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int D, bool asym) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
@@ -50,13 +52,23 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, bo
     g.PARTS = g.WRED ? g.C / 32 : g.C;
     g.RED_LD = g.PARTS + 1;
     g.RED_B = g.ROWS * g.RED_LD * 4;
-    // shared memory: x planes | partial sums [kStreamNRed] | ring [kStreamD] | barriers | abort flag
+    g.D = D;
+    // shared memory: x planes | partial sums [kStreamNRed] | ring [D] | barriers | abort flag
     g.OFF_RED = stream_round128(g.C * 28 * 4);
     g.OFF_RING = stream_round128(g.OFF_RED + kStreamNRed * g.RED_B);
-    g.OFF_BAR = g.OFF_RING + kStreamD * g.SLOT_B;
-    g.OFF_FLAG = g.OFF_BAR + 8 * (2 * kStreamD + 2 * kStreamNRed);
+    g.OFF_BAR = g.OFF_RING + D * g.SLOT_B;
+    g.OFF_FLAG = g.OFF_BAR + 8 * (2 * D + 2 * kStreamNRed);
     g.SMEM = g.OFF_FLAG + 16;
     return g;
+}
+
+// Ring slots: three (one more block in flight) when they fit the shared-memory
+// budget without lowering the CTAs an SM holds, else two.
+__host__ __device__ constexpr int stream_ctas_per_sm(int smem) { return kStreamSmemPerSM / (smem + 1024); }
+__host__ __device__ constexpr int stream_slots(int K, int G, int RG, bool asym) {
+    const int s2 = make_stream_geo(K, G, RG, 2, asym).SMEM;
+    const int s3 = make_stream_geo(K, G, RG, 3, asym).SMEM;
+    return (s3 <= kStreamSmemBudget && stream_ctas_per_sm(s3) >= stream_ctas_per_sm(s2)) ? 3 : 2;
 }
 
 struct StreamArgs {

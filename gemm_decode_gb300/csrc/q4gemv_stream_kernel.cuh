@@ -19,7 +19,7 @@ namespace {
 template <int KC, int GC, int RGC, bool ASYM>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
-        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, ASYM);
+        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, stream_slots(KC, GC, RGC, ASYM), ASYM);
         return g;
     } else {
         return rt;
@@ -31,8 +31,9 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 template <int KC, int GC, int RGC, bool ASYM>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgs a) {
-    constexpr int U = kStreamU, D = kStreamD, NRED = kStreamNRed;
+    constexpr int U = kStreamU, NRED = kStreamNRed;
     const StreamGeo G = geo_of<KC, GC, RGC, ASYM>(a.geo);
+    const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
