@@ -58,8 +58,8 @@ NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # the instance below on the LM-head shape (see profiles/); None once the kernel changes.
-DOMINANT_KERNEL = "q4gemv_stream_kernel<C=28, RG=8, G=32, ASYM, U=4, D=3>"
-DOMINANT_TRAFFIC_BYTES = 78_732_032 + 772_352
+DOMINANT_KERNEL = "q4gemv_stream_kernel<K=896, g=32, RG=8, ASYM> (U=8 rows per thread, 2 ring slots)"
+DOMINANT_TRAFFIC_BYTES = 78_733_056 + 947_712
 
 
 def algorithmic_bytes(M, N, K, group, symmetric=False):
@@ -389,6 +389,7 @@ def run_gpu(args, rank, world, local_rank):
     if args.controls and rank == 0:
         detail["controls"] = run_controls(args, torch, q4)
         detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
+        detail["decode_8b"] = run_decode_8b(args, torch, q4)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -745,6 +746,63 @@ def run_profile_case(args):
     print(json.dumps({"profile": args.profile, "launches": 7}))
 
 
+def _device_q4(torch, gen, N, K, g, symmetric, scale):
+    """Packed weights drawn on the device (timing inputs only; parity is the tests' job)."""
+    nb = K // g
+    c = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
+    sc = torch.empty((N, nb), dtype=torch.float16, device="cuda").uniform_(*scale, generator=gen).view(torch.int16)
+    z = None if symmetric else torch.randint(0, 256, (N, (nb + 1) // 2), dtype=torch.uint8, device="cuda",
+                                             generator=gen)
+    return c, sc, z
+
+
+def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n):
+    """Microseconds per q4gemv_run call: a CUDA graph of n launches over the replicas,
+    replayed once untimed, then twice between events on the launching stream."""
+    nrep = len(reps)
+    with torch.cuda.stream(stream):
+        for r in reps[:2]:
+            q4.q4gemv_run(*r, x, y, M, N, K, g, stream=stream)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(n):
+            q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        gr.replay()
+        e0.record(stream)
+        gr.replay()
+        gr.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (2 * n)
+
+
+def run_decode_8b(args, torch, q4):
+    """The 8B-class decode shapes (g = 128, M in 1, 2, 4, 8): microseconds per call and
+    GB/s from back-to-back launches over rotating replicas (cold in HBM)."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(8)
+    stream = torch.cuda.Stream()
+    g = synth.DECODE_8B["group"]
+    out = []
+    for name, N, K in synth.DECODE_8B["shapes"]:
+        wbytes = N * K // 2 + N * (K // g) * 2 + N * ((K // g + 1) // 2)
+        nrep = int(max(2, -(-6 * L2_BYTES // wbytes)))
+        reps = [_device_q4(torch, gen, N, K, g, False, synth.DECODE_8B["scale"]) for _ in range(nrep)]
+        for M in synth.DECODE_8B["Ms"]:
+            x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
+            y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            n = int(max(nrep, min(200, 20000 / max(2.0, wbytes / 5e3))))
+            us = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
+            out.append({"name": name, "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
+                        "gbs": round(algorithmic_bytes(M, N, K, g) / us / 1e3, 1)})
+        del reps
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_sweep(args):
     """Every cell of the shape sweep (M, K, N, group, symmetric): microseconds per
     q4gemv_run call and achieved GB/s, from a CUDA graph of back-to-back launches over
@@ -767,42 +825,18 @@ def run_sweep(args):
                 for sym in sw["symmetric"]:
                     wbytes = N * K // 2 + N * nb * 2 + (0 if sym else N * zrow)
                     nrep = int(min(256, max(2, -(-6 * L2_BYTES // wbytes))))
-                    reps = []
-                    for _ in range(nrep):
-                        c = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, device="cuda", generator=gen)
-                        sc = torch.empty((N, nb), dtype=torch.float16, device="cuda").uniform_(
-                            *sw["scale"], generator=gen).view(torch.int16)
-                        z = None if sym else torch.randint(0, 256, (N, zrow), dtype=torch.uint8, device="cuda",
-                                                           generator=gen)
-                        reps.append((c, sc, z))
+                    reps = [_device_q4(torch, gen, N, K, g, sym, sw["scale"]) for _ in range(nrep)]
                     for M in sw["Ms"]:
                         x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
                         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-                        with torch.cuda.stream(stream):
-                            for r in reps[:2]:
-                                q4.q4gemv_run(*r, x, y, M, N, K, g, stream=stream)
-                        torch.cuda.synchronize()
                         est_us = max(2.0, wbytes / 5e3)
                         n = int(max(nrep, min(400, 20000 / est_us)))
-                        gr = torch.cuda.CUDAGraph()
-                        with torch.cuda.graph(gr, stream=stream):
-                            for i in range(n):
-                                q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream)
-                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                        with torch.cuda.stream(stream):
-                            gr.replay()
-                            e0.record(stream)
-                            gr.replay()
-                            gr.replay()
-                            e1.record(stream)
-                        torch.cuda.synchronize()
-                        us = e0.elapsed_time(e1) * 1e3 / (2 * n)
+                        us = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
                         byts = algorithmic_bytes(M, N, K, g, symmetric=sym)
                         cells.append({"M": M, "N": N, "K": K, "group": g, "symmetric": sym,
                                       "us_per_call": round(us, 3), "gbs": round(byts / us / 1e3, 1),
                                       "packed_weight_bytes": wbytes,
                                       "cold": nrep * wbytes >= 2 * L2_BYTES})
-                        del gr
                     del reps
                     torch.cuda.empty_cache()
     big = [c for c in cells if c["M"] == 1 and c["packed_weight_bytes"] >= 64e6]
