@@ -67,6 +67,7 @@ static int stream_rg(int K) {
 
 static bool stream_geo_ok(const StreamGeo &g, bool asym) {
     if (g.TC % 32 != 0 || g.TC > kStreamMaxTC) return false;
+    if (g.WRED && (g.U & (g.U - 1)) != 0) return false;                  // warp sums need a power of two
     if (g.SC_B % 16 != 0 || (asym && g.Z_B % 16 != 0)) return false;   // bulk copies: 16-byte multiples
     if (g.CODE_B + g.SC_B + g.Z_B >= (1 << 20)) return false;            // mbarrier transaction count
     return g.SMEM <= device_info().smem_optin;
@@ -79,7 +80,8 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
     const int rg = stream_rg(K);
     if (rg == 0) return false;
     const bool asym = zeros != nullptr;
-    const StreamGeo g = make_stream_geo(K, group, rg, stream_slots(K, group, rg, asym), asym);
+    const int u = stream_u(K);
+    const StreamGeo g = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);
     // short rows (K < 2048): at least one block of rows per SM, below which the
     // register-resident kernel's finer row split keeps more SMs busy
     if (K < 2048 && (N + g.ROWS - 1) / g.ROWS < device_info().sms) return false;
@@ -105,7 +107,8 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
     a.timeout_ns = g_stream_timeout_ns;
     a.status = stream_status_word();
     if (a.status == nullptr) return Q4_ERR_CUDA;
-    a.geo = make_stream_geo(K, group, rg, stream_slots(K, group, rg, asym), asym);
+    const int u = stream_u(K);
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
     switch (K) {
@@ -114,7 +117,8 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
         case 4096: return launch_stream_k4096(a, group, asym, stream);
         case 8192: return launch_stream_k8192(a, group, asym, stream);
         case 16384: return launch_stream_k16384(a, group, asym, stream);
-        default: return asym ? launch_stream<0, 0, 0, true>(a, stream) : launch_stream<0, 0, 0, false>(a, stream);
+        default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
+            return asym ? launch_stream<0, 0, 0, 8, true>(a, stream) : launch_stream<0, 0, 0, 8, false>(a, stream);
     }
 }
 

@@ -14,7 +14,8 @@ struct StreamGeo {
     int NB;       // groups per row
     int ZROW;     // zero-point bytes per row
     int GSHIFT;   // log2(g / 32): chunk >> GSHIFT = group
-    int ROWS;     // rows per block
+    int U;        // rows per consumer thread and block
+    int ROWS;     // rows per block (U * RG)
     int TC;       // consumer threads (C * RG, whole warps)
     int NWC;      // consumer warps
     int CODE_B, SC_B, Z_B, SLOT_B;
@@ -26,7 +27,6 @@ struct StreamGeo {
     int OFF_RED, OFF_RING, OFF_BAR, OFF_FLAG, SMEM;
 };
 
-constexpr int kStreamU = 8;       // rows per consumer thread and block
 constexpr int kStreamNRed = 2;    // partial-sum buffers
 constexpr int kStreamMaxTC = 608; // consumer threads per CTA, at most
 constexpr int kStreamSmemBudget = 227 * 1024;   // opt-in shared memory per CTA on this GPU
@@ -34,14 +34,19 @@ constexpr int kStreamSmemPerSM = 228 * 1024;    // shared memory per SM (1 KB of
 
 __host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 128 * 128; }
 
-__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int D, bool asym) {
+// Rows per consumer thread and block: 6 for K = 896 (48-row blocks: three CTAs fit an
+// SM), 8 otherwise.  Rows that span whole warps (K % 1024 == 0) need a power of two.
+__host__ __device__ constexpr int stream_u(int K) { return K == 896 ? 6 : 8; }
+
+__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
     g.NB = K / G;
     g.ZROW = (g.NB + 1) / 2;
     g.GSHIFT = G == 32 ? 0 : (G == 64 ? 1 : 2);
-    g.ROWS = kStreamU * RG;
+    g.U = U;
+    g.ROWS = U * RG;
     g.TC = g.C * RG;
     g.NWC = g.TC / 32;
     g.CODE_B = g.ROWS * g.C * 16;
@@ -65,9 +70,9 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
 // Ring slots: three (one more block in flight) when they fit the shared-memory
 // budget without lowering the CTAs an SM holds, else two.
 __host__ __device__ constexpr int stream_ctas_per_sm(int smem) { return kStreamSmemPerSM / (smem + 1024); }
-__host__ __device__ constexpr int stream_slots(int K, int G, int RG, bool asym) {
-    const int s2 = make_stream_geo(K, G, RG, 2, asym).SMEM;
-    const int s3 = make_stream_geo(K, G, RG, 3, asym).SMEM;
+__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym) {
+    const int s2 = make_stream_geo(K, G, RG, U, 2, asym).SMEM;
+    const int s3 = make_stream_geo(K, G, RG, U, 3, asym).SMEM;
     return (s3 <= kStreamSmemBudget && stream_ctas_per_sm(s3) >= stream_ctas_per_sm(s2)) ? 3 : 2;
 }
 

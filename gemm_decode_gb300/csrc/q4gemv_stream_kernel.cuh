@@ -16,10 +16,10 @@ namespace {
 
 // The geometry an instance works with: compile-time when the instance fixes K, g
 // and RG (the tuned decode shapes), else the launcher's.
-template <int KC, int GC, int RGC, bool ASYM>
+template <int KC, int GC, int RGC, int UC, bool ASYM>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
-        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, stream_slots(KC, GC, RGC, ASYM), ASYM);
+        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM), ASYM);
         return g;
     } else {
         return rt;
@@ -28,11 +28,14 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 
 }  // namespace
 
-template <int KC, int GC, int RGC, bool ASYM>
+// UC: rows per consumer thread and block (compile-time in every instance; the host
+// geometry carries the same value).
+template <int KC, int GC, int RGC, int UC, bool ASYM>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgs a) {
-    constexpr int U = kStreamU, NRED = kStreamNRed;
-    const StreamGeo G = geo_of<KC, GC, RGC, ASYM>(a.geo);
+    constexpr int U = UC, NRED = kStreamNRed;
+    constexpr bool U_POW2 = (U & (U - 1)) == 0;
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -100,16 +103,20 @@ q4gemv_stream_kernel(const StreamArgs a) {
                     bulk_copy(dst + G.CODE_B, src_s, G.SC_B, full(s));
                     if (ASYM) bulk_copy(dst + G.CODE_B + G.SC_B, src_z, G.Z_B, full(s));
                 } else {
-                    // last, partial block: codes by bulk copy (rows * C * 16 bytes), the
-                    // scale and zero-point bytes by plain copies (their size need not be a
-                    // multiple of 16); the arrive below publishes the plain stores
-                    const int sb = rows * G.NB * 2, zb = rows * G.ZROW;
+                    // last, partial block: the codes (rows * C * 16 bytes) and the largest
+                    // 16-byte multiples of the scale and zero-point stretches by bulk copy,
+                    // the at most 15 bytes left of each by plain copies, which the arrive
+                    // below publishes (the stretches start 16-byte aligned: a whole block's
+                    // scale and zero bytes are multiples of 16)
+                    const int sb = rows * G.NB * 2, zb = ASYM ? rows * G.ZROW : 0;
+                    const int sb16 = sb & ~15, zb16 = zb & ~15;
                     unsigned char *sl = smem + G.OFF_RING + s * G.SLOT_B;
-                    for (int j = 0; j < sb; ++j) sl[G.CODE_B + j] = src_s[j];
-                    if (ASYM)
-                        for (int j = 0; j < zb; ++j) sl[G.CODE_B + G.SC_B + j] = src_z[j];
-                    mbar_expect_tx(full(s), rows * C * 16);
+                    for (int j = sb16; j < sb; ++j) sl[G.CODE_B + j] = src_s[j];
+                    for (int j = zb16; j < zb; ++j) sl[G.CODE_B + G.SC_B + j] = src_z[j];
+                    mbar_expect_tx(full(s), rows * C * 16 + sb16 + zb16);
                     bulk_copy(dst, src_c, rows * C * 16, full(s));
+                    if (sb16 > 0) bulk_copy(dst + G.CODE_B, src_s, sb16, full(s));
+                    if (zb16 > 0) bulk_copy(dst + G.CODE_B + G.SC_B, src_z, zb16, full(s));
                 }
                 issued = i + 1;
                 if (++s == D) {
@@ -207,10 +214,15 @@ q4gemv_stream_kernel(const StreamArgs a) {
             const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sh)));
             v[u] = (sc * P.f) * chunk_dot(cw, z, P);
         }
-        if (G.WRED) {
-            const float t = warp_sum_many<U>(v, lane);
-            if (red_writer) sts_f32(rd + red_off, t);
-        } else {
+        bool summed = false;
+        if constexpr (U_POW2) {
+            if (G.WRED) {   // (the host pairs whole-warp rows with a power-of-two U only)
+                const float t = warp_sum_many<U>(v, lane);
+                if (red_writer) sts_f32(rd + red_off, t);
+                summed = true;
+            }
+        }
+        if (!summed) {
 #pragma unroll
             for (int u = 0; u < U; ++u) sts_f32(rd + red_off + u * str_red, v[u]);
         }
@@ -250,9 +262,9 @@ q4gemv_stream_kernel(const StreamArgs a) {
     }
 }
 
-template <int KC, int GC, int RGC, bool ASYM>
+template <int KC, int GC, int RGC, int UC, bool ASYM>
 int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
-    auto kern = q4gemv_stream_kernel<KC, GC, RGC, ASYM>;
+    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM>;
     const StreamGeo &g = a0.geo;
     const int T = g.TC + 32;
     static int configured[64] = {};   // largest dynamic shared memory set so far, per device
@@ -295,14 +307,18 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
 
 
 // One translation unit per K instantiates the compile-time geometries of that K.
-#define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                          \
-    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, cudaStream_t s) {    \
-        switch (group) {                                                                    \
-            case 32: return asym ? launch_stream<KV, 32, RGV, true>(a, s) : launch_stream<KV, 32, RGV, false>(a, s);    \
-            case 64: return asym ? launch_stream<KV, 64, RGV, true>(a, s) : launch_stream<KV, 64, RGV, false>(a, s);    \
-            case 128: return asym ? launch_stream<KV, 128, RGV, true>(a, s) : launch_stream<KV, 128, RGV, false>(a, s); \
-            default: return Q4_ERR_UNSUPPORTED;                                             \
-        }                                                                                   \
+#define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
+    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, cudaStream_t s) {              \
+        constexpr int UV = stream_u(KV);                                                              \
+        switch (group) {                                                                              \
+            case 32: return asym ? launch_stream<KV, 32, RGV, UV, true>(a, s)                         \
+                                 : launch_stream<KV, 32, RGV, UV, false>(a, s);                       \
+            case 64: return asym ? launch_stream<KV, 64, RGV, UV, true>(a, s)                         \
+                                 : launch_stream<KV, 64, RGV, UV, false>(a, s);                       \
+            case 128: return asym ? launch_stream<KV, 128, RGV, UV, true>(a, s)                       \
+                                  : launch_stream<KV, 128, RGV, UV, false>(a, s);                     \
+            default: return Q4_ERR_UNSUPPORTED;                                                       \
+        }                                                                                             \
     }
 
 }  // namespace q4
