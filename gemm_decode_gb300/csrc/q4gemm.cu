@@ -5,18 +5,22 @@
 // "Dequantization"; its optimisation note "pre-dequantize tiles ... then
 // tiled multiply" is what this kernel does, on tcgen05).
 //
-// One CTA computes a 128 x 128 tile of C with UMMA (tcgen05.mma, kind::f16,
-// bf16 inputs, f32 accumulator in tensor memory), K in blocks of 64:
-//   warp 0      TMA producer: A tile [128 m x 64 k] bf16 -> shared memory,
+// One CTA computes an (NH * 128) x 128 tile of C with UMMA (tcgen05.mma,
+// kind::f16, bf16 inputs, f32 accumulators in tensor memory), K in blocks of 64.
+// With NH = 2 the CTA holds two 128-row halves of A against one dequantised
+// weight tile, so each weight tile is dequantised once per 256 rows of A:
+//   warp 0      TMA producer: A tile [NH*128 m x 64 k] bf16 -> shared memory,
 //               128-byte swizzled, completion counted on an mbarrier;
-//   warp 1      allocates 128 TMEM columns; one lane issues 4 MMAs per
-//               K-block and commits them to the stage's "empty" barrier;
+//   warp 1      allocates NH*128 TMEM columns; one lane issues NH*4 MMAs per
+//               K-block (one accumulator per half) and commits them to the
+//               stage's "empty" barrier;
 //   warps 2..9  dequantisers: each thread turns 32 codes of one weight row
 //               into exact binary32 (q - z) * s, rounds to bf16 (nearest
 //               even) and stores them in the same swizzled K-major layout
 //               the MMA reads; then fence.proxy.async and arrive;
-//   warps 2..5  afterwards read the accumulator (tcgen05.ld, one TMEM lane
-//               per thread) and store C in binary32.
+//   warps 2..9  afterwards read the accumulators (tcgen05.ld, one TMEM lane
+//               per thread; warp w reads lane quadrant w % 4 of half
+//               (w - 2) / 4) and store C in binary32.
 // A 4-stage ring of (A, B) tiles overlaps TMA, dequantisation and MMA.
 // Every mbarrier wait is bounded by a %globaltimer deadline; on expiry the
 // CTA raises a device status flag (read by q4gemv_device_status), stops
@@ -37,11 +41,9 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int kDequantWarps = 8;
 constexpr int kThreads = (2 + kDequantWarps) * 32;
-constexpr int kTileBytes = BM * BK * 2;   // 16 KB for A, same for B
-constexpr int kTmemCols = BN;
+constexpr int kTileBytes = BM * BK * 2;   // 16 KB: one 128-row half of A, or B
 
 struct GemmArgs {
     const uint8_t *codes;
@@ -141,15 +143,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 }  // namespace
 
+// NH: 128-row halves of A per CTA (1..4); STAGES: depth of the (A, B) ring.
+template <int NH, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
+    // TMEM allocations are powers of two columns, at least 32
+    constexpr int kTmemCols = NH * BN <= 128 ? 128 : (NH * BN <= 256 ? 256 : 512);
+    constexpr int kATile = NH * kTileBytes;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned tile area (swizzle atoms are address-based)
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    unsigned char *tiles_a = smem;                               // STAGES x 16 KB
-    unsigned char *tiles_b = smem + STAGES * kTileBytes;         // STAGES x 16 KB
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + 2 * STAGES * kTileBytes);
+    unsigned char *tiles_a = smem;                               // STAGES x NH x 16 KB
+    unsigned char *tiles_b = smem + STAGES * kATile;             // STAGES x 16 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * (kATile + kTileBytes));
     // bars: full_a[S], full_b[S], empty[S], done
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3 * STAGES + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -157,7 +164,7 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BN;
-    const int m0 = blockIdx.y * BM;
+    const int m0 = blockIdx.y * (NH * BM);
     const int kblocks = (g.K + BK - 1) / BK;
 
     const uint32_t bar0 = smem_addr(bars);
@@ -202,8 +209,11 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
                     fail();
                     break;
                 }
-                mbar_expect_tx(full_a(s), kTileBytes);
-                tma_load_2d(smem_addr(tiles_a + s * kTileBytes), &tmap_a, full_a(s), kb * BK, m0);
+                mbar_expect_tx(full_a(s), kATile);
+#pragma unroll
+                for (int h = 0; h < NH; ++h)   // one 128-row box per half
+                    tma_load_2d(smem_addr(tiles_a + s * kATile + h * kTileBytes), &tmap_a, full_a(s), kb * BK,
+                                m0 + h * BM);
                 issued = kb + 1;
             }
             if (*abort_flag) {
@@ -223,13 +233,18 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a_base = smem_addr(tiles_a + s * kTileBytes);
+                const uint32_t a_base = smem_addr(tiles_a + s * kATile);
                 const uint32_t b_base = smem_addr(tiles_b + s * kTileBytes);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    // advancing 16 bf16 = 32 bytes inside the 128-byte swizzle span
-                    umma_bf16(tmem, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32),
-                              (kb > 0 || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < NH; ++h) {
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // advancing 16 bf16 = 32 bytes inside the 128-byte swizzle span; half h
+                        // of A starts 16 KB (16 swizzle atoms) further, its accumulator 128
+                        // TMEM columns further
+                        umma_bf16(tmem + h * BN, umma_desc(a_base + h * kTileBytes + kk * 32),
+                                  umma_desc(b_base + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(empty(s));
             }
@@ -313,19 +328,20 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
             fence_proxy_async();      // generic-proxy stores -> visible to the tensor core
             mbar_arrive(full_b(s));
         }
-        // ------------------------------------------------------------ epilogue (warps 2..5)
-        if (warp < 6) {
+        // ------------------------------------------------------------ epilogue
+        // warps 2..5 read halves 0, 2, ..., warps 6..9 halves 1, 3, ...
+        for (int eh = (warp - 2) >> 2; eh < NH; eh += 2) {
             const int quad = warp & 3;             // TMEM lane quadrant this warp may access
             const int r = quad * 32 + lane;        // accumulator row = TMEM lane
             const bool ok = mbar_wait(done_bar, 0, limit);
             if (!ok) fail();
             if (ok && !*abort_flag) {
                 tc_fence_after();
-                const int m = m0 + r;
+                const int m = m0 + eh * BM + r;
 #pragma unroll 1
                 for (int cb = 0; cb < BN / 32; ++cb) {
                     uint32_t v[32];
-                    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + cb * 32;
+                    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + eh * BN + cb * 32;
                     asm volatile(
                         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
                         "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -392,13 +408,55 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-size_t gemm_smem_bytes() { return 1024 + 2 * STAGES * kTileBytes + 8 * (3 * STAGES + 1) + 16; }
+// Halves of A per CTA for M rows: the fewest padded rows plus dequantisation, counting
+// one dequantised weight tile as much work as 256 rows of MMA (the dequantiser warps,
+// not the tensor core, set the pace at the prefill shapes).
+static int gemm_halves(int M) {
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int nh = 4; nh >= 1; --nh) {
+        const int64_t tiles = (M + nh * BM - 1) / (nh * BM);
+        const int64_t cost = tiles * nh * BM + tiles * 2 * BM;
+        if (best_cost < 0 || cost < best_cost) {
+            best = nh;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+size_t gemm_smem_bytes(int nh, int stages) {
+    return 1024 + static_cast<size_t>(stages) * (nh + 1) * kTileBytes + 8 * (3 * stages + 1) + 16;
+}
+
+template <int NH, int STAGES>
+static int launch_tc(const CUtensorMap &map, const GemmArgs &g, int M, int64_t N, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = gemm_smem_bytes(NH, STAGES);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(q4gemm_tc_kernel<NH, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        configured[dev] = true;
+    }
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + NH * BM - 1) / (NH * BM)));
+    if (grid.y > 65535) return Q4_ERR_UNSUPPORTED;
+    q4gemm_tc_kernel<NH, STAGES><<<grid, kThreads, smem, stream>>>(map, g);
+    return launch_status();
+}
 
 int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const uint16_t *a, float *c,
                   int M, int64_t N, int K, int group, cudaStream_t stream) {
     if (K % 8 != 0) return Q4_ERR_UNSUPPORTED;   // TMA row pitch must be a multiple of 16 bytes
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode == nullptr) return Q4_ERR_CUDA;
+    // 128-row halves of A per CTA: each dequantised weight tile then serves nh * 128 rows
+    const int nh = gemm_halves(M);
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
@@ -408,19 +466,6 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return Q4_ERR_UNSUPPORTED;
-    static bool configured[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    const size_t smem = gemm_smem_bytes();
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(q4gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) {
-            set_cuda_error(e);
-            return Q4_ERR_CUDA;
-        }
-        configured[dev] = true;
-    }
     GemmArgs g;
     g.codes = codes;
     g.scales = scales;
@@ -434,10 +479,12 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
     g.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
     g.c_vec = (aligned(c, 16) && (N % 4) == 0) ? 1 : 0;
     g.timeout_ns = g_timeout_ns;
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
-    if (grid.y > 65535) return Q4_ERR_UNSUPPORTED;
-    q4gemm_tc_kernel<<<grid, kThreads, smem, stream>>>(map, g);
-    return launch_status();
+    switch (nh) {
+        case 4: return launch_tc<4, 2>(map, g, M, N, stream);
+        case 3: return launch_tc<3, 3>(map, g, M, N, stream);
+        case 2: return launch_tc<2, 4>(map, g, M, N, stream);
+        default: return launch_tc<1, 4>(map, g, M, N, stream);
+    }
 }
 
 int read_device_status(cudaStream_t stream) {

@@ -76,8 +76,11 @@ def test_hand_worked_examples_exact(torch, name):
 @pytest.mark.parametrize("g", [32, 64, 128])
 @pytest.mark.parametrize("symmetric", [False, True])
 def test_small_shapes(torch, g, symmetric):
+    # M > 128 takes tiles of 2, 3 or 4 128-row halves of A per CTA: 130 and 256 use two
+    # halves (the second partly empty, then full), 300 and 513 three (one and two
+    # tiles), 500 four; the last tile's halves run partly or wholly past M
     for M, N, K in [(1, 128, 128), (7, 200, 256), (128, 128, 2 * 64), (130, 256, 384), (300, 136, 512),
-                    (64, 384, 1024 if g <= 64 else 1152)]:
+                    (64, 384, 1024 if g <= 64 else 1152), (256, 128, 256), (513, 264, 384), (500, 136, 256)]:
         if K % g:
             continue
         w = synth.q4_weights(M + N + K + g, N, K, g, symmetric=symmetric)
