@@ -390,6 +390,8 @@ def run_gpu(args, rank, world, local_rank):
         detail["controls"] = run_controls(args, torch, q4)
         detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
         detail["decode_8b"] = run_decode_8b(args, torch, q4)
+        detail["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas,
+                                                          stream)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -812,6 +814,56 @@ def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n):
         e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / (2 * n)
+
+
+def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
+    """The decode step with q|k|v and gate|up stacked along N (the weight rows of
+    projections that share x, concatenated): 4 launches per step instead of 7, the
+    same weight bytes.  A CUDA graph of back-to-back steps over the replicas."""
+    names = [n for n, _, _ in shapes]
+    groups = [["q_proj", "k_proj", "v_proj"], ["gate_proj", "up_proj"], ["down_proj"], ["lm_head"]]
+    idx = [[names.index(n) for n in gr] for gr in groups]
+    fshapes, freps = [], []
+    for gi in idx:
+        fshapes.append(("+".join(names[i] for i in gi), sum(shapes[i][1] for i in gi), shapes[gi[0]][2]))
+    for r in range(replicas):
+        fr = []
+        for gi in idx:
+            parts = [reps[r][i] for i in gi]
+            if len(parts) == 1:
+                fr.append(parts[0])
+                continue
+            z = None if parts[0][2] is None else torch.cat([p[2] for p in parts])
+            fr.append((torch.cat([p[0] for p in parts]), torch.cat([p[1] for p in parts]), z))
+        freps.append(fr)
+    fxs = [xs[gi[0]] for gi in idx]
+    fys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in fshapes]
+
+    def step(r):
+        for p, (name, N, K) in enumerate(fshapes):
+            c, sc, z = freps[r][p]
+            q4.q4gemv_run(c, sc, z, fxs[p], fys[p], 1, N, K, group, stream=stream)
+
+    n = max(replicas, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for r in range(replicas):
+            step(r)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            step(i % replicas)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    byts = step_bytes(fshapes, 1, group)
+    return {"launches_per_step": len(fshapes), "shapes": [[nm, N, K] for nm, N, K in fshapes],
+            "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
 
 
 def run_decode_8b(args, torch, q4):
