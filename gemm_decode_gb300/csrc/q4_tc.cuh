@@ -1,0 +1,102 @@
+// q4_tc.cuh -- device helpers of the tcgen05 kernels (tensor-core matmul and the
+// small-M tensor-core GEMV): mbarriers with bounded waits, TMA tile loads, UMMA
+// shared-memory descriptors for K-major 128-byte-swizzled 16-bit tiles, MMA issue
+// and commit, tensor-memory fences.  Internal, not part of the public ABI.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "q4_common.cuh"
+
+namespace q4 {
+
+// cuTensorMapEncodeTiled from the driver, looked up once (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase with the given parity to complete, for at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_try(bar, parity)) return true;
+    if (limit_ns == 0) return false;   // a zero bound means one attempt (the timer is coarse)
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major, 128-byte-swizzled 16-bit tile whose
+// rows are 128 bytes and whose 8-row swizzle atoms are 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);   // start address
+    d |= static_cast<uint64_t>(1u) << 16;                // leading byte offset (unused when swizzled, K-major)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;        // stride byte offset: 8 rows * 128 B
+    d |= static_cast<uint64_t>(1u) << 46;                // descriptor version for this architecture
+    d |= static_cast<uint64_t>(2u) << 61;                // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor of kind::f16 with an f32 accumulator, both operands K-major:
+// bf16 = true for bf16 inputs, false for fp16; M rows of A and D, N rows of B.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
+    return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Byte offset of the 16-byte chunk j (k = 8j..8j+7) of row r in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int j) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
+}  // namespace tc
+}  // namespace q4

@@ -30,9 +30,12 @@
 #include <cuda_bf16.h>
 
 #include "q4_common.cuh"
+#include "q4_tc.cuh"
 #include "q4gemv_stream.cuh"
 
 namespace q4 {
+
+using namespace tc;
 
 __device__ unsigned int g_gemm_status = 0;   // 1 = a bounded wait expired
 
@@ -55,85 +58,11 @@ struct GemmArgs {
     unsigned long long timeout_ns;
 };
 
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait for the phase with the given parity to complete, for at most limit_ns.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
-    if (mbar_try(bar, parity)) return true;
-    if (limit_ns == 0) return false;   // a zero bound means one attempt (the timer is coarse)
-    const unsigned long long t0 = global_ns();
-    for (;;) {
-        if (mbar_try(bar, parity)) return true;
-        if (global_ns() - t0 > limit_ns) return false;
-    }
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor for a K-major, 128-byte-swizzled bf16 tile whose
-// rows are 128 bytes and whose 8-row swizzle atoms are 1024 bytes apart.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t addr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);   // start address
-    d |= static_cast<uint64_t>(1u) << 16;                // leading byte offset (unused when swizzled, K-major)
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;        // stride byte offset: 8 rows * 128 B
-    d |= static_cast<uint64_t>(1u) << 46;                // descriptor version for this architecture
-    d |= static_cast<uint64_t>(2u) << 61;                // 128-byte swizzle
-    return d;
-}
 // Instruction descriptor: D f32, A/B bf16, both K-major, N = BN, M = BM.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_f16(true, BM, BN);
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Byte offset of the 16-byte chunk j (k = 8j..8j+7) of row r in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int j) {
-    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+    umma_f16(d_tmem, a_desc, b_desc, kIdesc, accumulate);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -389,12 +318,31 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
 
 static unsigned long long g_timeout_ns = 1000ull * 1000 * 1000;   // 1 s per wait
 
+unsigned long long gemm_wait_timeout_ns() { return g_timeout_ns; }
+
+// Address of the tensor-core status word, for kernels in other translation units.
+unsigned int *gemm_status_word() {
+    static unsigned int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_gemm_status);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return nullptr;
+        }
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+
 void set_gemm_wait_timeout_ns(unsigned long long ns) {
     g_timeout_ns = ns;
     set_stream_wait_timeout_ns(ns);
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
         void *p = nullptr;

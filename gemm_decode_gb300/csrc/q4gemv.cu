@@ -73,6 +73,7 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
                   cudaStream_t stream) {
     if (stream_applies(M, N, K, group, codes, scales, zeros))
         return launch_q4gemv_stream(codes, scales, zeros, x, y, N, K, group, stream);
+    if (tc_gemv_applies(M, N, K, codes)) return launch_q4gemv_tc(codes, scales, zeros, x, y, M, N, K, group, stream);
     {
         XregPlan xp;
         XregArgs xa;

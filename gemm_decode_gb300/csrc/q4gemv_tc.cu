@@ -1,0 +1,447 @@
+// q4gemv_tc.cu -- the 2 <= M <= 16 int4 GEMV on the 5th-generation tensor cores.
+//
+// Computes y[m][n] = sum_k w[n][k] * x[m][k], w[n][k] = (q[n][k] - z[n][k/g]) * s[n][k/g]
+// (gerbil GPU-engine kernel reference, "3. MatMulInt4": "Computes", "Dequantization";
+// MatMulNBits layout).  With a few rows of x the work is still a stream of weights, but
+// the CUDA-core GEMV pays its multiply-adds once per row of x; here one dequantisation
+// of each weight serves every row through the tensor core.
+//
+// Roles: the weights are the MMA's A operand (M = 128 weight rows per CTA), x the B
+// operand.  x is split into two fp16 parts, x = hi + lo with hi = fp16(x) and
+// lo = fp16(x - hi), stored as 2*MP rows of B (hi rows 0..MP-1, lo rows MP..2MP-1,
+// rows past M zero), so the MMA's N is 16 or 32 and D = [W x_hi^T | W x_lo^T] sits in
+// 16 or 32 TMEM columns; the epilogue adds the two halves.  Each weight is dequantised
+// exactly in binary32 ((q - z) * s) and rounded once to fp16 (relative error at most
+// 2^-11, inside the 1e-3 tolerance); hi + lo carries x to about 2^-22.
+//
+//   warp 0      TMA producer: the 128 rows x 32 bytes of codes of each 64-wide K-block
+//               (2D tensor map over codes[N][K/2]) into a deep ring, completion counted
+//               on the slot's mbarrier;
+//   warp 1      allocates 32 TMEM columns; one lane issues 4 MMAs (K = 16 each) per
+//               K-block and commits them to the weight/x stage's "empty" barrier;
+//   warps 2..9  dequantisers: each thread turns 32 codes of one weight row (read from
+//               the code ring) into fp16 in the UMMA K-major 128-byte-swizzled layout
+//               (k permuted within each group of 8 to the decode's nibble-pair order),
+//               and converts its share of x for the same K-block into the hi/lo rows
+//               with the same permutation;
+//               scales, zero points and x are prefetched into registers 4 blocks ahead;
+//   warps 2..5  afterwards read the accumulator (one TMEM lane per weight row) and
+//               store y.
+// Every mbarrier wait is bounded by %globaltimer; on expiry the CTA raises the device
+// status word (read by q4gemv_device_status), drains what it issued and returns.
+#include <cuda_fp16.h>
+
+#include "q4_common.cuh"
+#include "q4_tc.cuh"
+
+namespace q4 {
+
+using namespace tc;
+
+unsigned int *gemm_status_word();
+unsigned long long gemm_wait_timeout_ns();
+
+namespace {
+
+constexpr int TM = 128;                    // weight rows per CTA (MMA M)
+constexpr int TK = 64;                     // K per block: one 128-byte row of fp16
+constexpr int CST = 10;                    // code-ring stages
+constexpr int WST = 3;                     // weight/x tile stages
+constexpr int PF = 4;                      // scale / zero-point prefetch distance (blocks)
+constexpr int kDeqWarps = 8;
+constexpr int kThreads = (2 + kDeqWarps) * 32;
+constexpr int kCodeStage = TM * TK / 2;    // 4 KB of codes per block
+constexpr int kWTile = TM * TK * 2;        // 16 KB of fp16 weights per block
+constexpr int kTmemCols = 32;
+
+struct TcArgs {
+    const uint16_t *scales;
+    const uint8_t *zeros;
+    const float *x;
+    float *y;
+    int64_t N;
+    int M, K, nb, zrow, gshift;
+    unsigned long long timeout_ns;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+__device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
+__device__ __forceinline__ uint32_t half2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
+// (a & mask) | bits, one LOP3
+__device__ __forceinline__ uint32_t lop3_or_and(uint32_t a, uint32_t mask, uint32_t bits) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+    return d;
+}
+// Slot j of an 8-code group in the stored tiles holds code k = perm(j): the nibble-pair
+// order (0,4), (1,5), (2,6), (3,7) of the decode.
+__device__ __forceinline__ int slot_k(int j) { return (j >> 1) + 4 * (j & 1); }
+
+}  // namespace
+
+template <int MP>
+constexpr size_t tc_smem_bytes() {
+    return 1024 + static_cast<size_t>(WST) * (kWTile + 2 * MP * TK * 2) + static_cast<size_t>(CST) * kCodeStage +
+           8 * (2 * CST + 2 * WST + 1) + 16;
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 2)
+q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g) {
+    constexpr int NX = 2 * MP;                   // MMA N: MP hi rows then MP lo rows
+    constexpr int kXTile = NX * TK * 2;          // 2 or 4 KB
+    constexpr uint32_t kIdescTc = idesc_f16(false, TM, NX);
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    unsigned char *wtiles = smem;                                  // WST x 16 KB
+    unsigned char *xtiles = wtiles + WST * kWTile;                 // WST x kXTile
+    unsigned char *ctiles = xtiles + WST * kXTile;                 // CST x 4 KB
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ctiles + CST * kCodeStage);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * CST + 2 * WST + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * TM;
+    const int kblocks = (g.K + TK - 1) / TK;
+    const unsigned long long limit = g.timeout_ns;
+
+    const uint32_t bar0 = smem_addr(bars);
+    auto cfull = [&](int s) { return bar0 + 8u * s; };
+    auto cempty = [&](int s) { return bar0 + 8u * (CST + s); };
+    auto wfull = [&](int s) { return bar0 + 8u * (2 * CST + s); };
+    auto wempty = [&](int s) { return bar0 + 8u * (2 * CST + WST + s); };
+    const uint32_t done_bar = bar0 + 8u * (2 * CST + 2 * WST);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < CST; ++s) {
+            mbar_init(cfull(s), 1);
+            mbar_init(cempty(s), kDeqWarps * 32);
+        }
+        for (int s = 0; s < WST; ++s) {
+            mbar_init(wfull(s), kDeqWarps * 32);
+            mbar_init(wempty(s), 1);
+        }
+        mbar_init(done_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    allow_next_grid();
+    const uint32_t tmem = *tmem_slot;
+
+    auto fail = [&]() {
+        *abort_flag = 1;
+        atomicOr(g.status, 1u);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (codes)
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
+                const int s = kb % CST;
+                if (kb >= CST && !mbar_wait(cempty(s), ((kb / CST) - 1) & 1, limit)) {
+                    fail();
+                    break;
+                }
+                mbar_expect_tx(cfull(s), kCodeStage);
+                tma_load_2d(smem_addr(ctiles + s * kCodeStage), &tmap_codes, cfull(s), kb * (TK / 2),
+                            static_cast<int>(n0));
+                issued = kb + 1;
+            }
+            if (*abort_flag) {
+                // drain (bounded): every issued box lands before the CTA may exit
+                for (int kb = issued - CST > 0 ? issued - CST : 0; kb < issued; ++kb)
+                    mbar_wait(cfull(kb % CST), (kb / CST) & 1, 50ull * 1000 * 1000);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
+                const int s = kb % WST;
+                if (!mbar_wait(wfull(s), (kb / WST) & 1, limit)) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_base = smem_addr(wtiles + s * kWTile);
+                const uint32_t b_base = smem_addr(xtiles + s * kXTile);
+#pragma unroll
+                for (int kk = 0; kk < TK / 16; ++kk)   // 16 fp16 = 32 bytes per step in the swizzle span
+                    umma_f16(tmem, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), kIdescTc,
+                             (kb > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(wempty(s));
+            }
+            umma_commit(done_bar);   // all issued MMAs complete (also the drain on abort)
+        }
+    } else {
+        // ------------------------------------------------------------ dequantisers
+        const int t = threadIdx.x - 64;            // 0..255
+        const int row = t >> 1;                    // weight row within the tile
+        const int half = t & 1;                    // which 32 codes of the 64-wide K-block
+        const int64_t n = n0 + row < g.N ? n0 + row : g.N - 1;
+        const uint16_t *srow = g.scales + n * g.nb;
+        const uint8_t *zrow = g.zeros ? g.zeros + n * g.zrow : nullptr;
+        // x share: VPT consecutive slots (see slot_k) of one x row per K-block
+        constexpr int VPT = MP / 4;                // 2 (MP = 8) or 4 (MP = 16)
+        constexpr int TPR = TK / VPT;              // threads per x row
+        const int xm = t / TPR;                    // x row (< MP)
+        const int xk = (t - xm * TPR) * VPT;       // first slot of the share within the block
+
+        // scale and zero-point byte of K-block kb for this thread's 32 codes, and this
+        // thread's share of x for the block
+        struct Side {
+            uint32_t sc, zb;
+            float xv[VPT];
+        };
+        auto fetch_w = [&](Side &f, int kb) {
+            const int k = kb * TK + half * 32;
+            if (kb < kblocks && k < g.K) {
+                const int grp = k >> (5 + g.gshift);
+                f.sc = ldg_u16(srow + grp);
+                f.zb = zrow ? ldg_u8(zrow + (grp >> 1)) : 0u;
+            }
+        };
+        auto fetch_x = [&](Side &f, int kb) {
+            // slots xk .. xk + VPT - 1 of the block hold x at k = 8 * (slot / 8) + slot_k(slot % 8)
+#pragma unroll
+            for (int i = 0; i < VPT; ++i) {
+                const int sl = xk + i;
+                const int k = kb * TK + (sl & ~7) + slot_k(sl & 7);
+                f.xv[i] = (kb < kblocks && xm < g.M && k < g.K) ? __ldg(g.x + static_cast<int64_t>(xm) * g.K + k) : 0.0f;
+            }
+        };
+        static_assert(PF == 4, "the prefetch ring below rotates four register sets");
+        Side f0{}, f1{}, f2{}, f3{};
+        fetch_w(f0, 0);
+        fetch_w(f1, 1);
+        fetch_w(f2, 2);
+        fetch_w(f3, 3);
+        wait_prior_grid();   // x and y may belong to the kernel before this one in the stream
+        fetch_x(f0, 0);
+        fetch_x(f1, 1);
+        fetch_x(f2, 2);
+        fetch_x(f3, 3);
+
+        for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
+            const int cs = kb % CST, ws = kb % WST;
+            const Side cur = f0;   // rotate without dynamic indexing (stays in registers)
+            f0 = f1;
+            f1 = f2;
+            f2 = f3;
+            fetch_w(f3, kb + PF);
+            fetch_x(f3, kb + PF);
+            const float *xv = cur.xv;
+            if (!mbar_wait(cfull(cs), (kb / CST) & 1, limit)) {
+                fail();
+                break;
+            }
+            uint4 cw;
+            {
+                const uint32_t ca = smem_addr(ctiles + cs * kCodeStage + row * (TK / 2) + half * 16);
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
+                             : "r"(ca));
+            }
+            if (kb >= WST && !mbar_wait(wempty(ws), ((kb / WST) - 1) & 1, limit)) {
+                fail();
+                break;
+            }
+            const int k = kb * TK + half * 32;     // first code of this thread's 32
+            uint32_t out[16];
+            if (k < g.K) {
+                const int grp = k >> (5 + g.gshift);
+                uint32_t z = 8u;
+                if (zrow) z = (grp & 1) ? (cur.zb >> 4) : (cur.zb & 0xFu);
+                // fp16 1024 + q from a nibble OR-ed into the fraction of 1024 (0x6400); the
+                // half2 subtraction of 1024 + z is exact, and one half2 multiply by s rounds the
+                // exact product (q - z) * s once -- the same value as rounding the binary32
+                // product.  Each word gives the nibble pairs (0,4), (1,5), (2,6), (3,7), stored in
+                // that order; x is stored with the same permutation of k.
+                const __half2 zz = u32_as_half2((0x6400u | z) * 0x00010001u);
+                const __half2 ss = u32_as_half2(cur.sc * 0x00010001u);
+                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const uint32_t m = lop3_or_and(words[w] >> (4 * p), 0x000F000Fu, 0x64006400u);
+                        const __half2 v = __hmul2(__hsub2(u32_as_half2(m), zz), ss);
+                        out[4 * w + p] = half2_as_u32(v);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) out[i] = 0u;   // K tail: zero weights
+            }
+            unsigned char *wt = wtiles + ws * kWTile;
+#pragma unroll
+            for (int w = 0; w < 4; ++w)
+                *reinterpret_cast<uint4 *>(wt + sw128_offset(row, half * 4 + w)) =
+                    make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+            // x: hi part in row xm, lo part in row MP + xm (VPT fp16 at slot offset xk)
+            {
+                uint32_t hi[VPT / 2], lo[VPT / 2];
+#pragma unroll
+                for (int i = 0; i < VPT / 2; ++i) {
+                    const __half h0 = __float2half_rn(xv[2 * i]), h1 = __float2half_rn(xv[2 * i + 1]);
+                    const float r0 = xv[2 * i] - __half2float(h0), r1 = xv[2 * i + 1] - __half2float(h1);
+                    const __half2 hh = __halves2half2(h0, h1);
+                    hi[i] = *reinterpret_cast<const uint32_t *>(&hh);
+                    lo[i] = pack_half2(r0, r1);
+                }
+                unsigned char *xt = xtiles + ws * kXTile;
+                const uint32_t within = static_cast<uint32_t>((xk & 7) * 2);   // byte offset inside the 16-byte chunk
+                if constexpr (VPT == 4) {
+                    *reinterpret_cast<uint2 *>(xt + sw128_offset(xm, xk >> 3) + within) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2 *>(xt + sw128_offset(MP + xm, xk >> 3) + within) = make_uint2(lo[0], lo[1]);
+                } else {
+                    *reinterpret_cast<uint32_t *>(xt + sw128_offset(xm, xk >> 3) + within) = hi[0];
+                    *reinterpret_cast<uint32_t *>(xt + sw128_offset(MP + xm, xk >> 3) + within) = lo[0];
+                }
+            }
+            fence_proxy_async();      // generic-proxy stores -> visible to the tensor core
+            mbar_arrive(wfull(ws));
+            // the code slot may be refilled only now, after the codes read from it have been
+            // consumed: releasing it right after the shared-memory load let the TMA refill
+            // overtake the load (measured: whole warps' rows wrong at random)
+            mbar_arrive(cempty(cs));
+        }
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        if (warp < 6) {
+            const int quad = warp & 3;             // TMEM lane quadrant this warp may access
+            const bool ok = mbar_wait(done_bar, 0, limit);
+            if (!ok) fail();
+            if (ok && !*abort_flag) {
+                tc_fence_after();
+                uint32_t v[32];
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+                if constexpr (NX == 32) {
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                          "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+                          "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+                          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                        : "r"(taddr));
+                } else {
+                    asm volatile(
+                        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                          "=r"(v[14]), "=r"(v[15])
+                        : "r"(taddr));
+                }
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                const int64_t nn = n0 + quad * 32 + lane;   // weight row = TMEM lane
+                if (nn < g.N) {
+#pragma unroll
+                    for (int m = 0; m < MP; ++m)
+                        if (m < g.M) g.y[static_cast<int64_t>(m) * g.N + nn] = __uint_as_float(v[m]) + __uint_as_float(v[MP + m]);
+                }
+            }
+        }
+    }
+    // ---- teardown: every issued MMA finished before TMEM is released ----
+    if (warp == 1 && lane == 0 && *abort_flag) mbar_wait(done_bar, 0, 50ull * 1000 * 1000);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+// Where the tensor-core GEMV beats the CUDA-core kernels (measured on the decode and
+// sweep shapes): its time is nearly flat in M but it has only N / 128 CTAs, so it wins
+// for many rows of x and enough weight rows.
+bool tc_gemv_applies(int M, int64_t N, int K, const void *codes) {
+    if (M < 3 || M > 16) return false;
+    if (K % 32 != 0 || !aligned(codes, 16)) return false;   // TMA: row pitch K/2 a multiple of 16 bytes
+    if (N > (int64_t(1) << 31) - TM) return false;
+    if (M >= 9) return N >= 4096;
+    if (M >= 5) return N >= 8192;
+    return N >= 65536;
+}
+
+template <int MP>
+static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t stream) {
+    auto kern = q4gemv_tc_kernel<MP>;
+    constexpr size_t smem = tc_smem_bytes<MP>();
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        configured[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((g.N + TM - 1) / TM), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    add_overlap_attr(cfg, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, g);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x, float *y,
+                     int M, int64_t N, int K, int group, cudaStream_t stream) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return Q4_ERR_CUDA;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {TK / 2, TM};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return Q4_ERR_UNSUPPORTED;
+    TcArgs g;
+    g.scales = scales;
+    g.zeros = zeros;
+    g.x = x;
+    g.y = y;
+    g.N = N;
+    g.M = M;
+    g.K = K;
+    g.nb = K / group;
+    g.zrow = (g.nb + 1) / 2;
+    g.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
+    g.timeout_ns = gemm_wait_timeout_ns();
+    g.status = gemm_status_word();
+    if (g.status == nullptr) return Q4_ERR_CUDA;
+    return M <= 8 ? launch_tc<8>(map, g, stream) : launch_tc<16>(map, g, stream);
+}
+
+}  // namespace q4

@@ -1,0 +1,151 @@
+"""GPU parity of the tensor-core GEMV against the CPU oracle.
+
+It serves 3 <= M <= 16 with enough weight rows (M >= 9 from N = 4096, M >= 5 from
+8192, M = 3..4 from 65536); the cases below pick M and N inside that region.  The
+kernel dequantises each weight exactly and rounds it once to fp16 (relative error
+<= 2^-11), splits x into fp16 hi + lo parts and accumulates in fp32 in tensor memory.  Every case is checked against the stated tolerance
+1e-3*sum|w x| + 1e-6 and against the tighter bound that follows from that
+arithmetic, (2^-11 + 2^-18)*sum|w x| + 1e-6.  Marked gpu.
+"""
+import numpy as np
+import pytest
+
+import gemm_decode_gb300 as q4
+import oracle
+import synth
+from gpu_util import assert_within_bound, dev, host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+FP16_REL = 2.0 ** -11 + 2.0 ** -18
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_cuda()
+    q4.lib()
+    return t
+
+
+def run(torch, w, x):
+    M, K = x.shape
+    guard = 64
+    buf = torch.full((M * w.N + 2 * guard,), 12345.0, dtype=torch.float32, device="cuda")
+    y = buf[guard:guard + M * w.N]
+    q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                  M, w.N, K, w.group)
+    torch.cuda.synchronize()
+    b = host(buf)
+    assert np.all(b[:guard] == 12345.0) and np.all(b[guard + M * w.N:] == 12345.0), "guard words written"
+    return b[guard:guard + M * w.N].reshape(M, w.N)
+
+
+def check(torch, w, x, what, rows=None):
+    y = run(torch, w, x)
+    if rows is None:
+        y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, w.group)
+        yy = y
+    else:
+        y_ref, bound = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, w.group, rows)
+        yy = y[:, rows]
+    assert_within_bound(yy, y_ref, bound, what)
+    err = np.abs(yy.astype(np.float64) - y_ref.astype(np.float64))
+    lim = FP16_REL * bound + 1e-6
+    assert np.all(err <= lim), f"{what}: outside the fp16-weight bound, worst {float(np.max(err / lim)):.3f}"
+    return y
+
+
+@pytest.mark.parametrize("N,K,g", [(8192, 896, 32), (8196, 2048, 64), (8323, 4096, 128), (8192, 4128, 32)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_shapes_against_oracle(torch, N, K, g, symmetric):
+    # N = 8196 / 8323: a partial last 128-row tile; K = 4128: a half-empty last K-block;
+    # M = 5..8 use 8 rows of x per half (N = 16 MMA), M = 9..16 use 16 (N = 32)
+    w = synth.q4_weights(N + K + g, N, K, g, symmetric=symmetric, tag="tc")
+    for M in (5, 8, 9, 16):
+        x = synth.activations_f32(M * 7 + K, M, K)
+        check(torch, w, x, f"M={M} N={N} K={K} g={g} sym={symmetric}")
+
+
+def test_few_rows_of_x_on_a_tall_matrix(torch):
+    # M = 3 and 4 take the tensor cores only for N >= 65536
+    N, K = 65600, 896
+    w = synth.q4_weights(7, N, K, 32, tag="tc-tall")
+    rng = np.random.default_rng(4)
+    rows = sorted(set(rng.choice(N, size=64, replace=False).tolist()) | {0, 65535, 65536, N - 1})
+    for M in (3, 4):
+        x = synth.activations_f32(50 + M, M, K)
+        check(torch, w, x, f"M={M} N={N}", rows=rows)
+
+
+@pytest.mark.parametrize("outlier", [10.0, 300.0])
+def test_heavy_tailed_activations(torch, outlier):
+    N, K = 4096, 2048
+    w = synth.q4_weights(5, N, K, 32, tag="tc-tail")
+    x = synth.activations_f32(6, 12, K)
+    r = np.random.default_rng(3)
+    cols = r.choice(K, size=16, replace=False)
+    x[:, cols] *= outlier
+    check(torch, w, x, f"outlier x{outlier}")
+
+
+def test_rows_of_x_are_independent(torch):
+    # row m of an M-row call equals the call on x[m] alone (M = 1 takes another kernel)
+    N, K = 8192, 1024
+    w = synth.q4_weights(8, N, K, 64, tag="tc-rows")
+    x = synth.activations_f32(9, 5, K)
+    y5 = run(torch, w, x)
+    for m in range(5):
+        y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x[m:m + 1], 64)
+        assert_within_bound(y5[m:m + 1], y_ref, bound, f"row {m}")
+
+
+def test_deterministic(torch):
+    w = synth.q4_weights(11, 8192, 896, 32, tag="tc-det")
+    x = synth.activations_f32(12, 16, 896)
+    a = run(torch, w, x)
+    b = run(torch, w, x)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_codes_equal_to_zero_point_give_exact_zero(torch):
+    N, K, g = 4096, 512, 32
+    w = synth.q4_weights(13, N, K, g, tag="tc-zero")
+    nb = K // g
+    z = np.zeros((N, nb), np.uint8)
+    for n in range(N):
+        for b in range(nb):
+            z[n, b] = (w.zeros[n, b // 2] >> (4 * (b % 2))) & 0xF
+    q = np.repeat(z, g, axis=1)
+    codes = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    w0 = synth.Q4Weights(codes, w.scales, w.zeros, N, K, g)
+    x = synth.activations_f32(14, 10, K)
+    y = run(torch, w0, x)
+    assert np.all(y == 0.0)
+
+
+def test_full_size_lm_head_sampled(torch):
+    name, N, K = synth.DECODE_8B["shapes"][3]
+    w = synth.q4_weights(31, N, K, 128, scale_range=synth.SCALE_8B, tag=name)
+    rng = np.random.default_rng(2)
+    rows = sorted(set(rng.choice(N, size=64, replace=False).tolist()) | {0, N - 1})
+    for M in (3, 4, 8, 16):
+        x = synth.activations_f32(40 + M, M, K)
+        check(torch, w, x, f"8B LM head M={M}", rows=rows)
+
+
+def test_bounded_wait_reports_timeout_without_fault(torch):
+    N, K = 151936, 896
+    w = synth.q4_weights(21, N, K, 32, tag="tc-timeout")
+    x = synth.activations_f32(22, 4, K)
+    y = torch.zeros((4, N), dtype=torch.float32, device="cuda")
+    try:
+        q4.q4gemm_set_wait_timeout_ns(0)
+        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                      4, N, K, 32)
+        st = q4.q4gemv_device_status()
+    finally:
+        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    assert st == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK   # the flag was cleared
+    rows = [0, 1, 4095, 77777, N - 1]
+    check(torch, w, x, "after timeout", rows=rows)
