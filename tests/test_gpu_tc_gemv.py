@@ -3,9 +3,10 @@
 It serves 3 <= M <= 16 with enough weight rows (M >= 9 from N = 4096, M >= 5 from
 8192, M = 3..4 from 65536); the cases below pick M and N inside that region.  The
 kernel dequantises each weight exactly and rounds it once to fp16 (relative error
-<= 2^-11), splits x into fp16 hi + lo parts and accumulates in fp32 in tensor memory.  Every case is checked against the stated tolerance
-1e-3*sum|w x| + 1e-6 and against the tighter bound that follows from that
-arithmetic, (2^-11 + 2^-18)*sum|w x| + 1e-6.  Marked gpu.
+<= 2^-11), splits x into fp16 hi + lo parts and accumulates in fp32 in tensor memory.
+Every case is checked against the stated tolerance 1e-3*sum|w x| + 1e-6 and against
+the tighter bound that follows from that arithmetic, (2^-11 + 2^-18)*sum|w x| + 1e-6.
+Marked gpu.
 """
 import numpy as np
 import pytest
