@@ -719,7 +719,7 @@ def parse_args(argv=None):
     p.add_argument("--ref-seconds", type=float, default=90.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--controls", type=int, default=1)
-    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "f32_lm_head",
+    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "tc_m16", "f32_lm_head",
                                          "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
@@ -742,6 +742,7 @@ PROFILE_CASES = {
     "lm_head": (151936, 896, 32, 1),
     "lm_head_8b": (128256, 4096, 128, 1),
     "down_8b": (4096, 14336, 128, 1),
+    "tc_m16": (32768, 4096, 128, 16),
 }
 
 

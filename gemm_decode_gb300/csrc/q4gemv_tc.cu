@@ -216,13 +216,22 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                 f.zb = zrow ? ldg_u8(zrow + (grp >> 1)) : 0u;
             }
         };
-        auto fetch_x = [&](Side &f, int kb) {
-            // slots xk .. xk + VPT - 1 of the block hold x at k = 8 * (slot / 8) + slot_k(slot % 8)
+        // slots xk .. xk + VPT - 1 of a block hold x at k = 8 * (slot / 8) + slot_k(slot % 8):
+        // offsets fixed per thread; rows of x past M read as zero
+        int xoff[VPT];
 #pragma unroll
-            for (int i = 0; i < VPT; ++i) {
-                const int sl = xk + i;
-                const int k = kb * TK + (sl & ~7) + slot_k(sl & 7);
-                f.xv[i] = (kb < kblocks && xm < g.M && k < g.K) ? __ldg(g.x + static_cast<int64_t>(xm) * g.K + k) : 0.0f;
+        for (int i = 0; i < VPT; ++i) xoff[i] = ((xk + i) & ~7) + slot_k((xk + i) & 7);
+        const float *xrow = g.x + static_cast<int64_t>(xm < g.M ? xm : 0) * g.K;
+        const bool xlive = xm < g.M;
+        auto fetch_x = [&](Side &f, int kb) {
+            const int k0 = kb * TK;
+            if (xlive && k0 + TK <= g.K) {          // a whole block inside K
+#pragma unroll
+                for (int i = 0; i < VPT; ++i) f.xv[i] = __ldg(xrow + k0 + xoff[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < VPT; ++i)
+                    f.xv[i] = (xlive && kb < kblocks && k0 + xoff[i] < g.K) ? __ldg(xrow + k0 + xoff[i]) : 0.0f;
             }
         };
         static_assert(PF == 4, "the prefetch ring below rotates four register sets");
