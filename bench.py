@@ -341,22 +341,11 @@ def run_gpu(args, rank, world, local_rank):
     # per-projection microseconds per call: for each projection, one graph of back-to-back
     # launches over the rotating replicas, timed from outside (no event nodes between
     # launches; event nodes cost a bubble of about a microsecond or more each)
-    per_proj_us = []
+    per_proj = []
     n_pp = max(replicas, min(args.steps, 200))
     for p, (name, N, K) in enumerate(shapes):
-        gp = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gp, stream=stream):
-            for i in range(n_pp):
-                c_, s_, z_ = reps[i % replicas][p]
-                q4.q4gemv_run(c_, s_, z_, xs[p], ys[p], 1, N, K, group, stream=stream)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            gp.replay()
-            e0.record(stream)
-            gp.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        per_proj_us.append(e0.elapsed_time(e1) * 1e3 / n_pp)
+        per_proj.append(_time_back_to_back(torch, q4, stream, [r[p] for r in reps], xs[p], ys[p], 1, N, K, group,
+                                           n_pp))
     bytes_per_step = step_bytes(shapes, 1, group)
     total_bytes = bytes_per_step * args.steps * world
     value = total_bytes / (ms_total_max * 1e-3) / 1e9
@@ -377,15 +366,18 @@ def run_gpu(args, rank, world, local_rank):
     e2e = run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dist)
 
     detail = {"projections": [
-        {"name": name, "N": N, "K": K, "us_per_call": round(us, 3),
-         "gbs": round(algorithmic_bytes(1, N, K, group) / (us * 1e-6) / 1e9, 1)}
-        for (name, N, K), us in zip(shapes, per_proj_us)],
+        {"name": name, "N": N, "K": K, "us_per_call": round(st["us"], 3),
+         "gbs": round(algorithmic_bytes(1, N, K, group) / (st["us"] * 1e-6) / 1e9, 1),
+         "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+         "t2n_over_tn": round(st["t2n_over_tn"], 3)}
+        for (name, N, K), st in zip(shapes, per_proj)],
         "weight_replicas": replicas, "replica_bytes": per_step_weight_bytes,
         "graph_steps": chunk, "event_mode": ev.mode,
         "lm_head_us_in_timed_region": round(lm_us, 3),
         "lm_head_event_samples": f"{len(sampled)} per {chunk}-step graph (every {stride}th step)",
         "us_per_call_note": "per projection: a graph of back-to-back launches over the rotating replicas, "
-                            "timed from outside; the LM head's in-step time carries the event-node bubble"}
+                            "5 timed replays (median; p10, p90, min) and t(2n)/t(n) from two replays; "
+                            "the LM head's in-step time carries the event-node bubble"}
     if args.controls and rank == 0:
         detail["controls"] = run_controls(args, torch, q4)
         detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
@@ -794,9 +786,11 @@ def _device_q4(torch, gen, N, K, g, symmetric, scale):
     return c, sc, z
 
 
-def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n):
-    """Microseconds per q4gemv_run call: a CUDA graph of n launches over the replicas,
-    replayed once untimed, then twice between events on the launching stream."""
+def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n, samples=5):
+    """Microseconds per q4gemv_run call from a CUDA graph of n back-to-back launches
+    over the replicas: one untimed replay, then `samples` replays each between events on
+    the launching stream (median, p10, p90, min), and one event pair around two replays
+    (t(2n) / t(n), which is 2 when the per-call time has no fixed overhead in it)."""
     nrep = len(reps)
     with torch.cuda.stream(stream):
         for r in reps[:2]:
@@ -806,15 +800,24 @@ def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n):
     with torch.cuda.graph(gr, stream=stream):
         for i in range(n):
             q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(samples + 1)]
     with torch.cuda.stream(stream):
         gr.replay()
-        e0.record(stream)
+        for i in range(samples):
+            ev[i][0].record(stream)
+            gr.replay()
+            ev[i][1].record(stream)
+        ev[samples][0].record(stream)
         gr.replay()
         gr.replay()
-        e1.record(stream)
+        ev[samples][1].record(stream)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) * 1e3 / (2 * n)
+    t = sorted(a.elapsed_time(b) * 1e3 / n for a, b in ev[:samples])
+    t2 = ev[samples][0].elapsed_time(ev[samples][1]) * 1e3 / n
+    med = statistics.median(t)
+    q = lambda f: t[min(len(t) - 1, max(0, int(round(f * (len(t) - 1)))))]
+    return {"us": med, "p10": q(0.1), "p90": q(0.9), "min": t[0], "samples": samples, "n": n,
+            "t2n_over_tn": t2 / med}
 
 
 def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
@@ -883,9 +886,11 @@ def run_decode_8b(args, torch, q4):
             x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
             y = torch.empty((M, N), dtype=torch.float32, device="cuda")
             n = int(max(nrep, min(200, 20000 / max(2.0, wbytes / 5e3))))
-            us = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
+            st = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
+            us = st["us"]
             out.append({"name": name, "M": M, "N": N, "K": K, "us_per_call": round(us, 3),
-                        "gbs": round(algorithmic_bytes(M, N, K, g) / us / 1e3, 1)})
+                        "gbs": round(algorithmic_bytes(M, N, K, g) / us / 1e3, 1),
+                        "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)]})
         del reps
         torch.cuda.empty_cache()
     return out
@@ -919,10 +924,14 @@ def run_sweep(args):
                         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
                         est_us = max(2.0, wbytes / 5e3)
                         n = int(max(nrep, min(400, 20000 / est_us)))
-                        us = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
+                        st = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
+                        us = st["us"]
                         byts = algorithmic_bytes(M, N, K, g, symmetric=sym)
                         cells.append({"M": M, "N": N, "K": K, "group": g, "symmetric": sym,
                                       "us_per_call": round(us, 3), "gbs": round(byts / us / 1e3, 1),
+                                      "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3),
+                                                         round(st["min"], 3)],
+                                      "t2n_over_tn": round(st["t2n_over_tn"], 3),
                                       "packed_weight_bytes": wbytes,
                                       "cold": nrep * wbytes >= 2 * L2_BYTES})
                     del reps
