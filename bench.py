@@ -717,6 +717,8 @@ def parse_args(argv=None):
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--sweep", action="store_true",
                    help="time every cell of the shape sweep instead of the decode step")
+    p.add_argument("--sweep-out", default=None,
+                   help="JSON-lines checkpoint for --sweep: cells already in the file are not re-timed")
     p.add_argument("--overlap", type=int, default=1,
                    help="1: q4gemv_set_overlapped_launch(1) (programmatic dependent launch); 0: serialised")
     p.add_argument("--event-stride", type=int, default=25,
@@ -896,6 +898,30 @@ def run_decode_8b(args, torch, q4):
     return out
 
 
+def sweep_key(cell):
+    return (cell["M"], cell["N"], cell["K"], cell["group"], cell["symmetric"])
+
+
+def load_sweep_checkpoint(path):
+    """Cells of an earlier --sweep run (one JSON object per line), keyed by
+    (M, N, K, group, symmetric); a missing file or path None gives none.  A line cut
+    short by an interrupted run is ignored."""
+    done = {}
+    if not path or not os.path.exists(path):
+        return done
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if not line:
+                continue
+            try:
+                c = json.loads(line)
+            except json.JSONDecodeError:
+                continue
+            done[sweep_key(c)] = c
+    return done
+
+
 def run_sweep(args):
     """Every cell of the shape sweep (M, K, N, group, symmetric): microseconds per
     q4gemv_run call and achieved GB/s, from a CUDA graph of back-to-back launches over
@@ -908,6 +934,13 @@ def run_sweep(args):
     gen = torch.Generator(device="cuda")
     gen.manual_seed(1234)
     stream = torch.cuda.Stream()
+    peak, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    device = {"name": props.name, "sms": props.multi_processor_count,
+              "l2_bytes": getattr(props, "L2_cache_size", None)}
+    # checkpoint: cells already in --sweep-out (JSON lines) are kept and not re-timed
+    done = load_sweep_checkpoint(args.sweep_out)
+    out = open(args.sweep_out, "a") if args.sweep_out else None
     cells = []
     sw = synth.SWEEP
     for K in sw["Ks"]:
@@ -917,9 +950,13 @@ def run_sweep(args):
                 zrow = (nb + 1) // 2
                 for sym in sw["symmetric"]:
                     wbytes = N * K // 2 + N * nb * 2 + (0 if sym else N * zrow)
+                    todo = [M for M in sw["Ms"] if (M, N, K, g, sym) not in done]
+                    cells += [done[(M, N, K, g, sym)] for M in sw["Ms"] if (M, N, K, g, sym) in done]
+                    if not todo:
+                        continue
                     nrep = int(min(256, max(2, -(-6 * L2_BYTES // wbytes))))
                     reps = [_device_q4(torch, gen, N, K, g, sym, sw["scale"]) for _ in range(nrep)]
-                    for M in sw["Ms"]:
+                    for M in todo:
                         x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
                         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
                         est_us = max(2.0, wbytes / 5e3)
@@ -927,18 +964,27 @@ def run_sweep(args):
                         st = _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n)
                         us = st["us"]
                         byts = algorithmic_bytes(M, N, K, g, symmetric=sym)
-                        cells.append({"M": M, "N": N, "K": K, "group": g, "symmetric": sym,
-                                      "us_per_call": round(us, 3), "gbs": round(byts / us / 1e3, 1),
-                                      "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3),
-                                                         round(st["min"], 3)],
-                                      "t2n_over_tn": round(st["t2n_over_tn"], 3),
-                                      "packed_weight_bytes": wbytes,
-                                      "cold": nrep * wbytes >= 2 * L2_BYTES})
+                        gbs = byts / us / 1e3
+                        cell = {"M": M, "N": N, "K": K, "group": g, "symmetric": sym,
+                                "us_per_call": round(us, 3), "gbs": round(gbs, 1),
+                                "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+                                "t2n_over_tn": round(st["t2n_over_tn"], 3),
+                                # a cell counts when twice the launches take at least 1.2x the time
+                                "status": "ok" if st["t2n_over_tn"] >= 1.2 else "noise",
+                                "pct_of_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                                "pct_of_measured_copy": round(100 * gbs / peak, 1),
+                                "packed_weight_bytes": wbytes,
+                                "cold": nrep * wbytes >= 2 * L2_BYTES}
+                        cells.append(cell)
+                        if out is not None:
+                            out.write(json.dumps(cell) + "\n")
+                            out.flush()
                     del reps
                     torch.cuda.empty_cache()
+    if out is not None:
+        out.close()
     big = [c for c in cells if c["M"] == 1 and c["packed_weight_bytes"] >= 64e6]
-    peak, peak_src = load_peaks()
-    summary = {"cells_m1_ge_64MB": len(big),
+    summary = {"device": device, "noise_cells": sum(1 for c in cells if c.get("status") == "noise"),"cells_m1_ge_64MB": len(big),
                "min_gbs_m1_ge_64MB": min(c["gbs"] for c in big) if big else None,
                "median_gbs_m1_ge_64MB": statistics.median(c["gbs"] for c in big) if big else None,
                "peak": peak, "peak_source": peak_src}

@@ -193,6 +193,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
     int s = 0, ph = 0;       // ring slot of block i and its wrap parity
     int rb = 0, rph = 0;     // partial-sum buffer of block i and its wrap parity
     int pb = 0, pph = 0;     // the same for block i - 1 (set at the end of each iteration)
+    int rw = 0;              // the warp that reduces block i - 1: (i - 1) mod NWC
     for (int i = 0; i < nbk; ++i) {
         if (aborted()) break;
         if (!mbar_wait(full(s), ph, limit)) {
@@ -232,7 +233,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             mbar_arrive(redfull(rb));   // this warp's partials of block i are written
         }
         // deferred reduction of block i-1 by one (rotating) consumer warp
-        if (i >= 1 && warp == (i - 1) % G.NWC) {
+        if (i >= 1 && warp == rw) {
             if (!mbar_wait(redfull(pb), pph, limit)) {
                 fail();
                 break;
@@ -241,6 +242,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(reddone(pb));
         }
+        if (i >= 1 && ++rw == G.NWC) rw = 0;
         pb = rb;
         pph = rph;
         if (++rb == NRED) {

@@ -1,5 +1,6 @@
 """Host-side logic of bench.py (no GPU): byte accounting, clock-sample parsing,
 and the max-over-ranks / sum-over-ranks reduction on two gloo ranks."""
+import json
 import os
 import socket
 import subprocess
@@ -80,3 +81,18 @@ def test_reference_arm_runs_the_oracle(tmp_path):
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_sweep_checkpoint_round_trip(tmp_path):
+    # the --sweep-out file is JSON lines; a rerun skips the cells it finds, and a last
+    # line cut short by an interrupted run is ignored
+    import bench
+    path = tmp_path / "sweep.jsonl"
+    cells = [{"M": 1, "N": 4096, "K": 896, "group": 32, "symmetric": False, "us_per_call": 2.0},
+             {"M": 16, "N": 4096, "K": 896, "group": 32, "symmetric": True, "us_per_call": 9.0}]
+    path.write_text("".join(json.dumps(c) + "\n" for c in cells) + '{"M": 1, "N": 51')
+    done = bench.load_sweep_checkpoint(str(path))
+    assert set(done) == {(1, 4096, 896, 32, False), (16, 4096, 896, 32, True)}
+    assert done[(16, 4096, 896, 32, True)]["us_per_call"] == 9.0
+    assert bench.load_sweep_checkpoint(str(tmp_path / "missing.jsonl")) == {}
+    assert bench.load_sweep_checkpoint(None) == {}
