@@ -47,7 +47,7 @@ constexpr int TM = 128;                    // weight rows per CTA (MMA M)
 constexpr int TK = 64;                     // K per block: one 128-byte row of fp16
 constexpr int CST = 10;                    // code-ring stages
 constexpr int WST = 3;                     // weight/x tile stages
-constexpr int PF = 4;                      // scale / zero-point prefetch distance (blocks)
+constexpr int PF = 4;                      // scale / zero-point / x prefetch distance (blocks)
 constexpr int kDeqWarps = 8;
 constexpr int kThreads = (2 + kDeqWarps) * 32;
 constexpr int kCodeStage = TM * TK / 2;    // 4 KB of codes per block
@@ -65,17 +65,31 @@ struct TcArgs {
     unsigned int *status;
 };
 
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t *>(&v);
-}
-__device__ __forceinline__ __half2 u32_as_half2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
-__device__ __forceinline__ uint32_t half2_as_u32(__half2 h) { return *reinterpret_cast<const uint32_t *>(&h); }
 // (a & mask) | bits, one LOP3
 __device__ __forceinline__ uint32_t lop3_or_and(uint32_t a, uint32_t mask, uint32_t bits) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
     return d;
+}
+// (m - zz) * ss on f16x2 pairs held in 32-bit registers: the subtraction is exact for the
+// decoded nibbles, the multiply rounds once.
+__device__ __forceinline__ uint32_t f16x2_sub_mul(uint32_t m, uint32_t zz, uint32_t ss) {
+    uint32_t d;
+    asm("{\n\t.reg .b32 t;\n\tsub.rn.f16x2 t, %1, %2;\n\tmul.rn.f16x2 %0, t, %3;\n\t}"
+        : "=r"(d)
+        : "r"(m), "r"(zz), "r"(ss));
+    return d;
+}
+// Two floats to fp16 hi + lo pairs: hi = fp16(a), fp16(b); lo = fp16(a - hi_a), fp16(b - hi_b).
+__device__ __forceinline__ void f16x2_split(float a, float b, uint32_t &hi, uint32_t &lo) {
+    asm("{\n\t.reg .b16 ha, hb;\n\t.reg .f32 fa, fb;\n\t"
+        "cvt.rn.f16x2.f32 %0, %3, %2;\n\t"
+        "mov.b32 {ha, hb}, %0;\n\t"
+        "cvt.f32.f16 fa, ha;\n\tcvt.f32.f16 fb, hb;\n\t"
+        "sub.rn.f32 fa, %2, fa;\n\tsub.rn.f32 fb, %3, fb;\n\t"
+        "cvt.rn.f16x2.f32 %1, fb, fa;\n\t}"
+        : "=r"(hi), "=r"(lo)
+        : "f"(a), "f"(b));
 }
 // Slot j of an 8-code group in the stored tiles holds code k = perm(j): the nibble-pair
 // order (0,4), (1,5), (2,6), (3,7) of the decode.
@@ -234,7 +248,7 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                     f.xv[i] = (xlive && kb < kblocks && k0 + xoff[i] < g.K) ? __ldg(xrow + k0 + xoff[i]) : 0.0f;
             }
         };
-        static_assert(PF == 4, "the prefetch ring below rotates four register sets");
+        static_assert(PF == 4, "the K loop below is unrolled over four register sets");
         Side f0{}, f1{}, f2{}, f3{};
         fetch_w(f0, 0);
         fetch_w(f1, 1);
@@ -246,51 +260,48 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         fetch_x(f2, 2);
         fetch_x(f3, 3);
 
-        for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
+        // loop-invariant shared-memory offsets of this thread
+        const uint32_t c_off = static_cast<uint32_t>(row * (TK / 2) + half * 16);
+        uint32_t w_off[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) w_off[w] = sw128_offset(row, half * 4 + w);
+        const uint32_t within = static_cast<uint32_t>((xk & 7) * 2);   // byte offset inside the 16-byte chunk
+        const uint32_t xhi_off = sw128_offset(xm, xk >> 3) + within;
+        const uint32_t xlo_off = sw128_offset(MP + xm, xk >> 3) + within;
+
+        // One K-block with the register set f that holds its side data, which is then
+        // refilled for block kb + PF.  Returns false when a bounded wait expired.
+        auto step = [&](Side &f, int kb) -> bool {
             const int cs = kb % CST, ws = kb % WST;
-            const Side cur = f0;   // rotate without dynamic indexing (stays in registers)
-            f0 = f1;
-            f1 = f2;
-            f2 = f3;
-            fetch_w(f3, kb + PF);
-            fetch_x(f3, kb + PF);
-            const float *xv = cur.xv;
-            if (!mbar_wait(cfull(cs), (kb / CST) & 1, limit)) {
-                fail();
-                break;
-            }
+            if (!mbar_wait(cfull(cs), (kb / CST) & 1, limit)) return false;
             uint4 cw;
             {
-                const uint32_t ca = smem_addr(ctiles + cs * kCodeStage + row * (TK / 2) + half * 16);
+                const uint32_t ca = smem_addr(ctiles + cs * kCodeStage) + c_off;
                 asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
                              : "r"(ca));
             }
-            if (kb >= WST && !mbar_wait(wempty(ws), ((kb / WST) - 1) & 1, limit)) {
-                fail();
-                break;
-            }
+            if (kb >= WST && !mbar_wait(wempty(ws), ((kb / WST) - 1) & 1, limit)) return false;
             const int k = kb * TK + half * 32;     // first code of this thread's 32
             uint32_t out[16];
             if (k < g.K) {
                 const int grp = k >> (5 + g.gshift);
                 uint32_t z = 8u;
-                if (zrow) z = (grp & 1) ? (cur.zb >> 4) : (cur.zb & 0xFu);
+                if (zrow) z = (grp & 1) ? (f.zb >> 4) : (f.zb & 0xFu);
                 // fp16 1024 + q from a nibble OR-ed into the fraction of 1024 (0x6400); the
                 // half2 subtraction of 1024 + z is exact, and one half2 multiply by s rounds the
                 // exact product (q - z) * s once -- the same value as rounding the binary32
                 // product.  Each word gives the nibble pairs (0,4), (1,5), (2,6), (3,7), stored in
                 // that order; x is stored with the same permutation of k.
-                const __half2 zz = u32_as_half2((0x6400u | z) * 0x00010001u);
-                const __half2 ss = u32_as_half2(cur.sc * 0x00010001u);
+                const uint32_t zz = (0x6400u | z) * 0x00010001u;
+                const uint32_t ss = f.sc * 0x00010001u;
                 const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
                         const uint32_t m = lop3_or_and(words[w] >> (4 * p), 0x000F000Fu, 0x64006400u);
-                        const __half2 v = __hmul2(__hsub2(u32_as_half2(m), zz), ss);
-                        out[4 * w + p] = half2_as_u32(v);
+                        out[4 * w + p] = f16x2_sub_mul(m, zz, ss);
                     }
                 }
             } else {
@@ -300,27 +311,20 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             unsigned char *wt = wtiles + ws * kWTile;
 #pragma unroll
             for (int w = 0; w < 4; ++w)
-                *reinterpret_cast<uint4 *>(wt + sw128_offset(row, half * 4 + w)) =
+                *reinterpret_cast<uint4 *>(wt + w_off[w]) =
                     make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
             // x: hi part in row xm, lo part in row MP + xm (VPT fp16 at slot offset xk)
             {
                 uint32_t hi[VPT / 2], lo[VPT / 2];
 #pragma unroll
-                for (int i = 0; i < VPT / 2; ++i) {
-                    const __half h0 = __float2half_rn(xv[2 * i]), h1 = __float2half_rn(xv[2 * i + 1]);
-                    const float r0 = xv[2 * i] - __half2float(h0), r1 = xv[2 * i + 1] - __half2float(h1);
-                    const __half2 hh = __halves2half2(h0, h1);
-                    hi[i] = *reinterpret_cast<const uint32_t *>(&hh);
-                    lo[i] = pack_half2(r0, r1);
-                }
+                for (int i = 0; i < VPT / 2; ++i) f16x2_split(f.xv[2 * i], f.xv[2 * i + 1], hi[i], lo[i]);
                 unsigned char *xt = xtiles + ws * kXTile;
-                const uint32_t within = static_cast<uint32_t>((xk & 7) * 2);   // byte offset inside the 16-byte chunk
                 if constexpr (VPT == 4) {
-                    *reinterpret_cast<uint2 *>(xt + sw128_offset(xm, xk >> 3) + within) = make_uint2(hi[0], hi[1]);
-                    *reinterpret_cast<uint2 *>(xt + sw128_offset(MP + xm, xk >> 3) + within) = make_uint2(lo[0], lo[1]);
+                    *reinterpret_cast<uint2 *>(xt + xhi_off) = make_uint2(hi[0], hi[1]);
+                    *reinterpret_cast<uint2 *>(xt + xlo_off) = make_uint2(lo[0], lo[1]);
                 } else {
-                    *reinterpret_cast<uint32_t *>(xt + sw128_offset(xm, xk >> 3) + within) = hi[0];
-                    *reinterpret_cast<uint32_t *>(xt + sw128_offset(MP + xm, xk >> 3) + within) = lo[0];
+                    *reinterpret_cast<uint32_t *>(xt + xhi_off) = hi[0];
+                    *reinterpret_cast<uint32_t *>(xt + xlo_off) = lo[0];
                 }
             }
             fence_proxy_async();      // generic-proxy stores -> visible to the tensor core
@@ -329,6 +333,22 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             // consumed: releasing it right after the shared-memory load let the TMA refill
             // overtake the load (measured: whole warps' rows wrong at random)
             mbar_arrive(cempty(cs));
+            // this register set now serves block kb + PF (issued late: the old values are
+            // consumed, so the loads land in the same registers without moves)
+            fetch_w(f, kb + PF);
+            fetch_x(f, kb + PF);
+            return true;
+        };
+
+        for (int kb0 = 0; kb0 < kblocks && !*abort_flag; kb0 += PF) {
+            bool ok = step(f0, kb0);
+            if (ok && kb0 + 1 < kblocks) ok = step(f1, kb0 + 1);
+            if (ok && kb0 + 2 < kblocks) ok = step(f2, kb0 + 2);
+            if (ok && kb0 + 3 < kblocks) ok = step(f3, kb0 + 3);
+            if (!ok) {
+                fail();
+                break;
+            }
         }
         // ------------------------------------------------------------ epilogue (warps 2..5)
         if (warp < 6) {
