@@ -20,6 +20,7 @@ __all__ = [
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
     "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
+    "q4gemv_bounds_violations",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
     "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT",
 ]
@@ -82,10 +83,11 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_device_status.argtypes = [_vp]
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
+            L.q4gemv_bounds_violations.argtypes = [_vp]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
-                      "q4gemv_set_overlapped_launch"):
+                      "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -204,6 +206,12 @@ def q4gemv_device_status(stream=None) -> int:
 
 def q4gemm_set_wait_timeout_ns(ns: int) -> int:
     return lib().q4gemm_set_wait_timeout_ns(int(ns))
+
+
+def q4gemv_bounds_violations(stream=None) -> int:
+    """Out-of-range accesses counted since the last call (bounds-checking builds), -1
+    in a library built without the checks."""
+    return lib().q4gemv_bounds_violations(_stream(stream) if stream is not None else None)
 
 
 def q4gemv_set_overlapped_launch(enable: bool) -> int:

@@ -38,21 +38,32 @@ def _inputs():
                                                                  os.path.abspath(__file__)]
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+# Library variants: the product, and a bounds-checking build for tests (every checked
+# shared- and global-memory index counted and skipped when out of range).
+VARIANTS = {
+    "": (LIB_PATH, BUILD_DIR, ()),
+    "check": (os.path.join(HERE, "libq4gemv_check.so"), os.path.join(BUILD_DIR, "check"), ("-DQ4_BOUNDS_CHECK",)),
+}
+
+
+def stale(variant: str = "") -> bool:
+    lib = VARIANTS[variant][0]
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), variant: str = "") -> str:
+    lib_path, build_dir, vflags = VARIANTS[variant]
+    if not force and not stale(variant):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
+    extra_flags = (*vflags, *extra_flags)
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,16 +74,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else ()))
+                extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else (),
+                variant="check" if "--check" in sys.argv else ""))

@@ -66,6 +66,27 @@ int check_q4_args(const void *codes, const void *scales, int64_t N, int64_t K, i
     return Q4_OK;
 }
 
+#ifdef Q4_BOUNDS_CHECK
+__device__ unsigned int g_bounds_violations = 0;
+
+unsigned int *bounds_counter() {
+    static unsigned int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bounds_violations) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        addr[dev] = static_cast<unsigned int *>(p);
+    }
+    return addr[dev];
+}
+#else
+unsigned int *bounds_counter() { return nullptr; }
+#endif
+
 }  // namespace q4
 
 using namespace q4;
@@ -167,6 +188,26 @@ int q4_dequant_bf16_run(const void *codes, const void *scales_f16, const void *z
 }
 
 int q4gemv_device_status(void *stream) { return read_device_status(static_cast<cudaStream_t>(stream)); }
+
+#ifdef Q4_BOUNDS_CHECK
+int q4gemv_bounds_violations(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    unsigned int v = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, q4::g_bounds_violations, sizeof v);
+    if (e == cudaSuccess && v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(q4::g_bounds_violations, &zero, sizeof zero);
+    }
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return -Q4_ERR_CUDA;
+    }
+    return static_cast<int>(v);
+}
+#else
+int q4gemv_bounds_violations(void *) { return -1; }
+#endif
+
 
 int q4gemm_set_wait_timeout_ns(uint64_t ns) {
     set_gemm_wait_timeout_ns(ns);

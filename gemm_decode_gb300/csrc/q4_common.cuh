@@ -73,7 +73,22 @@ int launch_dequant(const uint8_t *codes, const uint16_t *scales, const uint8_t *
 int launch_read_probe(const float4 *buf, int64_t n16, float *partial, int blocks,
                       cudaStream_t stream);
 
+// Device counter of out-of-range accesses in bounds-checking builds (nullptr when the
+// library is built without -DQ4_BOUNDS_CHECK).  Kernels receive it in their arguments.
+unsigned int *bounds_counter();
+
 // ---------------------------------------------------------------- device side
+
+// Bounds-checking builds: q4_in_bounds(cond, counter) counts a false condition and
+// returns it, so the caller can skip the access; other builds compile it to true.
+#ifdef Q4_BOUNDS_CHECK
+__device__ __forceinline__ bool q4_in_bounds(bool ok, unsigned int *counter) {
+    if (!ok && counter != nullptr) atomicAdd(counter, 1u);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool q4_in_bounds(bool, unsigned int *) { return true; }
+#endif
 
 // Programmatic dependent launch.  wait_prior_grid: block until the grid this one
 // depends on has completed and its memory writes are visible (a no-op when the

@@ -83,6 +83,7 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
             xa.zeros = zeros;
             xa.x = x;
             xa.y = y;
+            xa.bounds = bounds_counter();
             return launch_q4gemv_xreg(xp, xa, stream);
         }
     }

@@ -106,6 +106,7 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
     a.nblocks = 0;
     a.timeout_ns = g_stream_timeout_ns;
     a.status = stream_status_word();
+    a.bounds = bounds_counter();
     if (a.status == nullptr) return Q4_ERR_CUDA;
     const int u = stream_u(K);
     a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);

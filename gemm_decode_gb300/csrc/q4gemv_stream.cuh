@@ -86,6 +86,7 @@ struct StreamArgs {
     int nblocks;                     // blocks of rows (set by the launcher)
     unsigned long long timeout_ns;   // bound on every mbarrier wait
     unsigned int *status;            // device status word, set to 1 when a wait expires
+    unsigned int *bounds;            // out-of-range access counter (bounds-checking builds)
     StreamGeo geo;                   // used when the instance does not fix K and g
 };
 

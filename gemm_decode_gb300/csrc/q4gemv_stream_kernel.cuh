@@ -76,6 +76,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
     allow_next_grid();
 
     auto aborted = [&]() { return lds_volatile_u32(s_flag) != 0u; };
+    auto ib = [&](bool ok) { return q4_in_bounds(ok, a.bounds); };   // bounds-checking builds
     auto fail = [&]() {
         sts_volatile_u32(s_flag, 1u);
         atomicOr(a.status, 1u);
@@ -97,7 +98,9 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 const unsigned char *src_c = a.codes + row0 * (C * 16);
                 const unsigned char *src_s = reinterpret_cast<const unsigned char *>(a.scales) + row0 * (G.NB * 2);
                 const unsigned char *src_z = ASYM ? a.zeros + row0 * G.ZROW : nullptr;
-                if (rows == G.ROWS) {
+                if (!ib(row0 >= 0 && rows >= 1 && row0 + rows <= a.N && s < D)) {
+                    mbar_arrive(full(s));   // (checking builds) keep the ring moving, copy nothing
+                } else if (rows == G.ROWS) {
                     mbar_expect_tx(full(s), G.CODE_B + G.SC_B + G.Z_B);
                     bulk_copy(dst, src_c, G.CODE_B, full(s));
                     bulk_copy(dst + G.CODE_B, src_s, G.SC_B, full(s));
@@ -143,7 +146,8 @@ q4gemv_stream_kernel(const StreamArgs a) {
     for (int base = 0; base < C; base += G.TC / 4) {
         const int i = base + (tid >> 2);
         const bool in_range = i < C;
-        encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range, in_range, planes + (in_range ? i : 0) * kPlaneWords,
+        const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
+        encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range, planes + (in_range ? i : 0) * kPlaneWords,
                       tid & 3);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
@@ -185,7 +189,8 @@ q4gemv_stream_kernel(const StreamArgs a) {
         for (int rho = lane; rho < G.ROWS; rho += 32) {
             float acc = 0.0f;
 #pragma unroll 4
-            for (int q = 0; q < G.PARTS; ++q) acc += lds_f32(src + (rho * G.RED_LD + q) * 4);
+            for (int q = 0; q < G.PARTS; ++q)
+                if (ib(rho * G.RED_LD + q < G.ROWS * G.RED_LD)) acc += lds_f32(src + (rho * G.RED_LD + q) * 4);
             if (row0 + rho < a.N) a.y[row0 + rho] = acc;
         }
     };
@@ -209,9 +214,12 @@ q4gemv_stream_kernel(const StreamArgs a) {
         float v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const uint4 cw = lds128(sl + off_c + u * str_c);
-            const uint32_t sh = lds_u16(sl + off_s + u * str_s);
-            const int z = ASYM ? static_cast<int>((lds_u8(sl + off_z + u * str_z) >> zsh) & 0xFu) : 8;
+            const bool c_ok = ib(off_c + u * str_c + 16 <= static_cast<uint32_t>(G.CODE_B));
+            const bool s_ok = ib(off_s + u * str_s + 2 <= static_cast<uint32_t>(G.CODE_B + G.SC_B));
+            const bool z_ok = !ASYM || ib(off_z + u * str_z + 1 <= static_cast<uint32_t>(G.CODE_B + G.SC_B + G.Z_B));
+            const uint4 cw = c_ok ? lds128(sl + off_c + u * str_c) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t sh = s_ok ? lds_u16(sl + off_s + u * str_s) : 0u;
+            const int z = ASYM ? (z_ok ? static_cast<int>((lds_u8(sl + off_z + u * str_z) >> zsh) & 0xFu) : 8) : 8;
             const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sh)));
             v[u] = (sc * P.f) * chunk_dot(cw, z, P);
         }
@@ -219,13 +227,16 @@ q4gemv_stream_kernel(const StreamArgs a) {
         if constexpr (U_POW2) {
             if (G.WRED) {   // (the host pairs whole-warp rows with a power-of-two U only)
                 const float t = warp_sum_many<U>(v, lane);
-                if (red_writer) sts_f32(rd + red_off, t);
+                if (red_writer && ib(rb * G.RED_B + red_off + 4 <= static_cast<uint32_t>(kStreamNRed * G.RED_B)))
+                sts_f32(rd + red_off, t);
                 summed = true;
             }
         }
         if (!summed) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) sts_f32(rd + red_off + u * str_red, v[u]);
+            for (int u = 0; u < U; ++u)
+                if (ib(rb * G.RED_B + red_off + u * str_red + 4 <= static_cast<uint32_t>(kStreamNRed * G.RED_B)))
+                    sts_f32(rd + red_off + u * str_red, v[u]);
         }
         __syncwarp();
         if (lane == 0) {

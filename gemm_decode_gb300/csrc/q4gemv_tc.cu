@@ -63,6 +63,7 @@ struct TcArgs {
     int M, K, nb, zrow, gshift;
     unsigned long long timeout_ns;
     unsigned int *status;
+    unsigned int *bounds;   // out-of-range access counter (bounds-checking builds)
 };
 
 // (a & mask) | bits, one LOP3
@@ -160,6 +161,7 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         *abort_flag = 1;
         atomicOr(g.status, 1u);
     };
+    auto ib = [&](bool ok) { return q4_in_bounds(ok, g.bounds); };   // bounds-checking builds
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (codes)
@@ -171,9 +173,13 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                     fail();
                     break;
                 }
-                mbar_expect_tx(cfull(s), kCodeStage);
-                tma_load_2d(smem_addr(ctiles + s * kCodeStage), &tmap_codes, cfull(s), kb * (TK / 2),
-                            static_cast<int>(n0));
+                if (!ib(kb * (TK / 2) < (g.K + 1) / 2 && n0 < g.N)) {
+                    mbar_arrive(cfull(s));   // (checking builds) keep the ring moving, load nothing
+                } else {
+                    mbar_expect_tx(cfull(s), kCodeStage);
+                    tma_load_2d(smem_addr(ctiles + s * kCodeStage), &tmap_codes, cfull(s), kb * (TK / 2),
+                                static_cast<int>(n0));
+                }
                 issued = kb + 1;
             }
             if (*abort_flag) {
@@ -226,8 +232,8 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             const int k = kb * TK + half * 32;
             if (kb < kblocks && k < g.K) {
                 const int grp = k >> (5 + g.gshift);
-                f.sc = ldg_u16(srow + grp);
-                f.zb = zrow ? ldg_u8(zrow + (grp >> 1)) : 0u;
+                if (ib(grp < g.nb)) f.sc = ldg_u16(srow + grp);
+                if (zrow && ib((grp >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp >> 1));
             }
         };
         // slots xk .. xk + VPT - 1 of a block hold x at k = 8 * (slot / 8) + slot_k(slot % 8):
@@ -274,8 +280,8 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         auto step = [&](Side &f, int kb) -> bool {
             const int cs = kb % CST, ws = kb % WST;
             if (!mbar_wait(cfull(cs), (kb / CST) & 1, limit)) return false;
-            uint4 cw;
-            {
+            uint4 cw = make_uint4(0u, 0u, 0u, 0u);
+            if (ib(c_off + 16 <= static_cast<uint32_t>(kCodeStage))) {
                 const uint32_t ca = smem_addr(ctiles + cs * kCodeStage) + c_off;
                 asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                              : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
@@ -311,20 +317,25 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             unsigned char *wt = wtiles + ws * kWTile;
 #pragma unroll
             for (int w = 0; w < 4; ++w)
-                *reinterpret_cast<uint4 *>(wt + w_off[w]) =
-                    make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+                if (ib(w_off[w] + 16 <= static_cast<uint32_t>(kWTile)))
+                    *reinterpret_cast<uint4 *>(wt + w_off[w]) =
+                        make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
             // x: hi part in row xm, lo part in row MP + xm (VPT fp16 at slot offset xk)
             {
                 uint32_t hi[VPT / 2], lo[VPT / 2];
 #pragma unroll
                 for (int i = 0; i < VPT / 2; ++i) f16x2_split(f.xv[2 * i], f.xv[2 * i + 1], hi[i], lo[i]);
                 unsigned char *xt = xtiles + ws * kXTile;
-                if constexpr (VPT == 4) {
-                    *reinterpret_cast<uint2 *>(xt + xhi_off) = make_uint2(hi[0], hi[1]);
-                    *reinterpret_cast<uint2 *>(xt + xlo_off) = make_uint2(lo[0], lo[1]);
-                } else {
-                    *reinterpret_cast<uint32_t *>(xt + xhi_off) = hi[0];
-                    *reinterpret_cast<uint32_t *>(xt + xlo_off) = lo[0];
+                const bool x_ok = ib(xhi_off + VPT * 2 <= static_cast<uint32_t>(kXTile) &&
+                                     xlo_off + VPT * 2 <= static_cast<uint32_t>(kXTile));
+                if (x_ok) {
+                    if constexpr (VPT == 4) {
+                        *reinterpret_cast<uint2 *>(xt + xhi_off) = make_uint2(hi[0], hi[1]);
+                        *reinterpret_cast<uint2 *>(xt + xlo_off) = make_uint2(lo[0], lo[1]);
+                    } else {
+                        *reinterpret_cast<uint32_t *>(xt + xhi_off) = hi[0];
+                        *reinterpret_cast<uint32_t *>(xt + xlo_off) = lo[0];
+                    }
                 }
             }
             fence_proxy_async();      // generic-proxy stores -> visible to the tensor core
@@ -470,6 +481,7 @@ int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t
     g.timeout_ns = gemm_wait_timeout_ns();
     g.status = gemm_status_word();
     if (g.status == nullptr) return Q4_ERR_CUDA;
+    g.bounds = bounds_counter();
     return M <= 8 ? launch_tc<8>(map, g, stream) : launch_tc<16>(map, g, stream);
 }
 

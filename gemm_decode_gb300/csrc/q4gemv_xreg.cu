@@ -99,6 +99,14 @@ q4gemv_xreg_kernel(const XregArgs a) {
     const uint32_t my_s = ring_s + U * T * 16 + tid * 4;
     const uint32_t my_z = my_s + U * T * 4;
 
+    // bounds-checking builds: every global source lies inside its array (codes 16 bytes,
+    // scale and zero-point words 4 bytes), else the copy is counted and skipped
+    const int64_t codes_b = static_cast<int64_t>(a.N) * pitch, scales_b = static_cast<int64_t>(a.N) * nb * 2,
+                  zeros_b = static_cast<int64_t>(a.N) * zrow;
+    auto src_ok = [&](const void *p, const void *base, int64_t size, int bytes) {
+        const int64_t off = reinterpret_cast<const unsigned char *>(p) - reinterpret_cast<const unsigned char *>(base);
+        return q4_in_bounds(off >= 0 && off + bytes <= size, a.bounds);
+    };
     int issued = 0;
     auto issue_next = [&]() {
         if (active) {
@@ -107,9 +115,10 @@ q4gemv_xreg_kernel(const XregArgs a) {
             if (rb + ROWS_IT <= a.N) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    cp_async16(my_c + so + u * T * 16, gc + u * rg_c);
-                    cp_async4(my_s + so + u * T * 4, gs + u * rg_s);
-                    if (ASYM) cp_async4(my_z + so + u * T * 4, gz + u * rg_z);
+                    if (src_ok(gc + u * rg_c, a.codes, codes_b, 16)) cp_async16(my_c + so + u * T * 16, gc + u * rg_c);
+                    if (src_ok(gs + u * rg_s, a.scales, scales_b, 4)) cp_async4(my_s + so + u * T * 4, gs + u * rg_s);
+                    if (ASYM && src_ok(gz + u * rg_z, a.zeros, zeros_b, 4))
+                        cp_async4(my_z + so + u * T * 4, gz + u * rg_z);
                 }
             } else {
                 // Tail: a row past N reads row n - RG*k <= N-1 instead (same alignment
@@ -120,9 +129,10 @@ q4gemv_xreg_kernel(const XregArgs a) {
                     int64_t back = 0;
                     if (n >= a.N) back = (n - (a.N - 1) + RG - 1) / RG;
                     const int64_t j = u - back;
-                    cp_async16(my_c + so + u * T * 16, gc + j * rg_c);
-                    cp_async4(my_s + so + u * T * 4, gs + j * rg_s);
-                    if (ASYM) cp_async4(my_z + so + u * T * 4, gz + j * rg_z);
+                    if (src_ok(gc + j * rg_c, a.codes, codes_b, 16)) cp_async16(my_c + so + u * T * 16, gc + j * rg_c);
+                    if (src_ok(gs + j * rg_s, a.scales, scales_b, 4)) cp_async4(my_s + so + u * T * 4, gs + j * rg_s);
+                    if (ASYM && src_ok(gz + j * rg_z, a.zeros, zeros_b, 4))
+                        cp_async4(my_z + so + u * T * 4, gz + j * rg_z);
                 }
             }
         }

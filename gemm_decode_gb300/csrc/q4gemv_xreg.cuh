@@ -29,6 +29,7 @@ struct XregArgs {
     int red_ld;   // leading dimension of the partial-sum buffer
     int nsuper;   // iterations over all rows (kXregU * RG rows each)
     int off_red, off_ring, off_ysum;   // shared-memory offsets (bytes)
+    unsigned int *bounds;              // out-of-range access counter (bounds-checking builds)
 };
 
 struct XregPlan {

@@ -160,6 +160,15 @@ Q4_API int q4_dequant_bf16_run(const void *codes, const void *scales_f16, const 
 Q4_API int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t blocks,
                         int32_t *blocks_used, void *stream);
 
+/* Bounds-checking builds (compiled with -DQ4_BOUNDS_CHECK, a test-only variant of this
+ * library): the streamed, tensor-core and register-resident GEMV kernels check every
+ * shared- and global-memory index against its buffer, count each one out of range on a
+ * device counter and skip that access.  Synchronise `stream`, then return the count and
+ * reset it; -1 in a library built without the checks (the call touches no device then),
+ * -Q4_ERR_CUDA if synchronising or reading the counter failed.
+ * This is a debugging substitute for a memory checker; the pages have no counterpart. */
+Q4_API int q4gemv_bounds_violations(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

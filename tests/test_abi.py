@@ -131,3 +131,9 @@ def test_overlapped_launch_setting_round_trips(L):
     assert L.q4gemv_set_overlapped_launch(7) == 1
     assert L.q4gemv_set_overlapped_launch(0) == 1
     assert L.q4gemv_set_overlapped_launch(0) == 0
+
+
+def test_bounds_violations_query_without_checks(L):
+    # the product library is built without -DQ4_BOUNDS_CHECK: the query answers -1 and
+    # touches no device
+    assert L.q4gemv_bounds_violations(None) == -1

@@ -1,0 +1,76 @@
+"""The bounds-checking build (libq4gemv_check.so, -DQ4_BOUNDS_CHECK): every checked
+shared- and global-memory index of the streamed, tensor-core and register-resident GEMV
+kernels is compared with its buffer; one out of range is counted on a device counter
+and skipped.  With a memory checker unavailable, these tests run the shapes with the
+most index arithmetic (ragged last blocks and tiles, K tails, runtime geometry) through
+that build and require zero counted violations and results within tolerance.  Marked gpu.
+"""
+import numpy as np
+import pytest
+
+import gemm_decode_gb300 as q4
+import oracle
+import synth
+from gemm_decode_gb300 import build as q4build
+from gpu_util import assert_within_bound, dev, host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_cuda()
+    path = q4build.build(variant="check")
+    saved_lib, saved_path = q4._lib, q4.library_path
+    q4._lib = None
+    q4.library_path = lambda: path
+    try:
+        q4.lib()
+        assert q4.q4gemv_bounds_violations() == 0   # a checking build, counter clear
+        yield t
+    finally:
+        q4._lib, q4.library_path = saved_lib, saved_path
+
+
+def run_checked(torch, w, x, what, rows=None):
+    M, K = x.shape
+    y = torch.full((M, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                  M, w.N, K, w.group)
+    assert q4.q4gemv_bounds_violations() == 0, f"{what}: out-of-range accesses counted"
+    yh = host(y)
+    if rows is None:
+        y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, w.group)
+        assert_within_bound(yh, y_ref, bound, what)
+    else:
+        y_ref, bound = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, w.group, rows)
+        assert_within_bound(yh[:, rows], y_ref, bound, what)
+
+
+@pytest.mark.parametrize("symmetric", [False, True])
+@pytest.mark.parametrize("N,K,g", [(9765, 896, 32), (4899, 4096, 128), (4101, 14336, 128), (4099, 16384, 32)])
+def test_streamed_kernel(torch, N, K, g, symmetric):
+    # M = 1, many rows: the TMA-streamed kernel, partial last block; K = 14336 has no
+    # compile-time instance (runtime geometry)
+    w = synth.q4_weights(N + K, N, K, g, symmetric=symmetric, tag="bounds")
+    x = synth.activations_f32(N, 1, K)
+    run_checked(torch, w, x, f"streamed N={N} K={K} g={g}")
+
+
+@pytest.mark.parametrize("M,N,K,g", [(16, 8323, 4128, 32), (5, 8196, 2048, 64), (9, 4100, 896, 128)])
+def test_tensor_core_kernel(torch, M, N, K, g):
+    # partial last 128-row tile; K = 4128 leaves the last K-block half empty
+    w = synth.q4_weights(M + N + K, N, K, g, tag="bounds-tc")
+    x = synth.activations_f32(M + K, M, K)
+    run_checked(torch, w, x, f"tensor-core M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("M,N,K,g", [(1, 896, 896, 32), (1, 128, 896, 32), (1, 4864, 896, 32),
+                                     (1, 896, 4864, 32), (2, 1000, 2048, 64), (2, 77, 4096, 128)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_register_resident_kernel(torch, M, N, K, g, symmetric):
+    # M <= 2 below the streamed kernel's row count: per-thread cp.async rings, ragged
+    # row tails, split-K clusters for the long rows
+    w = synth.q4_weights(M * 3 + N + K, N, K, g, symmetric=symmetric, tag="bounds-xreg")
+    x = synth.activations_f32(N + M, M, K)
+    run_checked(torch, w, x, f"register-resident M={M} N={N} K={K}")
