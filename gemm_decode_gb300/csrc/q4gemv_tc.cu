@@ -45,8 +45,8 @@ namespace {
 
 constexpr int TM = 128;                    // weight rows per CTA (MMA M)
 constexpr int TK = 64;                     // K per block: one 128-byte row of fp16
-constexpr int CST = 10;                    // code-ring stages
-constexpr int WST = 3;                     // weight/x tile stages
+constexpr int CST = 16;                    // code-ring stages (a power of two: cheap slot and parity)
+constexpr int WST = 2;                     // weight/x tile stages (a power of two)
 constexpr int PF = 4;                      // scale / zero-point / x prefetch distance (blocks)
 constexpr int kDeqWarps = 8;
 constexpr int kThreads = (2 + kDeqWarps) * 32;
