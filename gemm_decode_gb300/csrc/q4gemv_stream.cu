@@ -17,7 +17,7 @@
 // sums go to one of two shared buffers (summed over the warp first when a row
 // spans whole warps); the reduction of block b is done by one consumer warp
 // (rotating) while the others already compute block b+1, ordered by mbarriers
-// rather than CTA barriers.  Every wait is bounded by a %globaltimer deadline
+// rather than CTA barriers; all consumer warps share the last block's.  Every wait is bounded by a %globaltimer deadline
 // (device status word on expiry).  The row geometry is fixed at compile time for
 // the two decode LM-head shapes and read from the arguments otherwise.
 #include "q4gemv_stream_kernel.cuh"

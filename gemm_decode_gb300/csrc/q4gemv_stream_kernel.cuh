@@ -184,14 +184,23 @@ q4gemv_stream_kernel(const StreamArgs a) {
     const uint32_t red_off = G.WRED ? ((red_u * G.RG + r) * G.RED_LD + (c >> 5)) * 4 : (r * G.RED_LD + c) * 4;
     const uint32_t str_red = G.RG * G.RED_LD * 4;
 
-    auto reduce_block = [&](int buf, int64_t row0) {
+    // Sum the partials of rows [lo, hi) of a block and store them: ql lanes per row
+    // (a power of two), each adding every ql-th partial, combined by shuffles.
+    // ql = 1 is a lane per row, partials in order.
+    auto reduce_rows = [&](int buf, int64_t row0, int lo, int hi, int ql) {
         const uint32_t src = s_red + buf * G.RED_B;
-        for (int rho = lane; rho < G.ROWS; rho += 32) {
+        const int q = lane & (ql - 1);
+        for (int base = lo; base < hi; base += 32 / ql) {   // warp-uniform trip count
+            const int rho = base + lane / ql;
+            const bool mine = rho < hi;
             float acc = 0.0f;
+            if (mine) {
 #pragma unroll 4
-            for (int q = 0; q < G.PARTS; ++q)
-                if (ib(rho * G.RED_LD + q < G.ROWS * G.RED_LD)) acc += lds_f32(src + (rho * G.RED_LD + q) * 4);
-            if (row0 + rho < a.N) a.y[row0 + rho] = acc;
+                for (int p = q; p < G.PARTS; p += ql)
+                    if (ib(rho * G.RED_LD + p < G.ROWS * G.RED_LD)) acc += lds_f32(src + (rho * G.RED_LD + p) * 4);
+            }
+            for (int o = ql >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (mine && q == 0 && row0 + rho < a.N) a.y[row0 + rho] = acc;
         }
     };
 
@@ -249,7 +258,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 fail();
                 break;
             }
-            reduce_block(pb, static_cast<int64_t>(b_begin + i - 1) * G.ROWS);
+            reduce_rows(pb, static_cast<int64_t>(b_begin + i - 1) * G.ROWS, 0, G.ROWS, 1);
             __syncwarp();
             if (lane == 0) mbar_arrive(reddone(pb));
         }
@@ -265,13 +274,29 @@ q4gemv_stream_kernel(const StreamArgs a) {
             ph ^= 1;
         }
     }
-    // the last block's reduction
-    if (nbk > 0 && !aborted() && warp == (nbk - 1) % G.NWC) {
+    // the last block's reduction.  With per-thread partials (many per row) and a
+    // compile-time geometry it is shared by all consumer warps, none of which has a
+    // block left: warp w sums rows [w * rpw, (w + 1) * rpw), ql lanes per row.
+    // Otherwise the next warp of the rotation does all of it, as for the other
+    // blocks (measured faster with per-warp partials, and it keeps the registers of
+    // the runtime-geometry instance down).
+    if (nbk > 0 && !aborted()) {
+        int lo = 0, hi = G.ROWS, ql = 1;
+        if (KC == 0 || G.WRED) {
+            if (warp != (nbk - 1) % G.NWC) hi = 0;
+        } else {
+            const int rpw = (G.ROWS + G.NWC - 1) / G.NWC;
+            lo = warp * rpw < G.ROWS ? warp * rpw : G.ROWS;
+            hi = lo + rpw < G.ROWS ? lo + rpw : G.ROWS;
+            while (ql * 2 * rpw <= 32 && ql < G.PARTS) ql *= 2;
+        }
         const int lb = (nbk - 1) % NRED;
-        if (!mbar_wait(redfull(lb), ((nbk - 1) / NRED) & 1, limit))
-            fail();
-        else
-            reduce_block(lb, static_cast<int64_t>(b_end - 1) * G.ROWS);
+        if (lo < hi) {
+            if (!mbar_wait(redfull(lb), ((nbk - 1) / NRED) & 1, limit))
+                fail();
+            else
+                reduce_rows(lb, static_cast<int64_t>(b_end - 1) * G.ROWS, lo, hi, ql);
+        }
     }
 }
 

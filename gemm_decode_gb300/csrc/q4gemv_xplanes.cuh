@@ -169,28 +169,17 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// try_wait with a suspend-time hint: the thread sleeps until the phase completes or
-// about hint_ns pass, instead of spinning through the issue slots of working warps.
-__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
 // Wait for the phase with the given parity to complete, for at most limit_ns
-// (checked between suspended tries of at most 20 us each).
+// (checked between potentially blocking tries, each suspended for at most the
+// system's own time limit; measured slightly faster than a 20 us suspend hint
+// and than spinning on test_wait in the streamed GEMV).
 // A zero bound means one non-blocking test (the timer is too coarse to mean less).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
     if (limit_ns == 0) return mbar_test(bar, parity);
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
-        if (mbar_try_sleep(bar, parity, 20000u)) return true;
+        if (mbar_try(bar, parity)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
