@@ -749,6 +749,8 @@ def parse_args(argv=None):
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--sweep", action="store_true",
                    help="time every cell of the shape sweep instead of the decode step")
+    p.add_argument("--sweep-parts", default="q4,f32,probe",
+                   help="comma-separated parts of --sweep: q4 (int4 GEMV cells), f32 (control), probe (read sizes)")
     p.add_argument("--sweep-out", default=None,
                    help="JSON-lines checkpoint for --sweep: cells already in the file are not re-timed")
     p.add_argument("--overlap", type=int, default=1,
@@ -820,20 +822,20 @@ def _device_q4(torch, gen, N, K, g, symmetric, scale):
     return c, sc, z
 
 
-def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n, samples=5):
-    """Microseconds per q4gemv_run call from a CUDA graph of n back-to-back launches
-    over the replicas: one untimed replay, then `samples` replays each between events on
-    the launching stream (median, p10, p90, min), and one event pair around two replays
-    (t(2n) / t(n), which is 2 when the per-call time has no fixed overhead in it)."""
-    nrep = len(reps)
+def _time_launches(torch, stream, launch, n, samples=5):
+    """Microseconds per call of launch(i) from a CUDA graph of n back-to-back calls
+    (i = 0 .. n-1): two eager calls, one untimed replay, then `samples` replays each
+    between events on the launching stream (median, p10, p90, min), and one event pair
+    around two replays (t(2n) / t(n), which is 2 when the per-call time has no fixed
+    overhead in it)."""
     with torch.cuda.stream(stream):
-        for r in reps[:2]:
-            q4.q4gemv_run(*r, x, y, M, N, K, g, stream=stream)
+        for i in range(2):
+            launch(i)
     torch.cuda.synchronize()
     gr = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gr, stream=stream):
         for i in range(n):
-            q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream)
+            launch(i)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(samples + 1)]
     with torch.cuda.stream(stream):
         gr.replay()
@@ -852,6 +854,14 @@ def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n, samples=5):
     q = lambda f: t[min(len(t) - 1, max(0, int(round(f * (len(t) - 1)))))]
     return {"us": med, "p10": q(0.1), "p90": q(0.9), "min": t[0], "samples": samples, "n": n,
             "t2n_over_tn": t2 / med}
+
+
+def _time_back_to_back(torch, q4, stream, reps, x, y, M, N, K, g, n, samples=5):
+    """Microseconds per q4gemv_run call from a CUDA graph of n back-to-back launches
+    over the weight replicas (see _time_launches)."""
+    nrep = len(reps)
+    return _time_launches(torch, stream,
+                          lambda i: q4.q4gemv_run(*reps[i % nrep], x, y, M, N, K, g, stream=stream), n, samples)
 
 
 def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
@@ -931,12 +941,18 @@ def run_decode_8b(args, torch, q4):
 
 
 def sweep_key(cell):
+    kind = cell.get("kind", "q4")
+    if kind == "f32":
+        return ("f32", cell["M"], cell["N"], cell["K"])
+    if kind == "probe":
+        return ("probe", cell["bytes"])
     return (cell["M"], cell["N"], cell["K"], cell["group"], cell["symmetric"])
 
 
 def load_sweep_checkpoint(path):
     """Cells of an earlier --sweep run (one JSON object per line), keyed by
-    (M, N, K, group, symmetric); a missing file or path None gives none.  A line cut
+    (M, N, K, group, symmetric) for int4 cells, ("f32", M, N, K) for the f32 control
+    and ("probe", bytes) for the read probe; a missing file or path None gives none.  A line cut
     short by an interrupted run is ignored."""
     done = {}
     if not path or not os.path.exists(path):
@@ -955,10 +971,13 @@ def load_sweep_checkpoint(path):
 
 
 def run_sweep(args):
-    """Every cell of the shape sweep (M, K, N, group, symmetric): microseconds per
-    q4gemv_run call and achieved GB/s, from a CUDA graph of back-to-back launches over
-    rotating weight replicas (cold in HBM where the replicas exceed twice the L2).
-    Weights are drawn on the device (timing only; parity is the tests' job)."""
+    """Every cell of the shape sweep: the int4 GEMV over (M, K, N, group, symmetric),
+    the f32 control over (M, K, N), and the vec4 read probe over buffer sizes 16 KiB,
+    32 KiB, ... 4 GiB (--sweep-parts picks among "q4", "f32", "probe").  Microseconds per
+    call and achieved GB/s, from a CUDA graph of back-to-back launches; the GEMVs rotate
+    over weight replicas (cold in HBM where the replicas exceed twice the L2), the probe
+    re-reads one buffer (so sizes below the L2 show its read rate, the knee).  Inputs are
+    drawn on the device (timing only; parity is the tests' job)."""
     import torch
     import gemm_decode_gb300 as q4
     q4.lib()
@@ -975,7 +994,15 @@ def run_sweep(args):
     out = open(args.sweep_out, "a") if args.sweep_out else None
     cells = []
     sw = synth.SWEEP
-    for K in sw["Ks"]:
+    parts = set(args.sweep_parts.split(","))
+
+    def emit(cell):
+        cells.append(cell)
+        if out is not None:
+            out.write(json.dumps(cell) + "\n")
+            out.flush()
+
+    for K in (sw["Ks"] if "q4" in parts else ()):
         for N in sw["Ns"]:
             for g in sw["groups"]:
                 nb = K // g
@@ -1007,20 +1034,71 @@ def run_sweep(args):
                                 "pct_of_measured_copy": round(100 * gbs / peak, 1),
                                 "packed_weight_bytes": wbytes,
                                 "cold": nrep * wbytes >= 2 * L2_BYTES}
-                        cells.append(cell)
-                        if out is not None:
-                            out.write(json.dumps(cell) + "\n")
-                            out.flush()
+                        emit(cell)
                     del reps
                     torch.cuda.empty_cache()
+    # the f32 control: W ~ N(0, 0.02) drawn on the device, 4 bytes per weight
+    for K in (sw["Ks"] if "f32" in parts else ()):
+        for N in sw["Ns"]:
+            wbytes = 4 * N * K
+            todo = [M for M in sw["Ms"] if ("f32", M, N, K) not in done]
+            cells += [done[("f32", M, N, K)] for M in sw["Ms"] if ("f32", M, N, K) in done]
+            if not todo:
+                continue
+            nrep = int(min(256, max(2, -(-6 * L2_BYTES // wbytes))))
+            Ws = [torch.randn((N, K), dtype=torch.float32, device="cuda", generator=gen) * 0.02 for _ in range(nrep)]
+            for M in todo:
+                x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
+                y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+                est_us = max(2.0, wbytes / 5e6)   # at about 5 TB/s
+                n = int(max(nrep, min(400, 20000 / est_us)))
+                st = _time_launches(torch, stream,
+                                    lambda i: q4.f32gemv_run(Ws[i % nrep], x, y, M, N, K, stream=stream), n)
+                byts = wbytes + 4 * M * K + 4 * M * N
+                gbs = byts / st["us"] / 1e3
+                emit({"kind": "f32", "M": M, "N": N, "K": K, "us_per_call": round(st["us"], 3),
+                      "gbs": round(gbs, 1),
+                      "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+                      "t2n_over_tn": round(st["t2n_over_tn"], 3),
+                      "status": "ok" if st["t2n_over_tn"] >= 1.2 else "noise",
+                      "pct_of_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                      "pct_of_measured_copy": round(100 * gbs / peak, 1),
+                      "weight_bytes": wbytes, "cold": nrep * wbytes >= 2 * L2_BYTES})
+            del Ws
+            torch.cuda.empty_cache()
+    # the read probe: prefixes of one 4 GiB buffer, 16 KiB doubling to 4 GiB
+    if "probe" in parts:
+        sizes = [16384 << i for i in range(19)]
+        todo = [b for b in sizes if ("probe", b) not in done]
+        cells += [done[("probe", b)] for b in sizes if ("probe", b) in done]
+        if todo:
+            pbuf = torch.rand(max(todo) // 4, dtype=torch.float32, device="cuda", generator=gen)
+            partial = torch.zeros(1 << 16, dtype=torch.float32, device="cuda")
+            for b in todo:
+                est_us = max(2.0, b / 6e6)   # at about 6 TB/s
+                n = int(max(8, min(400, 20000 / est_us)))
+                st = _time_launches(torch, stream,
+                                    lambda i: q4.vec4_read_probe_run(pbuf, b, partial, stream=stream), n)
+                gbs = b / st["us"] / 1e3
+                emit({"kind": "probe", "bytes": b, "us_per_call": round(st["us"], 3), "gbs": round(gbs, 1),
+                      "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+                      "t2n_over_tn": round(st["t2n_over_tn"], 3),
+                      "status": "ok" if st["t2n_over_tn"] >= 1.2 else "noise",
+                      "in_l2": b <= L2_BYTES, "pct_of_measured_copy": round(100 * gbs / peak, 1)})
+            del pbuf
+            torch.cuda.empty_cache()
     if out is not None:
         out.close()
-    big = [c for c in cells if c["M"] == 1 and c["packed_weight_bytes"] >= 64e6]
+    big = [c for c in cells if c.get("kind", "q4") == "q4" and c["M"] == 1 and c["packed_weight_bytes"] >= 64e6]
+    probe = [c for c in cells if c.get("kind") == "probe"]
     summary = {"device": device, "noise_cells": sum(1 for c in cells if c.get("status") == "noise"),"cells_m1_ge_64MB": len(big),
                "min_gbs_m1_ge_64MB": min(c["gbs"] for c in big) if big else None,
                "median_gbs_m1_ge_64MB": statistics.median(c["gbs"] for c in big) if big else None,
-               "peak": peak, "peak_source": peak_src}
-    return {"metric": "int4 GEMV sweep: us/call and achieved GB/s per cell", "unit": "GB/s",
+               "peak": peak, "peak_source": peak_src,
+               "probe_max_gbs_in_l2": max((c["gbs"] for c in probe if c["in_l2"]), default=None),
+               "probe_max_gbs_beyond_l2": max((c["gbs"] for c in probe if not c["in_l2"]), default=None)}
+    return {"metric": "GEMV sweep (int4, f32 control) and read-probe sizes: us/call and achieved GB/s per cell",
+            "unit": "GB/s",
             "launch": "overlapped" if args.overlap else "serialised", "summary": summary, "cells": cells}
 
 

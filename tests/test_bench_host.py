@@ -89,10 +89,14 @@ def test_sweep_checkpoint_round_trip(tmp_path):
     import bench
     path = tmp_path / "sweep.jsonl"
     cells = [{"M": 1, "N": 4096, "K": 896, "group": 32, "symmetric": False, "us_per_call": 2.0},
-             {"M": 16, "N": 4096, "K": 896, "group": 32, "symmetric": True, "us_per_call": 9.0}]
+             {"M": 16, "N": 4096, "K": 896, "group": 32, "symmetric": True, "us_per_call": 9.0},
+             {"kind": "f32", "M": 1, "N": 4096, "K": 896, "us_per_call": 3.0},
+             {"kind": "probe", "bytes": 16384, "us_per_call": 1.5}]
     path.write_text("".join(json.dumps(c) + "\n" for c in cells) + '{"M": 1, "N": 51')
     done = bench.load_sweep_checkpoint(str(path))
-    assert set(done) == {(1, 4096, 896, 32, False), (16, 4096, 896, 32, True)}
+    assert set(done) == {(1, 4096, 896, 32, False), (16, 4096, 896, 32, True), ("f32", 1, 4096, 896),
+                         ("probe", 16384)}
     assert done[(16, 4096, 896, 32, True)]["us_per_call"] == 9.0
+    assert done[("f32", 1, 4096, 896)]["us_per_call"] == 3.0
     assert bench.load_sweep_checkpoint(str(tmp_path / "missing.jsonl")) == {}
     assert bench.load_sweep_checkpoint(None) == {}
