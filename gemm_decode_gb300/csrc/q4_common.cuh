@@ -62,7 +62,7 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
                   cudaStream_t stream);
 int launch_f32gemv(const float *W, const float *x, float *y, int M, int64_t N, int K,
                    cudaStream_t stream);
-// 2 <= M <= 16 on the tensor cores (q4gemv_tc.cu): whether it serves the problem, and the launch.
+// 3 <= M <= 16 on the tensor cores (q4gemv_tc.cu): whether it serves the problem, and the launch.
 bool tc_gemv_applies(int M, int64_t N, int K, const void *codes);
 int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x, float *y,
                      int M, int64_t N, int K, int group, cudaStream_t stream);

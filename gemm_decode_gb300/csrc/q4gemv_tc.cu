@@ -1,4 +1,4 @@
-// q4gemv_tc.cu -- the 2 <= M <= 16 int4 GEMV on the 5th-generation tensor cores.
+// q4gemv_tc.cu -- the 3 <= M <= 16 int4 GEMV on the 5th-generation tensor cores.
 //
 // Computes y[m][n] = sum_k w[n][k] * x[m][k], w[n][k] = (q[n][k] - z[n][k/g]) * s[n][k/g]
 // (gerbil GPU-engine kernel reference, "3. MatMulInt4": "Computes", "Dequantization";
@@ -27,8 +27,15 @@
 //               scales, zero points and x are prefetched into registers 4 blocks ahead;
 //   warps 2..5  afterwards read the accumulator (one TMEM lane per weight row) and
 //               store y.
+// Few weight rows (N / 128 tiles well below two per SM): the K-blocks of a tile are
+// split over a cluster of S CTAs (grid y), each accumulating its own range in its own
+// TMEM; the epilogue leaves each CTA's partial rows in shared memory and every CTA of
+// the cluster finishes a share of the rows by adding the S partials in rank order
+// through distributed shared memory (deterministic, nothing written to global memory
+// but y).
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA raises the device
 // status word (read by q4gemv_device_status), drains what it issued and returns.
+#include <cooperative_groups.h>
 #include <cuda_fp16.h>
 
 #include "q4_common.cuh"
@@ -37,6 +44,7 @@
 namespace q4 {
 
 using namespace tc;
+namespace cg = cooperative_groups;
 
 unsigned int *gemm_status_word();
 unsigned long long gemm_wait_timeout_ns();
@@ -61,6 +69,7 @@ struct TcArgs {
     float *y;
     int64_t N;
     int M, K, nb, zrow, gshift;
+    int S;                  // K split: CTAs per cluster (grid y), 1 = no cluster
     unsigned long long timeout_ns;
     unsigned int *status;
     unsigned int *bounds;   // out-of-range access counter (bounds-checking builds)
@@ -104,7 +113,9 @@ constexpr size_t tc_smem_bytes() {
            8 * (2 * CST + 2 * WST + 1) + 16;
 }
 
-template <int MP>
+// SPLIT: the launch is a cluster of g.S CTAs along grid y sharing each tile's K-blocks
+// (compiled separately so the unsplit kernel carries none of it).
+template <int MP, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 2)
 q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g) {
     constexpr int NX = 2 * MP;                   // MMA N: MP hi rows then MP lo rows
@@ -123,7 +134,14 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * TM;
-    const int kblocks = (g.K + TK - 1) / TK;
+    // this CTA's K-blocks: [kb_begin, kb_end) of the tile's kblocks_all (its share of the
+    // cluster's split); ring slots and parities count from kb_begin
+    const int kblocks_all = (g.K + TK - 1) / TK;
+    const int split = SPLIT ? g.S : 1;
+    const int rank = SPLIT ? static_cast<int>(blockIdx.y) : 0;
+    const int kb_begin = static_cast<int>(static_cast<int64_t>(kblocks_all) * rank / split);
+    const int kb_end = static_cast<int>(static_cast<int64_t>(kblocks_all) * (rank + 1) / split);
+    const int nkb = kb_end - kb_begin;
     const unsigned long long limit = g.timeout_ns;
 
     const uint32_t bar0 = smem_addr(bars);
@@ -167,9 +185,10 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         // ------------------------------------------------------------ TMA producer (codes)
         if (lane == 0) {
             int issued = 0;
-            for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
-                const int s = kb % CST;
-                if (kb >= CST && !mbar_wait(cempty(s), ((kb / CST) - 1) & 1, limit)) {
+            for (int j = 0; j < nkb && !*abort_flag; ++j) {
+                const int kb = kb_begin + j;
+                const int s = j % CST;
+                if (j >= CST && !mbar_wait(cempty(s), ((j / CST) - 1) & 1, limit)) {
                     fail();
                     break;
                 }
@@ -180,20 +199,20 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                     tma_load_2d(smem_addr(ctiles + s * kCodeStage), &tmap_codes, cfull(s), kb * (TK / 2),
                                 static_cast<int>(n0));
                 }
-                issued = kb + 1;
+                issued = j + 1;
             }
             if (*abort_flag) {
                 // drain (bounded): every issued box lands before the CTA may exit
-                for (int kb = issued - CST > 0 ? issued - CST : 0; kb < issued; ++kb)
-                    mbar_wait(cfull(kb % CST), (kb / CST) & 1, 50ull * 1000 * 1000);
+                for (int j = issued - CST > 0 ? issued - CST : 0; j < issued; ++j)
+                    mbar_wait(cfull(j % CST), (j / CST) & 1, 50ull * 1000 * 1000);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
-                const int s = kb % WST;
-                if (!mbar_wait(wfull(s), (kb / WST) & 1, limit)) {
+            for (int j = 0; j < nkb && !*abort_flag; ++j) {
+                const int s = j % WST;
+                if (!mbar_wait(wfull(s), (j / WST) & 1, limit)) {
                     fail();
                     break;
                 }
@@ -203,7 +222,7 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
 #pragma unroll
                 for (int kk = 0; kk < TK / 16; ++kk)   // 16 fp16 = 32 bytes per step in the swizzle span
                     umma_f16(tmem, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), kIdescTc,
-                             (kb > 0 || kk > 0) ? 1u : 0u);
+                             (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(wempty(s));
             }
             umma_commit(done_bar);   // all issued MMAs complete (also the drain on abort)
@@ -230,7 +249,7 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         };
         auto fetch_w = [&](Side &f, int kb) {
             const int k = kb * TK + half * 32;
-            if (kb < kblocks && k < g.K) {
+            if (kb < kb_end && k < g.K) {
                 const int grp = k >> (5 + g.gshift);
                 if (ib(grp < g.nb)) f.sc = ldg_u16(srow + grp);
                 if (zrow && ib((grp >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp >> 1));
@@ -245,26 +264,26 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         const bool xlive = xm < g.M;
         auto fetch_x = [&](Side &f, int kb) {
             const int k0 = kb * TK;
-            if (xlive && k0 + TK <= g.K) {          // a whole block inside K
+            if (xlive && kb < kb_end && k0 + TK <= g.K) {   // a whole block inside K
 #pragma unroll
                 for (int i = 0; i < VPT; ++i) f.xv[i] = __ldg(xrow + k0 + xoff[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < VPT; ++i)
-                    f.xv[i] = (xlive && kb < kblocks && k0 + xoff[i] < g.K) ? __ldg(xrow + k0 + xoff[i]) : 0.0f;
+                    f.xv[i] = (xlive && kb < kb_end && k0 + xoff[i] < g.K) ? __ldg(xrow + k0 + xoff[i]) : 0.0f;
             }
         };
         static_assert(PF == 4, "the K loop below is unrolled over four register sets");
         Side f0{}, f1{}, f2{}, f3{};
-        fetch_w(f0, 0);
-        fetch_w(f1, 1);
-        fetch_w(f2, 2);
-        fetch_w(f3, 3);
+        fetch_w(f0, kb_begin);
+        fetch_w(f1, kb_begin + 1);
+        fetch_w(f2, kb_begin + 2);
+        fetch_w(f3, kb_begin + 3);
         wait_prior_grid();   // x and y may belong to the kernel before this one in the stream
-        fetch_x(f0, 0);
-        fetch_x(f1, 1);
-        fetch_x(f2, 2);
-        fetch_x(f3, 3);
+        fetch_x(f0, kb_begin);
+        fetch_x(f1, kb_begin + 1);
+        fetch_x(f2, kb_begin + 2);
+        fetch_x(f3, kb_begin + 3);
 
         // loop-invariant shared-memory offsets of this thread
         const uint32_t c_off = static_cast<uint32_t>(row * (TK / 2) + half * 16);
@@ -275,11 +294,13 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         const uint32_t xhi_off = sw128_offset(xm, xk >> 3) + within;
         const uint32_t xlo_off = sw128_offset(MP + xm, xk >> 3) + within;
 
-        // One K-block with the register set f that holds its side data, which is then
-        // refilled for block kb + PF.  Returns false when a bounded wait expired.
-        auto step = [&](Side &f, int kb) -> bool {
-            const int cs = kb % CST, ws = kb % WST;
-            if (!mbar_wait(cfull(cs), (kb / CST) & 1, limit)) return false;
+        // The j-th K-block of this CTA (block kb_begin + j) with the register set f that
+        // holds its side data, which is then refilled for block kb + PF.  Returns false
+        // when a bounded wait expired.
+        auto step = [&](Side &f, int j) -> bool {
+            const int kb = kb_begin + j;
+            const int cs = j % CST, ws = j % WST;
+            if (!mbar_wait(cfull(cs), (j / CST) & 1, limit)) return false;
             uint4 cw = make_uint4(0u, 0u, 0u, 0u);
             if (ib(c_off + 16 <= static_cast<uint32_t>(kCodeStage))) {
                 const uint32_t ca = smem_addr(ctiles + cs * kCodeStage) + c_off;
@@ -287,7 +308,7 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                              : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
                              : "r"(ca));
             }
-            if (kb >= WST && !mbar_wait(wempty(ws), ((kb / WST) - 1) & 1, limit)) return false;
+            if (j >= WST && !mbar_wait(wempty(ws), ((j / WST) - 1) & 1, limit)) return false;
             const int k = kb * TK + half * 32;     // first code of this thread's 32
             uint32_t out[16];
             if (k < g.K) {
@@ -351,11 +372,11 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             return true;
         };
 
-        for (int kb0 = 0; kb0 < kblocks && !*abort_flag; kb0 += PF) {
-            bool ok = step(f0, kb0);
-            if (ok && kb0 + 1 < kblocks) ok = step(f1, kb0 + 1);
-            if (ok && kb0 + 2 < kblocks) ok = step(f2, kb0 + 2);
-            if (ok && kb0 + 3 < kblocks) ok = step(f3, kb0 + 3);
+        for (int j0 = 0; j0 < nkb && !*abort_flag; j0 += PF) {
+            bool ok = step(f0, j0);
+            if (ok && j0 + 1 < nkb) ok = step(f1, j0 + 1);
+            if (ok && j0 + 2 < nkb) ok = step(f2, j0 + 2);
+            if (ok && j0 + 3 < nkb) ok = step(f3, j0 + 3);
             if (!ok) {
                 fail();
                 break;
@@ -392,13 +413,48 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                 }
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 const int64_t nn = n0 + quad * 32 + lane;   // weight row = TMEM lane
-                if (nn < g.N) {
+                if constexpr (!SPLIT) {
+                    if (nn < g.N) {
+#pragma unroll
+                        for (int m = 0; m < MP; ++m)
+                            if (m < g.M)
+                                g.y[static_cast<int64_t>(m) * g.N + nn] = __uint_as_float(v[m]) + __uint_as_float(v[MP + m]);
+                    }
+                } else {
+                    // this CTA's partial of row quad * 32 + lane (no MMA ran if its K range is
+                    // empty: the partial is 0), into the freed weight tiles
+                    float *red = reinterpret_cast<float *>(wtiles);
+                    const int r = quad * 32 + lane;
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
-                        if (m < g.M) g.y[static_cast<int64_t>(m) * g.N + nn] = __uint_as_float(v[m]) + __uint_as_float(v[MP + m]);
+                        if (ib((r * (MP + 1) + m + 1) * 4 <= WST * kWTile))
+                            red[r * (MP + 1) + m] = nkb > 0 ? __uint_as_float(v[m]) + __uint_as_float(v[MP + m]) : 0.0f;
                 }
             }
         }
+    }
+    if constexpr (SPLIT) {
+        // every CTA of the cluster finishes rows [rank * TM / S, (rank + 1) * TM / S) of
+        // the tile by adding the S partials in rank order
+        cg::cluster_group cluster = cg::this_cluster();
+        __syncwarp();     // (the producer and MMA lanes rejoin their warps first)
+        cluster.sync();
+        if (warp >= 2 && warp < 6 && !*abort_flag) {
+            const float *red = reinterpret_cast<const float *>(wtiles);
+            const int r_lo = rank * TM / split, r_hi = (rank + 1) * TM / split;
+            for (int i = (warp - 2) * 32 + lane; i < (r_hi - r_lo) * MP; i += 128) {
+                const int r = r_lo + i / MP, m = i % MP;
+                const int64_t nn = n0 + r;
+                if (m < g.M && nn < g.N) {
+                    float acc = 0.0f;
+                    for (int q = 0; q < split; ++q)
+                        if (ib((r * (MP + 1) + m + 1) * 4 <= WST * kWTile))
+                            acc += cluster.map_shared_rank(red, q)[r * (MP + 1) + m];
+                    g.y[static_cast<int64_t>(m) * g.N + nn] = acc;
+                }
+            }
+        }
+        cluster.sync();   // peers' shared memory stays valid until every read is done
     }
     // ---- teardown: every issued MMA finished before TMEM is released ----
     if (warp == 1 && lane == 0 && *abort_flag) mbar_wait(done_bar, 0, 50ull * 1000 * 1000);
@@ -412,21 +468,36 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
 
 // ------------------------------------------------------------------ host side
 
+// K split (CTAs per cluster, a power of two up to the portable 8): the fewest that give
+// a CTA per SM, keeping at least four K-blocks per CTA.  (Splitting further, to two
+// CTAs per SM, measured slower: the extra CTAs run as a second wave.)
+static int tc_gemv_split(int64_t N, int K) {
+    const int64_t tiles = (N + TM - 1) / TM;
+    const int kblocks = (K + TK - 1) / TK;
+    const int64_t want = device_info().sms;
+    int S = 1;
+    while (S < 8 && tiles * S < want && kblocks / (2 * S) >= 4) S *= 2;
+    return S;
+}
+
 // Where the tensor-core GEMV beats the CUDA-core kernels (measured on the decode and
-// sweep shapes): its time is nearly flat in M but it has only N / 128 CTAs, so it wins
-// for many rows of x and enough weight rows.
+// sweep shapes at M = 3, 4, 5, 8, 9, 16): with the K split it wins from M = 5 on every
+// matrix of at least 2^20 weights, and at M = 3 and 4 on long rows (K >= 2048, N >= 768)
+// and on large matrices (2^24 weights and up); the CUDA-core kernels keep the small
+// short-row shapes (896 x 896, 4864 x 896, 512 x 2048 at M <= 4), whose launches are
+// latency-bound.
 bool tc_gemv_applies(int M, int64_t N, int K, const void *codes) {
     if (M < 3 || M > 16) return false;
     if (K % 32 != 0 || !aligned(codes, 16)) return false;   // TMA: row pitch K/2 a multiple of 16 bytes
-    if (N > (int64_t(1) << 31) - TM) return false;
-    if (M >= 9) return N >= 4096;
-    if (M >= 5) return N >= 8192;
-    return N >= 65536;
+    if (N < TM || N > (int64_t(1) << 31) - TM) return false;   // at least one whole 128-row tile
+    const int64_t weights = N * static_cast<int64_t>(K);
+    if (M >= 5) return weights >= (int64_t(1) << 20);
+    return (K >= 2048 && N >= 768) || weights >= (int64_t(1) << 24);
 }
 
-template <int MP>
+template <int MP, bool SPLIT>
 static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t stream) {
-    auto kern = q4gemv_tc_kernel<MP>;
+    auto kern = q4gemv_tc_kernel<MP, SPLIT>;
     constexpr size_t smem = tc_smem_bytes<MP>();
     static bool configured[64] = {};
     int dev = 0;
@@ -440,11 +511,19 @@ static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t strea
         configured[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((g.N + TM - 1) / TM), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>((g.N + TM - 1) / TM), static_cast<unsigned>(g.S), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    if (SPLIT) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = static_cast<unsigned>(g.S);
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     add_overlap_attr(cfg, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, g);
     if (e != cudaSuccess) {
@@ -482,7 +561,9 @@ int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t
     g.status = gemm_status_word();
     if (g.status == nullptr) return Q4_ERR_CUDA;
     g.bounds = bounds_counter();
-    return M <= 8 ? launch_tc<8>(map, g, stream) : launch_tc<16>(map, g, stream);
+    g.S = tc_gemv_split(N, K);
+    if (g.S > 1) return M <= 8 ? launch_tc<8, true>(map, g, stream) : launch_tc<16, true>(map, g, stream);
+    return M <= 8 ? launch_tc<8, false>(map, g, stream) : launch_tc<16, false>(map, g, stream);
 }
 
 }  // namespace q4

@@ -57,12 +57,23 @@ def test_streamed_kernel(torch, N, K, g, symmetric):
     run_checked(torch, w, x, f"streamed N={N} K={K} g={g}")
 
 
-@pytest.mark.parametrize("M,N,K,g", [(16, 8323, 4128, 32), (5, 8196, 2048, 64), (9, 4100, 896, 128)])
+@pytest.mark.parametrize("M,N,K,g", [(16, 8323, 4128, 32), (5, 8196, 2048, 64), (9, 4100, 896, 128),
+                                     (8, 4100, 4128, 32), (3, 900, 4864, 64)])
 def test_tensor_core_kernel(torch, M, N, K, g):
-    # partial last 128-row tile; K = 4128 leaves the last K-block half empty
+    # partial last 128-row tile; K = 4128 leaves the last K-block half empty; with these
+    # few tiles each tile's K-blocks are split over a cluster (2 to 8 CTAs, uneven shares)
     w = synth.q4_weights(M + N + K, N, K, g, tag="bounds-tc")
     x = synth.activations_f32(M + K, M, K)
     run_checked(torch, w, x, f"tensor-core M={M} N={N} K={K}")
+
+
+def test_tensor_core_kernel_unsplit(torch):
+    # 153 tiles (more than one per SM): no K split; partial last tile and K-block
+    M, N, K, g = 16, 19500, 4128, 32
+    w = synth.q4_weights(41, N, K, g, tag="bounds-tc-unsplit")
+    x = synth.activations_f32(42, M, K)
+    rows = sorted(set(np.random.default_rng(6).choice(N, size=64, replace=False).tolist()) | {0, N - 1})
+    run_checked(torch, w, x, f"tensor-core unsplit M={M} N={N} K={K}", rows=rows)
 
 
 @pytest.mark.parametrize("M,N,K,g", [(1, 896, 896, 32), (1, 128, 896, 32), (1, 4864, 896, 32),

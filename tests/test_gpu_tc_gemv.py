@@ -1,8 +1,11 @@
 """GPU parity of the tensor-core GEMV against the CPU oracle.
 
-It serves 3 <= M <= 16 with enough weight rows (M >= 9 from N = 4096, M >= 5 from
-8192, M = 3..4 from 65536); the cases below pick M and N inside that region.  The
-kernel dequantises each weight exactly and rounds it once to fp16 (relative error
+It serves 3 <= M <= 16 from one whole 128-row tile on: for M >= 5 every matrix of at
+least 2^20 weights, for M = 3..4 long rows (K >= 2048, N >= 768) and matrices of at
+least 2^24 weights; the cases below pick M and N inside that region.  With few tiles
+the K-blocks of each tile are split over a cluster of up to 8 CTAs whose partial sums
+are added in rank order (the split cases below).  The kernel dequantises each weight
+exactly and rounds it once to fp16 (relative error
 <= 2^-11), splits x into fp16 hi + lo parts and accumulates in fp32 in tensor memory.
 Every case is checked against the stated tolerance 1e-3*sum|w x| + 1e-6 and against
 the tighter bound that follows from that arithmetic, (2^-11 + 2^-18)*sum|w x| + 1e-6.
@@ -150,3 +153,44 @@ def test_bounded_wait_reports_timeout_without_fault(torch):
     assert q4.q4gemv_device_status() == q4.Q4_OK   # the flag was cleared
     rows = [0, 1, 4095, 77777, N - 1]
     check(torch, w, x, "after timeout", rows=rows)
+
+
+@pytest.mark.parametrize("N,K,g,Ms", [
+    (4096, 4096, 128, (3, 4, 5, 8, 9, 16)),     # 32 tiles: 8 CTAs per cluster, 8 K-blocks each
+    (896, 4864, 32, (3, 8, 16)),                # 7 tiles, 76 K-blocks over 8 CTAs (uneven shares)
+    (4099, 14336, 128, (4, 9)),                 # a 3-row last tile, 224 K-blocks
+    (1024, 4128, 32, (5, 16)),                  # 65 K-blocks, the last one half empty
+    (14336, 4096, 64, (4, 8)),                  # 112 tiles: 2 CTAs per cluster
+    (300, 4864, 64, (5, 13)),                   # 3 tiles, the last one 44 rows
+])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_split_k_clusters_against_oracle(torch, N, K, g, Ms, symmetric):
+    w = synth.q4_weights(N + 3 * K + g, N, K, g, symmetric=symmetric, tag="tc-split")
+    rows = None if N <= 4096 else sorted(set(np.random.default_rng(5).choice(N, size=96, replace=False).tolist())
+                                         | {0, N - 1})
+    for M in Ms:
+        x = synth.activations_f32(N + M, M, K)
+        check(torch, w, x, f"split N={N} K={K} g={g} M={M} sym={symmetric}", rows=rows)
+
+
+def test_split_k_deterministic(torch):
+    # partial sums are added in rank order: repeated calls agree bit for bit
+    w = synth.q4_weights(17, 4096, 14336, 128, tag="tc-split-det")
+    x = synth.activations_f32(18, 8, 14336)
+    np.testing.assert_array_equal(run(torch, w, x), run(torch, w, x))
+
+
+def test_split_k_bounded_wait_reports_timeout_without_fault(torch):
+    N, K = 4096, 4096
+    w = synth.q4_weights(23, N, K, 128, tag="tc-split-timeout")
+    x = synth.activations_f32(24, 8, K)
+    y = torch.zeros((8, N), dtype=torch.float32, device="cuda")
+    try:
+        q4.q4gemm_set_wait_timeout_ns(0)
+        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y, 8, N, K, 128)
+        st = q4.q4gemv_device_status()
+    finally:
+        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    assert st == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK
+    check(torch, w, x, "after timeout (split)")
