@@ -6,33 +6,34 @@
 // the CUDA-core GEMV pays its multiply-adds once per row of x; here one dequantisation
 // of each weight serves every row through the tensor core.
 //
-// Roles: the weights are the MMA's A operand (M = 128 weight rows per CTA), x the B
-// operand.  x is split into two fp16 parts, x = hi + lo with hi = fp16(x) and
-// lo = fp16(x - hi), stored as 2*MP rows of B (hi rows 0..MP-1, lo rows MP..2MP-1,
-// rows past M zero), so the MMA's N is 16 or 32 and D = [W x_hi^T | W x_lo^T] sits in
-// 16 or 32 TMEM columns; the epilogue adds the two halves.  Each weight is dequantised
-// exactly in binary32 ((q - z) * s) and rounded once to fp16 (relative error at most
-// 2^-11, inside the 1e-3 tolerance); hi + lo carries x to about 2^-22.
+// Roles: the weights are the MMA's A operand (256 weight rows per CTA, two MMAs of
+// M = 128 sharing each x tile), x the B operand.  x is split into two fp16 parts,
+// x = hi + lo with hi = fp16(x) and lo = fp16(x - hi), stored as 2*MP rows of B (hi rows
+// 0..MP-1, lo rows MP..2MP-1, rows past M zero), so the MMA's N is 16 or 32 and each
+// D = [W x_hi^T | W x_lo^T] sits in 16 or 32 TMEM columns; the epilogue adds the two
+// halves.  Each weight is dequantised exactly in binary32 ((q - z) * s) and rounded once
+// to fp16 (relative error at most 2^-11, inside the 1e-3 tolerance); hi + lo carries x to
+// about 2^-22.
 //
-//   warp 0      TMA producer: the 128 rows x 32 bytes of codes of each 64-wide K-block
-//               (2D tensor map over codes[N][K/2]) into a deep ring, completion counted
-//               on the slot's mbarrier;
-//   warp 1      allocates 32 TMEM columns; one lane issues 4 MMAs (K = 16 each) per
-//               K-block and commits them to the weight/x stage's "empty" barrier;
-//   warps 2..9  dequantisers: each thread turns 32 codes of one weight row (read from
-//               the code ring) into fp16 in the UMMA K-major 128-byte-swizzled layout
-//               (k permuted within each group of 8 to the decode's nibble-pair order),
-//               and converts its share of x for the same K-block into the hi/lo rows
-//               with the same permutation;
-//               scales, zero points and x are prefetched into registers 4 blocks ahead;
-//   warps 2..5  afterwards read the accumulator (one TMEM lane per weight row) and
-//               store y.
-// Few weight rows (N / 128 tiles well below two per SM): the K-blocks of a tile are
-// split over a cluster of S CTAs (grid y), each accumulating its own range in its own
-// TMEM; the epilogue leaves each CTA's partial rows in shared memory and every CTA of
-// the cluster finishes a share of the rows by adding the S partials in rank order
-// through distributed shared memory (deterministic, nothing written to global memory
-// but y).
+//   warp 0      TMA producer: the 256 rows x 32 bytes of codes of each 64-wide K-block
+//               (2D tensor map over codes[N][K/2]) into a 4-stage ring, completion
+//               counted on the slot's mbarrier;
+//   warp 1      allocates 64 TMEM columns (two accumulators); one lane issues 2 x 4 MMAs
+//               (K = 16 each) per K-block and commits them to the weight/x stage's
+//               "empty" barrier;
+//   warps 2..9  dequantisers: each thread turns the 64 codes of one weight row in a
+//               K-block (read from the code ring) into fp16 in the UMMA K-major
+//               128-byte-swizzled layout (k permuted within each group of 8 to the
+//               decode's nibble-pair order), and converts its share of x for the same
+//               K-block into the hi/lo rows with the same permutation; scales, zero
+//               points and x are prefetched into registers 4 blocks ahead; afterwards
+//               each warp reads one TMEM lane quadrant of one accumulator (one lane per
+//               weight row) and stores y.
+// Few weight rows (N / 256 tiles below one per SM): the K-blocks of a tile are split
+// over a cluster of S CTAs (grid y), each accumulating its own range in its own TMEM;
+// the epilogue leaves each CTA's partial rows in shared memory and every CTA of the
+// cluster finishes a share of the rows by adding the S partials in rank order through
+// distributed shared memory (deterministic, nothing written to global memory but y).
 // Every mbarrier wait is bounded by %globaltimer; on expiry the CTA raises the device
 // status word (read by q4gemv_device_status), drains what it issued and returns.
 #include <cooperative_groups.h>
@@ -51,16 +52,26 @@ unsigned long long gemm_wait_timeout_ns();
 
 namespace {
 
-constexpr int TM = 128;                    // weight rows per CTA (MMA M)
+constexpr int TMH = 128;                   // MMA M
 constexpr int TK = 64;                     // K per block: one 128-byte row of fp16
-constexpr int CST = 16;                    // code-ring stages (a power of two: cheap slot and parity)
 constexpr int WST = 2;                     // weight/x tile stages (a power of two)
 constexpr int PF = 4;                      // scale / zero-point / x prefetch distance (blocks)
 constexpr int kDeqWarps = 8;
 constexpr int kThreads = (2 + kDeqWarps) * 32;
-constexpr int kCodeStage = TM * TK / 2;    // 4 KB of codes per block
-constexpr int kWTile = TM * TK * 2;        // 16 KB of fp16 weights per block
-constexpr int kTmemCols = 32;
+
+// Tile geometry: TM weight rows per CTA, 128 (one MMA, two dequantiser threads per row)
+// or 256 (two MMAs sharing each x tile, one dequantiser thread per row: half the
+// per-weight cost of the waits, side data and x conversion, half the tiles).
+template <int TM_>
+struct TcGeo {
+    static constexpr int TM = TM_;
+    static constexpr int NACC = TM / TMH;              // accumulators: MMAs per K step
+    static constexpr int NH = TM / TMH;                // 32-code halves per dequantiser thread and block
+    static constexpr int CST = TM == 256 ? 4 : 16;     // code-ring stages (a power of two: cheap slot and parity)
+    static constexpr int kCodeStage = TM * TK / 2;     // codes per block: 4 or 8 KB
+    static constexpr int kWTile = TM * TK * 2;         // fp16 weights per block: 16 or 32 KB
+    static constexpr int kTmemCols = 32 * NACC;        // accumulators of up to 32 columns
+};
 
 struct TcArgs {
     const uint16_t *scales;
@@ -107,20 +118,24 @@ __device__ __forceinline__ int slot_k(int j) { return (j >> 1) + 4 * (j & 1); }
 
 }  // namespace
 
-template <int MP>
+template <int MP, int TMV>
 constexpr size_t tc_smem_bytes() {
-    return 1024 + static_cast<size_t>(WST) * (kWTile + 2 * MP * TK * 2) + static_cast<size_t>(CST) * kCodeStage +
-           8 * (2 * CST + 2 * WST + 1) + 16;
+    using Gm = TcGeo<TMV>;
+    return 1024 + static_cast<size_t>(WST) * (Gm::kWTile + 2 * MP * TK * 2) +
+           static_cast<size_t>(Gm::CST) * Gm::kCodeStage + 8 * (2 * Gm::CST + 2 * WST + 1) + 16;
 }
 
 // SPLIT: the launch is a cluster of g.S CTAs along grid y sharing each tile's K-blocks
 // (compiled separately so the unsplit kernel carries none of it).
-template <int MP, bool SPLIT>
+template <int MP, bool SPLIT, int TMV>
 __global__ void __launch_bounds__(kThreads, 2)
 q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g) {
+    using Gm = TcGeo<TMV>;
+    constexpr int TM = Gm::TM, NACC = Gm::NACC, NH = Gm::NH, CST = Gm::CST;
+    constexpr int kCodeStage = Gm::kCodeStage, kWTile = Gm::kWTile, kTmemCols = Gm::kTmemCols;
     constexpr int NX = 2 * MP;                   // MMA N: MP hi rows then MP lo rows
     constexpr int kXTile = NX * TK * 2;          // 2 or 4 KB
-    constexpr uint32_t kIdescTc = idesc_f16(false, TM, NX);
+    constexpr uint32_t kIdescTc = idesc_f16(false, TMH, NX);
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -220,9 +235,11 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                 const uint32_t a_base = smem_addr(wtiles + s * kWTile);
                 const uint32_t b_base = smem_addr(xtiles + s * kXTile);
 #pragma unroll
-                for (int kk = 0; kk < TK / 16; ++kk)   // 16 fp16 = 32 bytes per step in the swizzle span
-                    umma_f16(tmem, umma_desc(a_base + kk * 32), umma_desc(b_base + kk * 32), kIdescTc,
-                             (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < TK / 16; ++kk)     // 16 fp16 = 32 bytes per step in the swizzle span
+#pragma unroll
+                    for (int a = 0; a < NACC; ++a)       // rows 128 a .. 128 a + 127 into columns 32 a ..
+                        umma_f16(tmem + 32u * a, umma_desc(a_base + a * (kWTile / NACC) + kk * 32),
+                                 umma_desc(b_base + kk * 32), kIdescTc, (j > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(wempty(s));
             }
             umma_commit(done_bar);   // all issued MMAs complete (also the drain on abort)
@@ -230,8 +247,10 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
     } else {
         // ------------------------------------------------------------ dequantisers
         const int t = threadIdx.x - 64;            // 0..255
-        const int row = t >> 1;                    // weight row within the tile
-        const int half = t & 1;                    // which 32 codes of the 64-wide K-block
+        // weight row within the tile and the first of the NH 32-code halves of each block
+        // this thread decodes (TM = 256: the whole row; TM = 128: one half)
+        const int row = NH == 2 ? t : t >> 1;
+        const int h0 = NH == 2 ? 0 : (t & 1);
         const int64_t n = n0 + row < g.N ? n0 + row : g.N - 1;
         const uint16_t *srow = g.scales + n * g.nb;
         const uint8_t *zrow = g.zeros ? g.zeros + n * g.zrow : nullptr;
@@ -241,18 +260,23 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         const int xm = t / TPR;                    // x row (< MP)
         const int xk = (t - xm * TPR) * VPT;       // first slot of the share within the block
 
-        // scale and zero-point byte of K-block kb for this thread's 32 codes, and this
-        // thread's share of x for the block
+        // scales of this thread's halves of K-block kb (the same group unless g = 32), the
+        // zero-point byte that holds their nibbles (with two halves and g = 32 the first
+        // half's group is even), and this thread's share of x for the block
         struct Side {
-            uint32_t sc, zb;
+            uint32_t sc[NH], zb;
             float xv[VPT];
         };
         auto fetch_w = [&](Side &f, int kb) {
-            const int k = kb * TK + half * 32;
+            const int k = kb * TK + h0 * 32;
             if (kb < kb_end && k < g.K) {
-                const int grp = k >> (5 + g.gshift);
-                if (ib(grp < g.nb)) f.sc = ldg_u16(srow + grp);
-                if (zrow && ib((grp >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp >> 1));
+                const int grp0 = k >> (5 + g.gshift);
+                if (ib(grp0 < g.nb)) f.sc[0] = ldg_u16(srow + grp0);
+                if constexpr (NH == 2) {
+                    const int grp1 = (k + 32) >> (5 + g.gshift);
+                    if (k + 32 < g.K && ib(grp1 < g.nb)) f.sc[1] = grp1 == grp0 ? f.sc[0] : ldg_u16(srow + grp1);
+                }
+                if (zrow && ib((grp0 >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp0 >> 1));
             }
         };
         // slots xk .. xk + VPT - 1 of a block hold x at k = 8 * (slot / 8) + slot_k(slot % 8):
@@ -285,11 +309,12 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         fetch_x(f2, kb_begin + 2);
         fetch_x(f3, kb_begin + 3);
 
-        // loop-invariant shared-memory offsets of this thread
-        const uint32_t c_off = static_cast<uint32_t>(row * (TK / 2) + half * 16);
-        uint32_t w_off[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) w_off[w] = sw128_offset(row, half * 4 + w);
+        // loop-invariant shared-memory offsets of this thread: its 32 code bytes, and its
+        // row in the weight tile (rows 128..255: the second operand).  Chunk w of the row
+        // sits at w_row ^ (w << 4): the swizzle XORs the chunk index with row & 7, and the
+        // row offset has those bits clear (a multiple of 128), as has the tile base.
+        const uint32_t c_off = static_cast<uint32_t>(row * (TK / 2) + h0 * 16);
+        const uint32_t w_row = (row >= TMH ? kWTile / 2 : 0) + sw128_offset(row & (TMH - 1), 0);
         const uint32_t within = static_cast<uint32_t>((xk & 7) * 2);   // byte offset inside the 16-byte chunk
         const uint32_t xhi_off = sw128_offset(xm, xk >> 3) + within;
         const uint32_t xlo_off = sw128_offset(MP + xm, xk >> 3) + within;
@@ -301,46 +326,58 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             const int kb = kb_begin + j;
             const int cs = j % CST, ws = j % WST;
             if (!mbar_wait(cfull(cs), (j / CST) & 1, limit)) return false;
-            uint4 cw = make_uint4(0u, 0u, 0u, 0u);
-            if (ib(c_off + 16 <= static_cast<uint32_t>(kCodeStage))) {
+            uint4 cw[NH];
+#pragma unroll
+            for (int i = 0; i < NH; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (ib(c_off + 16 * NH <= static_cast<uint32_t>(kCodeStage))) {
                 const uint32_t ca = smem_addr(ctiles + cs * kCodeStage) + c_off;
-                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                             : "=r"(cw.x), "=r"(cw.y), "=r"(cw.z), "=r"(cw.w)
-                             : "r"(ca));
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(cw[h].x), "=r"(cw[h].y), "=r"(cw[h].z), "=r"(cw[h].w)
+                                 : "r"(ca + 16u * h));
             }
             if (j >= WST && !mbar_wait(wempty(ws), ((j / WST) - 1) & 1, limit)) return false;
-            const int k = kb * TK + half * 32;     // first code of this thread's 32
-            uint32_t out[16];
-            if (k < g.K) {
-                const int grp = k >> (5 + g.gshift);
-                uint32_t z = 8u;
-                if (zrow) z = (grp & 1) ? (f.zb >> 4) : (f.zb & 0xFu);
-                // fp16 1024 + q from a nibble OR-ed into the fraction of 1024 (0x6400); the
-                // half2 subtraction of 1024 + z is exact, and one half2 multiply by s rounds the
-                // exact product (q - z) * s once -- the same value as rounding the binary32
-                // product.  Each word gives the nibble pairs (0,4), (1,5), (2,6), (3,7), stored in
-                // that order; x is stored with the same permutation of k.
-                const uint32_t zz = (0x6400u | z) * 0x00010001u;
-                const uint32_t ss = f.sc * 0x00010001u;
-                const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            const uint32_t wrow_addr = smem_addr(wtiles + ws * kWTile) + w_row;
+            // this thread's 32-code halves of the row's block, one after the other
+#pragma unroll
+            for (int i = 0; i < NH; ++i) {
+                const int h = h0 + i;              // which half of the 64-wide block
+                const int k = kb * TK + h * 32;    // first code of this half
+                uint32_t out[16];
+                if (k < g.K) {
+                    const int grp = k >> (5 + g.gshift);
+                    uint32_t z = 8u;
+                    if (zrow) z = (grp & 1) ? (f.zb >> 4) : (f.zb & 0xFu);
+                    // fp16 1024 + q from a nibble OR-ed into the fraction of 1024 (0x6400); the
+                    // half2 subtraction of 1024 + z is exact, and one half2 multiply by s rounds the
+                    // exact product (q - z) * s once -- the same value as rounding the binary32
+                    // product.  Each word gives the nibble pairs (0,4), (1,5), (2,6), (3,7), stored
+                    // in that order; x is stored with the same permutation of k.
+                    const uint32_t zz = (0x6400u | z) * 0x00010001u;
+                    const uint32_t ss = f.sc[i] * 0x00010001u;
+                    const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            const uint32_t m = lop3_or_and(words[w] >> (4 * p), 0x000F000Fu, 0x64006400u);
+                            out[4 * w + p] = f16x2_sub_mul(m, zz, ss);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) out[i] = 0u;   // K tail: zero weights
+                }
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const uint32_t m = lop3_or_and(words[w] >> (4 * p), 0x000F000Fu, 0x64006400u);
-                        out[4 * w + p] = f16x2_sub_mul(m, zz, ss);
-                    }
+                    const uint32_t chunk = static_cast<uint32_t>(4 * h + w) << 4;
+                    if (ib((w_row ^ chunk) + 16 <= static_cast<uint32_t>(kWTile)))
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(wrow_addr ^ chunk),
+                                     "r"(out[4 * w]), "r"(out[4 * w + 1]), "r"(out[4 * w + 2]), "r"(out[4 * w + 3])
+                                     : "memory");
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) out[i] = 0u;   // K tail: zero weights
             }
-            unsigned char *wt = wtiles + ws * kWTile;
-#pragma unroll
-            for (int w = 0; w < 4; ++w)
-                if (ib(w_off[w] + 16 <= static_cast<uint32_t>(kWTile)))
-                    *reinterpret_cast<uint4 *>(wt + w_off[w]) =
-                        make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
             // x: hi part in row xm, lo part in row MP + xm (VPT fp16 at slot offset xk)
             {
                 uint32_t hi[VPT / 2], lo[VPT / 2];
@@ -382,15 +419,16 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                 break;
             }
         }
-        // ------------------------------------------------------------ epilogue (warps 2..5)
-        if (warp < 6) {
+        // ------------------------------------------------------------ epilogue (warps 2..9, or 2..5)
+        if (NACC == 2 || warp < 6) {
             const int quad = warp & 3;             // TMEM lane quadrant this warp may access
+            const int acc = NACC == 2 ? (warp - 2) >> 2 : 0;   // accumulator: rows 0..127 or 128..255
             const bool ok = mbar_wait(done_bar, 0, limit);
             if (!ok) fail();
             if (ok && !*abort_flag) {
                 tc_fence_after();
                 uint32_t v[32];
-                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * 32);
                 if constexpr (NX == 32) {
                     asm volatile(
                         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -412,7 +450,8 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                         : "r"(taddr));
                 }
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                const int64_t nn = n0 + quad * 32 + lane;   // weight row = TMEM lane
+                const int r = acc * TMH + quad * 32 + lane;   // weight row: accumulator, TMEM lane
+                const int64_t nn = n0 + r;
                 if constexpr (!SPLIT) {
                     if (nn < g.N) {
 #pragma unroll
@@ -421,10 +460,9 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                                 g.y[static_cast<int64_t>(m) * g.N + nn] = __uint_as_float(v[m]) + __uint_as_float(v[MP + m]);
                     }
                 } else {
-                    // this CTA's partial of row quad * 32 + lane (no MMA ran if its K range is
-                    // empty: the partial is 0), into the freed weight tiles
+                    // this CTA's partial of row r (no MMA ran if its K range is empty: the
+                    // partial is 0), into the freed weight tiles
                     float *red = reinterpret_cast<float *>(wtiles);
-                    const int r = quad * 32 + lane;
 #pragma unroll
                     for (int m = 0; m < MP; ++m)
                         if (ib((r * (MP + 1) + m + 1) * 4 <= WST * kWTile))
@@ -439,10 +477,10 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         cg::cluster_group cluster = cg::this_cluster();
         __syncwarp();     // (the producer and MMA lanes rejoin their warps first)
         cluster.sync();
-        if (warp >= 2 && warp < 6 && !*abort_flag) {
+        if (warp >= 2 && !*abort_flag) {
             const float *red = reinterpret_cast<const float *>(wtiles);
             const int r_lo = rank * TM / split, r_hi = (rank + 1) * TM / split;
-            for (int i = (warp - 2) * 32 + lane; i < (r_hi - r_lo) * MP; i += 128) {
+            for (int i = (warp - 2) * 32 + lane; i < (r_hi - r_lo) * MP; i += kDeqWarps * 32) {
                 const int r = r_lo + i / MP, m = i % MP;
                 const int64_t nn = n0 + r;
                 if (m < g.M && nn < g.N) {
@@ -468,16 +506,28 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
 
 // ------------------------------------------------------------------ host side
 
-// K split (CTAs per cluster, a power of two up to the portable 8): the fewest that give
-// a CTA per SM, keeping at least four K-blocks per CTA.  (Splitting further, to two
-// CTAs per SM, measured slower: the extra CTAs run as a second wave.)
-static int tc_gemv_split(int64_t N, int K) {
-    const int64_t tiles = (N + TM - 1) / TM;
+// K split (CTAs per cluster, a power of two up to the portable 8) for tiles of tm rows:
+// the fewest that give a CTA per SM, keeping at least four K-blocks per CTA.  (Splitting
+// further, to two CTAs per SM, measured slower: the extra CTAs run as a second wave.)
+static int tc_gemv_split(int64_t N, int K, int tm) {
+    const int64_t tiles = (N + tm - 1) / tm;
     const int kblocks = (K + TK - 1) / TK;
     const int64_t want = device_info().sms;
     int S = 1;
     while (S < 8 && tiles * S < want && kblocks / (2 * S) >= 4) S *= 2;
     return S;
+}
+
+// Tile height: 256 rows (cheaper per weight) when that still gives two tiles per SM,
+// or when both heights need a K split and 256 rows launch at least as many CTAs;
+// otherwise 128 rows (twice the tiles).  Measured on the decode and sweep shapes.
+static int tc_gemv_tile_rows(int64_t N, int K) {
+    const int64_t sms = device_info().sms;
+    const int64_t t128 = (N + 127) / 128, t256 = (N + 255) / 256;
+    const int s128 = tc_gemv_split(N, K, 128), s256 = tc_gemv_split(N, K, 256);
+    if (t256 >= 2 * sms) return 256;
+    if (s128 > 1 && t256 * s256 >= t128 * s128) return 256;
+    return 128;
 }
 
 // Where the tensor-core GEMV beats the CUDA-core kernels (measured on the decode and
@@ -489,16 +539,16 @@ static int tc_gemv_split(int64_t N, int K) {
 bool tc_gemv_applies(int M, int64_t N, int K, const void *codes) {
     if (M < 3 || M > 16) return false;
     if (K % 32 != 0 || !aligned(codes, 16)) return false;   // TMA: row pitch K/2 a multiple of 16 bytes
-    if (N < TM || N > (int64_t(1) << 31) - TM) return false;   // at least one whole 128-row tile
+    if (N < TMH || N > (int64_t(1) << 31) - 256) return false;   // at least one whole 128-row tile
     const int64_t weights = N * static_cast<int64_t>(K);
     if (M >= 5) return weights >= (int64_t(1) << 20);
     return (K >= 2048 && N >= 768) || weights >= (int64_t(1) << 24);
 }
 
-template <int MP, bool SPLIT>
+template <int MP, bool SPLIT, int TMV>
 static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t stream) {
-    auto kern = q4gemv_tc_kernel<MP, SPLIT>;
-    constexpr size_t smem = tc_smem_bytes<MP>();
+    auto kern = q4gemv_tc_kernel<MP, SPLIT, TMV>;
+    constexpr size_t smem = tc_smem_bytes<MP, TMV>();
     static bool configured[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -511,7 +561,7 @@ static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t strea
         configured[dev] = true;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((g.N + TM - 1) / TM), static_cast<unsigned>(g.S), 1);
+    cfg.gridDim = dim3(static_cast<unsigned>((g.N + TMV - 1) / TMV), static_cast<unsigned>(g.S), 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -533,14 +583,22 @@ static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t strea
     return launch_status();
 }
 
+template <int TMV>
+static int launch_tc_rows(const CUtensorMap &map, const TcArgs &g, cudaStream_t stream) {
+    if (g.S > 1)
+        return g.M <= 8 ? launch_tc<8, true, TMV>(map, g, stream) : launch_tc<16, true, TMV>(map, g, stream);
+    return g.M <= 8 ? launch_tc<8, false, TMV>(map, g, stream) : launch_tc<16, false, TMV>(map, g, stream);
+}
+
 int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x, float *y,
                      int M, int64_t N, int K, int group, cudaStream_t stream) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode == nullptr) return Q4_ERR_CUDA;
+    const int tm = tc_gemv_tile_rows(N, K);
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    const cuuint32_t box[2] = {TK / 2, TM};
+    const cuuint32_t box[2] = {TK / 2, static_cast<cuuint32_t>(tm)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -561,9 +619,8 @@ int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t
     g.status = gemm_status_word();
     if (g.status == nullptr) return Q4_ERR_CUDA;
     g.bounds = bounds_counter();
-    g.S = tc_gemv_split(N, K);
-    if (g.S > 1) return M <= 8 ? launch_tc<8, true>(map, g, stream) : launch_tc<16, true>(map, g, stream);
-    return M <= 8 ? launch_tc<8, false>(map, g, stream) : launch_tc<16, false>(map, g, stream);
+    g.S = tc_gemv_split(N, K, tm);
+    return tm == 256 ? launch_tc_rows<256>(map, g, stream) : launch_tc_rows<128>(map, g, stream);
 }
 
 }  // namespace q4

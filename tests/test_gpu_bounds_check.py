@@ -67,11 +67,12 @@ def test_tensor_core_kernel(torch, M, N, K, g):
     run_checked(torch, w, x, f"tensor-core M={M} N={N} K={K}")
 
 
-def test_tensor_core_kernel_unsplit(torch):
-    # 153 tiles (more than one per SM): no K split; partial last tile and K-block
-    M, N, K, g = 16, 19500, 4128, 32
-    w = synth.q4_weights(41, N, K, g, tag="bounds-tc-unsplit")
-    x = synth.activations_f32(42, M, K)
+@pytest.mark.parametrize("M,N,K,g", [(16, 39100, 4128, 32), (9, 78000, 896, 128)])
+def test_tensor_core_kernel_unsplit(torch, M, N, K, g):
+    # enough tiles for no K split: 306 tiles of 128 rows, and 305 of 256 rows (two MMAs per
+    # CTA); partial last tiles, a half-empty last K-block
+    w = synth.q4_weights(41 + M, N, K, g, tag="bounds-tc-unsplit")
+    x = synth.activations_f32(42 + M, M, K)
     rows = sorted(set(np.random.default_rng(6).choice(N, size=64, replace=False).tolist()) | {0, N - 1})
     run_checked(torch, w, x, f"tensor-core unsplit M={M} N={N} K={K}", rows=rows)
 

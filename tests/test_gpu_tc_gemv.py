@@ -1,6 +1,7 @@
 """GPU parity of the tensor-core GEMV against the CPU oracle.
 
-It serves 3 <= M <= 16 from one whole 128-row tile on: for M >= 5 every matrix of at
+It serves 3 <= M <= 16 from one whole 128-row tile on (tiles of 128 rows, or of 256 as
+two MMAs per CTA where that still fills the GPU): for M >= 5 every matrix of at
 least 2^20 weights, for M = 3..4 long rows (K >= 2048, N >= 768) and matrices of at
 least 2^24 weights; the cases below pick M and N inside that region.  With few tiles
 the K-blocks of each tile are split over a cluster of up to 8 CTAs whose partial sums
@@ -156,11 +157,12 @@ def test_bounded_wait_reports_timeout_without_fault(torch):
 
 
 @pytest.mark.parametrize("N,K,g,Ms", [
-    (4096, 4096, 128, (3, 4, 5, 8, 9, 16)),     # 32 tiles: 8 CTAs per cluster, 8 K-blocks each
+    (4096, 4096, 128, (3, 4, 5, 8, 9, 16)),     # 32 tiles of 128 rows: 8 CTAs per cluster, 8 K-blocks each
     (896, 4864, 32, (3, 8, 16)),                # 7 tiles, 76 K-blocks over 8 CTAs (uneven shares)
     (4099, 14336, 128, (4, 9)),                 # a 3-row last tile, 224 K-blocks
     (1024, 4128, 32, (5, 16)),                  # 65 K-blocks, the last one half empty
-    (14336, 4096, 64, (4, 8)),                  # 112 tiles: 2 CTAs per cluster
+    (14336, 4096, 64, (4, 8)),                  # 56 tiles of 256 rows: 4 CTAs per cluster
+    (8196, 2048, 32, (5, 16)),                  # 33 tiles of 256 rows, the last 4 rows; 8 CTAs per cluster
     (300, 4864, 64, (5, 13)),                   # 3 tiles, the last one 44 rows
 ])
 @pytest.mark.parametrize("symmetric", [False, True])
