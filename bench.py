@@ -743,8 +743,8 @@ def parse_args(argv=None):
     p.add_argument("--ref-seconds", type=float, default=90.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--controls", type=int, default=1)
-    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "tc_m16", "f32_lm_head",
-                                         "gemm_ffn", "gemm_gate"],
+    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "tc_m16", "tc_lm05_m8",
+                                         "tc_down8b_m8", "f32_lm_head", "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--sweep", action="store_true",
@@ -770,7 +770,9 @@ PROFILE_CASES = {
     "lm_head": (151936, 896, 32, 1),
     "lm_head_8b": (128256, 4096, 128, 1),
     "down_8b": (4096, 14336, 128, 1),
-    "tc_m16": (32768, 4096, 128, 16),
+    "tc_m16": (32768, 4096, 128, 16),      # tensor-core GEMV, 128-row tiles, no K split
+    "tc_lm05_m8": (151936, 896, 32, 8),    # tensor-core GEMV, 256-row tiles (two MMAs per CTA)
+    "tc_down8b_m8": (4096, 14336, 128, 8), # tensor-core GEMV, K split over 8-CTA clusters
 }
 
 
