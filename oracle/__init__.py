@@ -93,6 +93,15 @@ def lib() -> ctypes.CDLL:
             L.orc_f32_gemv.restype = None
             L.orc_sum_f32.argtypes = [_f32p, _i64]
             L.orc_sum_f32.restype = ctypes.c_double
+            L.orc_rmsnorm.argtypes = [_f32p, _f32p, ctypes.c_double, _i64, _i64, _f64p]
+            L.orc_rmsnorm.restype = None
+            L.orc_q4_gemv_f64.argtypes = [_u8p, _u16p, _u8p, _f64p, _i64, _i64, _i64,
+                                          _i64, _f64p, _f64p]
+            L.orc_q4_gemv_f64.restype = None
+            L.orc_silu.argtypes = [ctypes.c_double]
+            L.orc_silu.restype = ctypes.c_double
+            L.orc_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
+            L.orc_swiglu.restype = None
             _lib = L
         return _lib
 
@@ -283,3 +292,89 @@ def f32_gemv_rows(W, x, rows):
 def sum_f32(buf) -> float:
     buf = np.ascontiguousarray(buf, np.float32).reshape(-1)
     return lib().orc_sum_f32(_ptr(buf, _f32p), buf.size)
+
+
+# --------------------------------------------------------------------------
+# the fused decode variants: RMSNorm prologue, SwiGLU epilogue
+# --------------------------------------------------------------------------
+
+SILU_SLOPE_MAX = 1.1   # |d silu / dv| <= 1.0998 for every real v
+
+
+def rmsnorm(x, gamma, eps: float) -> np.ndarray:
+    """binary64 [M, K]: x[m][k] / sqrt(mean_k x[m][k]^2 + eps) * gamma[k]."""
+    x = np.ascontiguousarray(x, np.float32)
+    gamma = np.ascontiguousarray(gamma, np.float32)
+    M, K = x.shape
+    assert gamma.shape == (K,)
+    out = np.empty((M, K), np.float64)
+    lib().orc_rmsnorm(_ptr(x, _f32p), _ptr(gamma, _f32p), float(eps), M, K, _ptr(out, _f64p))
+    return out
+
+
+def silu(v: float) -> float:
+    return lib().orc_silu(float(v))
+
+
+def swiglu(gate, up) -> np.ndarray:
+    gate = np.ascontiguousarray(gate, np.float64)
+    up = np.ascontiguousarray(up, np.float64)
+    assert gate.shape == up.shape
+    out = np.empty(gate.shape, np.float64)
+    lib().orc_swiglu(_ptr(gate, _f64p), _ptr(up, _f64p), gate.size, _ptr(out, _f64p))
+    return out
+
+
+def _q4_gemv_f64_rows(codes, scales, zeros, xf, g: int, rows):
+    M, K = xf.shape
+    N, nb = _check_q4(codes, scales, zeros, K, g)
+    zrow = (nb + 1) // 2
+    y = np.empty((M, len(rows)), np.float64)
+    b = np.empty((M, len(rows)), np.float64)
+    yr = np.empty((M, 1), np.float64)
+    br = np.empty((M, 1), np.float64)
+    for j, n in enumerate(rows):
+        lib().orc_q4_gemv_f64(_ptr(codes, _u8p, n * (K // 2)), _ptr(scales, _u16p, n * nb),
+                              None if zeros is None else _ptr(zeros, _u8p, n * zrow),
+                              _ptr(xf, _f64p), M, 1, K, g, _ptr(yr, _f64p), _ptr(br, _f64p))
+        y[:, j] = yr[:, 0]
+        b[:, j] = br[:, 0]
+    return y, b
+
+
+def q4_gemv_fused(codes, scales, zeros, x, gamma, eps: float, g: int, swiglu_epilogue: bool,
+                  outputs=None):
+    """The fused variant: y = W . RMSNorm(x) (or W . x when gamma is None), and with
+    the SwiGLU epilogue h[m][i] = silu(y[m][2i]) * y[m][2i+1] (rows 2i, 2i+1 of W are
+    the gate / up pair of output i).  `outputs` selects output columns (all when None).
+    Returns the reference (binary64) and the tolerance bound per output:
+      plain:  1e-3 * sum_k |w x'| + 1e-6, x' the (normalised) input, as for the GEMV;
+      SwiGLU: with B_g, B_u those bounds of the pair,
+              SILU_SLOPE_MAX * B_g * (|u| + B_u) + (|silu(g)| + SILU_SLOPE_MAX * B_g) * B_u
+              + 2^-20 |h| + 1e-6
+              (the first-order propagation of the pair's errors through silu(g) * u, and
+              binary32 rounding of the combine)."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    N, _ = _check_q4(codes, scales, zeros, K, g)
+    if gamma is None:
+        xf = x.astype(np.float64)
+    else:
+        xf = rmsnorm(x, gamma, eps)
+    if not swiglu_epilogue:
+        cols = list(range(N)) if outputs is None else [int(c) for c in outputs]
+        y, mag = _q4_gemv_f64_rows(codes, scales, zeros, xf, g, cols)
+        return y, 1e-3 * mag + 1e-6
+    assert N % 2 == 0
+    cols = list(range(N // 2)) if outputs is None else [int(c) for c in outputs]
+    rows = []
+    for i in cols:
+        rows += [2 * i, 2 * i + 1]
+    y, mag = _q4_gemv_f64_rows(codes, scales, zeros, xf, g, rows)
+    gate, up = y[:, 0::2], y[:, 1::2]
+    bg, bu = 1e-3 * mag[:, 0::2] + 1e-6, 1e-3 * mag[:, 1::2] + 1e-6
+    h = swiglu(gate, up)
+    sg = np.abs(swiglu(gate, np.ones_like(gate)))
+    bound = (SILU_SLOPE_MAX * bg * (np.abs(up) + bu) + (sg + SILU_SLOPE_MAX * bg) * bu
+             + 2.0 ** -20 * np.abs(h) + 1e-6)
+    return h, bound

@@ -224,6 +224,65 @@ void orc_f32_gemv(const float *W, const float *x, int64_t M, int64_t N,
     }
 }
 
+/* ---------------------------------------------------------------------- */
+/* The fused decode variants (the prologue and epilogue of a projection). */
+/* ---------------------------------------------------------------------- */
+
+/* gerbil GPU-engine kernel reference, section "4. RMSNorm", "Computes": each
+ * row of the input is divided by its root mean square, rms(v) =
+ * sqrt(mean(v^2) + eps), and multiplied elementwise by the weight vector.
+ * xn[m][k] = x[m][k] / rms(x[m][:]) * gamma[k], all in binary64 (the sum of
+ * squares in k order), nothing rounded. */
+void orc_rmsnorm(const float *x, const float *gamma, double eps, int64_t M,
+                 int64_t K, double *xn)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)x[m * K + k];
+            ss += v * v;
+        }
+        double rms = sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            xn[m * K + k] = (double)x[m * K + k] / rms * (double)gamma[k];
+    }
+}
+
+/* The GEMV of section "3. MatMulInt4" on a binary64 input (the normalised
+ * activations of the fused variant): y[m][n] = sum_k W[n][k] * x[m][k] and
+ * bound[m][n] = sum_k |W[n][k] * x[m][k]|, binary64 in k order, unrounded. */
+void orc_q4_gemv_f64(const uint8_t *codes, const uint16_t *scales,
+                     const uint8_t *zeros, const double *x, int64_t M,
+                     int64_t N, int64_t K, int64_t g, double *y, double *bound)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double w = (double)orc_q4_weight(codes, scales, zeros, K, g, n, k);
+                double p = w * x[m * K + k];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[m * N + n] = acc;
+            bound[m * N + n] = mag;
+        }
+    }
+}
+
+/* Section "9. SiLU", "Computes": silu(v) = v / (1 + exp(-v)); its
+ * optimisation notes name the SwiGLU combine, out = silu(gate) * up. */
+double orc_silu(double v)
+{
+    return v / (1.0 + exp(-v));
+}
+
+void orc_swiglu(const double *gate, const double *up, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_silu(gate[i]) * up[i];
+}
+
 /* Read probe (webgpu-bench README, "read-bandwidth"; Refractometer
  * "a) bandwidth"): the sum of every binary32 element of a buffer, in
  * binary64.  The probe kernel's own partial sums are compared against it. */

@@ -40,6 +40,14 @@ MUTANTS = {
                      "                mag += p;\n            }\n            y[m * N + n] = (float)acc;"),
     "f32_control_index": ("double p = (double)W[n * K + k] * (double)x[m * K + k];",
                           "double p = (double)W[k * N + n] * (double)x[m * K + k];"),
+    "rmsnorm_no_eps": ("double rms = sqrt(ss / (double)K + eps);", "double rms = sqrt(ss / (double)K);"),
+    "rmsnorm_mean_over_k_minus_1": ("double rms = sqrt(ss / (double)K + eps);",
+                                    "double rms = sqrt(ss / (double)(K - 1) + eps);"),
+    "rmsnorm_gamma_index": ("/ rms * (double)gamma[k];", "/ rms * (double)gamma[K - 1 - k];"),
+    "silu_sign": ("return v / (1.0 + exp(-v));", "return v / (1.0 + exp(v));"),
+    "swiglu_swapped": ("out[i] = orc_silu(gate[i]) * up[i];", "out[i] = orc_silu(up[i]) * gate[i];"),
+    "gemv_f64_dropped_first_term": ("double p = w * x[m * K + k];",
+                                    "double p = (k == 0) ? 0.0 : w * x[m * K + k];"),
 }
 
 

@@ -266,3 +266,86 @@ def test_brute_force_every_code_and_zero(g):
 def test_code_accessor_nibble_order():
     codes = np.array([[0x21, 0x43]], np.uint8)
     assert [oracle.q4_code(codes, 4, 0, k) for k in range(4)] == [1, 2, 3, 4]
+
+
+# ---------------------------------------------------------------------------
+# The fused decode variants: RMSNorm prologue ("4. RMSNorm" of the kernel
+# reference page), SiLU and the SwiGLU combine ("9. SiLU" and its notes).
+# ---------------------------------------------------------------------------
+
+SIGMOID_1 = 0.7310585786300049   # 1 / (1 + e^-1), the logistic function at 1
+
+
+def test_rmsnorm_constant_rows_closed_form():
+    # a row of equal values c: mean of squares c^2, so every element becomes
+    # c / sqrt(c^2 + eps) * gamma[k]; a row of -c gives the negation
+    K, c, eps = 96, 3.0, 0.25
+    x = np.full((2, K), c, np.float32)
+    x[1] = -c
+    gamma = np.random.default_rng(7).uniform(0.5, 2.0, K).astype(np.float32)
+    xn = oracle.rmsnorm(x, gamma, eps)
+    expect = c / math.sqrt(c * c + eps) * gamma.astype(np.float64)
+    np.testing.assert_allclose(xn[0], expect, rtol=1e-15, atol=0)
+    np.testing.assert_allclose(xn[1], -expect, rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_unit_mean_square_and_scale_invariance():
+    # with gamma = 1 and eps = 0 the output has mean square 1, and scaling a row by a
+    # power of two leaves it unchanged (every step scales exactly)
+    K = 640
+    x = synth.activations_f32(31, 3, K)
+    ones = np.ones(K, np.float32)
+    xn = oracle.rmsnorm(x, ones, 0.0)
+    np.testing.assert_allclose((xn * xn).mean(axis=1), 1.0, rtol=1e-13, atol=0)
+    np.testing.assert_array_equal(oracle.rmsnorm(x * np.float32(4.0), ones, 0.0), xn)
+
+
+def test_silu_values_and_odd_part():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(1.0) == pytest.approx(SIGMOID_1, rel=1e-15)
+    # silu(v) - silu(-v) = v (v sigma(v) + v (1 - sigma(v)))
+    for v in (-3.0, -0.5, 0.7, 5.0, 20.0):
+        assert oracle.silu(v) - oracle.silu(-v) == pytest.approx(v, rel=1e-14)
+    assert oracle.silu(60.0) == pytest.approx(60.0, rel=1e-15)
+    assert -1e-20 < oracle.silu(-60.0) < 0.0
+
+
+def test_swiglu_is_silu_of_gate_times_up():
+    gate = np.array([[0.0, 1.0, 1.0, -60.0]])
+    up = np.array([[5.0, 2.0, -3.0, 7.0]])
+    h = oracle.swiglu(gate, up)
+    np.testing.assert_allclose(h[0, :3], [0.0, 2.0 * SIGMOID_1, -3.0 * SIGMOID_1], rtol=1e-15, atol=0)
+    assert abs(h[0, 3]) < 1e-20
+
+
+def test_fused_gemv_reduces_to_the_plain_gemv():
+    N, K, g = 12, 256, 64
+    w = synth.q4_weights(41, N, K, g)
+    x = synth.activations_f32(42, 2, K)
+    y32, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, g)
+    # no normalisation: the binary64 result rounds to the plain oracle's value
+    y64, tol = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, None, 0.0, g, False)
+    np.testing.assert_array_equal(y64.astype(np.float32), y32)
+    # a row of +-1 has root mean square 1: with gamma = 1 and eps = 0 nothing changes
+    xs = np.where(x >= 0, 1.0, -1.0).astype(np.float32)
+    ys32, _ = oracle.q4_gemv(w.codes, w.scales, w.zeros, xs, g)
+    yn, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, xs, np.ones(K, np.float32), 0.0, g, False)
+    np.testing.assert_array_equal(yn.astype(np.float32), ys32)
+    # gamma = 2 doubles the normalised input, hence the output, exactly
+    y2, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, xs, np.full(K, 2.0, np.float32), 0.0, g, False)
+    np.testing.assert_array_equal(y2, 2.0 * yn)
+
+
+def test_fused_swiglu_pairs_even_rows_with_odd_rows():
+    # rows 2i (gate) and 2i+1 (up) of the weight feed output i
+    N, K, g = 10, 128, 32
+    w = synth.q4_weights(43, N, K, g)
+    x = synth.activations_f32(44, 2, K)
+    gamma = np.random.default_rng(9).uniform(0.5, 1.5, K).astype(np.float32)
+    y, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-5, g, False)
+    h, tol = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-5, g, True)
+    np.testing.assert_array_equal(h, oracle.swiglu(y[:, 0::2], y[:, 1::2]))
+    assert h.shape == (2, N // 2) and np.all(tol > 0)
+    # the selected-outputs form agrees with the full one
+    hs, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-5, g, True, outputs=[4, 1])
+    np.testing.assert_array_equal(hs, h[:, [4, 1]])
