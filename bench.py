@@ -912,8 +912,72 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / n
     byts = step_bytes(fshapes, 1, group)
-    return {"launches_per_step": len(fshapes), "shapes": [[nm, N, K] for nm, N, K in fshapes],
-            "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
+    out = {"launches_per_step": len(fshapes), "shapes": [[nm, N, K] for nm, N, K in fshapes],
+           "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
+
+    # the same four launches with the RMSNorm prologue fused into q|k|v, gate|up and the
+    # LM head, and the SwiGLU combine into gate|up (its rows read as interleaved gate / up
+    # pairs); down reads the combined activations gate|up leaves
+    K0 = fshapes[0][2]
+    gammas = [torch.from_numpy(np.random.default_rng(60 + i).uniform(0.5, 1.5, K0).astype(np.float32)).cuda()
+              for i in range(3)]
+    N_gu = fshapes[1][1]
+    h = torch.empty((1, N_gu // 2), dtype=torch.float32, device="cuda")
+    assert fshapes[2][2] == N_gu // 2
+
+    def step_fused(r):
+        (nq, Nq, Kq), (ng, Ng, Kg), (nd, Nd, Kd), (nl, Nl, Kl) = fshapes
+        c, sc, z = freps[r][0]
+        q4.q4gemv_fused_run(c, sc, z, fxs[0], gammas[0], 1e-6, fys[0], 1, Nq, Kq, group, stream=stream)
+        c, sc, z = freps[r][1]
+        q4.q4gemv_fused_run(c, sc, z, fxs[1], gammas[1], 1e-6, h, 1, Ng, Kg, group,
+                            epilogue=q4.Q4_EPILOGUE_SWIGLU, stream=stream)
+        c, sc, z = freps[r][2]
+        q4.q4gemv_run(c, sc, z, h, fys[2], 1, Nd, Kd, group, stream=stream)
+        c, sc, z = freps[r][3]
+        q4.q4gemv_fused_run(c, sc, z, fxs[3], gammas[2], 1e-6, fys[3], 1, Nl, Kl, group, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for r in range(replicas):
+            step_fused(r)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        for i in range(n):
+            step_fused(i % replicas)
+    with torch.cuda.stream(stream):
+        g2.replay()
+        e0.record(stream)
+        g2.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us2 = e0.elapsed_time(e1) * 1e3 / n
+    byts2 = byts - 4 * (N_gu // 2) + 3 * 4 * K0   # gate|up writes N/2 outputs; three gamma vectors
+    # each launch of the fused step alone, back to back over the replicas
+    (nq, Nq, Kq), (ng, Ng, Kg), (nd, Nd, Kd), (nl, Nl, Kl) = fshapes
+    nb = max(replicas, 200)
+    per_launch = {
+        nq + " (RMSNorm)": _time_launches(torch, stream, lambda i: q4.q4gemv_fused_run(
+            *freps[i % replicas][0], fxs[0], gammas[0], 1e-6, fys[0], 1, Nq, Kq, group, stream=stream), nb)["us"],
+        ng + " (RMSNorm, SwiGLU)": _time_launches(torch, stream, lambda i: q4.q4gemv_fused_run(
+            *freps[i % replicas][1], fxs[1], gammas[1], 1e-6, h, 1, Ng, Kg, group,
+            epilogue=q4.Q4_EPILOGUE_SWIGLU, stream=stream), nb)["us"],
+        nl + " (RMSNorm)": _time_launches(torch, stream, lambda i: q4.q4gemv_fused_run(
+            *freps[i % replicas][3], fxs[3], gammas[2], 1e-6, fys[3], 1, Nl, Kl, group, stream=stream), nb)["us"],
+    }
+    per_launch_plain = {
+        nm: _time_launches(torch, stream, lambda i, p=p, N=N, K=K: q4.q4gemv_run(
+            *freps[i % replicas][p], fxs[p], fys[p], 1, N, K, group, stream=stream), nb)["us"]
+        for p, (nm, N, K) in enumerate(fshapes) if p != 2}
+    out["with_rmsnorm_swiglu"] = {
+        "us_per_step": round(us2, 3), "gbs": round(byts2 / us2 / 1e3, 1), "bytes_per_step": byts2,
+        "launches_per_step": 4,
+        "us_per_launch_back_to_back": {k: round(v, 3) for k, v in per_launch.items()},
+        "us_per_launch_plain": {k: round(v, 3) for k, v in per_launch_plain.items()},
+        "what": "q4gemv_fused_run: RMSNorm prologue on q|k|v, gate|up and the LM head, SwiGLU epilogue on "
+                "gate|up (its output feeds down); the separate norm and activation launches this replaces "
+                "are not in the plain step"}
+    return out
 
 
 def run_decode_8b(args, torch, q4):

@@ -16,13 +16,13 @@ import threading
 
 __all__ = [
     "Q4Error", "lib", "library_path", "exported_names",
-    "q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
+    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemm_run", "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
     "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
     "q4gemv_bounds_violations",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
-    "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT",
+    "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT", "Q4_EPILOGUE_NONE", "Q4_EPILOGUE_SWIGLU",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +30,7 @@ _ROOT = os.path.dirname(_HERE)
 HEADER = os.path.join(_ROOT, "include", "q4gemv.h")
 
 Q4_OK, Q4_ERR_INVALID_ARG, Q4_ERR_UNSUPPORTED, Q4_ERR_MISALIGNED, Q4_ERR_CUDA, Q4_ERR_TIMEOUT = range(6)
+Q4_EPILOGUE_NONE, Q4_EPILOGUE_SWIGLU = 0, 1
 
 
 def library_path() -> str:
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(path)
             L.q4gemv_pack_info.argtypes = [_i64, _i64, _i32, ctypes.POINTER(_PackInfo)]
             L.q4gemv_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
+            L.q4gemv_fused_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i32, _i64, _i64,
+                                           _i32, _i32, _vp]
             L.q4gemm_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
             L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_status_string.argtypes = [ctypes.c_int]
@@ -84,7 +87,7 @@ def lib() -> ctypes.CDLL:
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
             L.q4gemv_bounds_violations.argtypes = [_vp]
-            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemm_run", "f32gemv_run",
+            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
                       "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations"):
@@ -154,6 +157,16 @@ def q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M=None, N=None, K=None
                           _addr(y), M, N, K, int(group), _stream(stream))
     if check:
         _check(st, "q4gemv_run")
+    return st
+
+
+def q4gemv_fused_run(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M=None, N=None, K=None, group=32,
+                     epilogue=Q4_EPILOGUE_NONE, stream=None, check=True) -> int:
+    M, N, K = _mnk_q4(codes, x, M, N, K)
+    st = lib().q4gemv_fused_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(x), _addr(gamma),
+                                float(eps), _addr(y), M, N, K, int(group), int(epilogue), _stream(stream))
+    if check:
+        _check(st, "q4gemv_fused_run")
     return st
 
 

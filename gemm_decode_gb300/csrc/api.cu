@@ -139,6 +139,27 @@ int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_o
                          static_cast<cudaStream_t>(stream));
 }
 
+int q4gemv_fused_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const float *x,
+                     const float *gamma, float eps, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
+                     int32_t epilogue, void *stream) {
+    int st = check_shape(M, N, K, group);
+    if (st != Q4_OK) return st;
+    if (epilogue != Q4_EPILOGUE_NONE && epilogue != Q4_EPILOGUE_SWIGLU) return Q4_ERR_INVALID_ARG;
+    if (epilogue == Q4_EPILOGUE_SWIGLU && N % 2 != 0) return Q4_ERR_INVALID_ARG;
+    if (gamma != nullptr && !(eps >= 0.0f && eps <= 3.0e38f)) return Q4_ERR_INVALID_ARG;   // NaN fails too
+    if (M == 0 || N == 0) return Q4_OK;
+    if (M > 16) return Q4_ERR_UNSUPPORTED;
+    if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
+    if (x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 4) || (gamma != nullptr && !aligned(gamma, 16))) return Q4_ERR_MISALIGNED;
+    if (gamma == nullptr && epilogue == Q4_EPILOGUE_NONE)
+        return q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M, N, K, group, stream);
+    return launch_q4gemv_fused(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
+                               static_cast<const uint8_t *>(zeros_u4_or_null), x, gamma, eps,
+                               epilogue == Q4_EPILOGUE_SWIGLU ? 1 : 0, y, M, N, static_cast<int>(K), group,
+                               static_cast<cudaStream_t>(stream));
+}
+
 int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const void *a_bf16,
                float *c, int32_t M, int64_t N, int64_t K, int32_t group, void *stream) {
     int st = check_shape(M, N, K, group);

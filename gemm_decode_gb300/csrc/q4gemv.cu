@@ -13,6 +13,13 @@ extern template int launch_q4gemv_mt<2>(const GemvPlan &, const GemvArgs &, cuda
 extern template int launch_q4gemv_mt<4>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 extern template int launch_q4gemv_mt<8>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 extern template int launch_q4gemv_mt<16>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+template <int MT>
+int launch_q4gemv_fused_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
+extern template int launch_q4gemv_fused_mt<1>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_fused_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_fused_mt<4>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_fused_mt<8>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q4gemv_fused_mt<16>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 
 static int rows_per_cta(int MT, int L) {
     const int R = (MT <= 2) ? 2 : 1;
@@ -104,6 +111,9 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
     a.zrow = (a.nb + 1) / 2;
     a.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
     a.CS = p.CS;
+    a.gamma = nullptr;
+    a.eps = 0.0f;
+    a.swiglu = 0;
     switch (p.MT) {
         case 1: return launch_q4gemv_mt<1>(p, a, stream);
         case 2: return launch_q4gemv_mt<2>(p, a, stream);
@@ -112,6 +122,67 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
         case 16: return launch_q4gemv_mt<16>(p, a, stream);
         default: return Q4_ERR_UNSUPPORTED;
     }
+}
+
+// The fused variant (q4gemv_fused_run): the streamed kernel for M = 1 where it applies,
+// else the general kernel's fused instance (16 lanes per row, no K split) over tiles of
+// rows of x as large as the shared memory holds (x of every row of the tile for all of
+// K, plus the RMSNorm sums), one launch per tile.
+int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                        const float *gamma, float eps, int swiglu, float *y, int M, int64_t N, int K, int group,
+                        cudaStream_t stream) {
+    if (stream_applies(M, N, K, group, codes, scales, zeros)) {
+        const int st = launch_q4gemv_stream_fused(codes, scales, zeros, x, gamma, eps, swiglu, y, N, K, group, stream);
+        if (st != Q4_ERR_UNSUPPORTED) return st;   // (the fused carve-up is 128 bytes larger)
+    }
+    const int C = K / 32;
+    const size_t budget = static_cast<size_t>(device_info().smem_optin) - 1024;
+    auto smem_for = [&](int mt) {
+        return static_cast<size_t>(mt) * C * kChunkFloats * sizeof(float) +
+               static_cast<size_t>(kGemvWarps) * mt * sizeof(float);
+    };
+    int MT = 1;
+    while (MT < M && MT < 16) MT <<= 1;
+    while (MT > 1 && smem_for(MT) > budget) MT >>= 1;
+    if (smem_for(MT) > budget) return Q4_ERR_UNSUPPORTED;
+    GemvPlan p;
+    p.MT = MT;
+    p.L = 16;
+    p.S = 1;
+    p.CS = C;
+    p.asym = zeros != nullptr;
+    p.smem = smem_for(MT);
+    p.row_blocks = static_cast<int>((N + rows_per_cta(MT, 16) - 1) / rows_per_cta(MT, 16));
+    const int64_t ycols = swiglu ? N / 2 : N;
+    for (int m0 = 0; m0 < M; m0 += MT) {
+        GemvArgs a;
+        a.codes = codes;
+        a.scales = scales;
+        a.zeros = zeros;
+        a.x = x + static_cast<int64_t>(m0) * K;
+        a.y = y + static_cast<int64_t>(m0) * ycols;
+        a.M = M - m0 < MT ? M - m0 : MT;
+        a.N = static_cast<int>(N);
+        a.K = K;
+        a.C = C;
+        a.nb = K / group;
+        a.zrow = (a.nb + 1) / 2;
+        a.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
+        a.CS = C;
+        a.gamma = gamma;
+        a.eps = eps;
+        a.swiglu = swiglu;
+        int st = Q4_ERR_UNSUPPORTED;
+        switch (MT) {
+            case 1: st = launch_q4gemv_fused_mt<1>(p, a, stream); break;
+            case 2: st = launch_q4gemv_fused_mt<2>(p, a, stream); break;
+            case 4: st = launch_q4gemv_fused_mt<4>(p, a, stream); break;
+            case 8: st = launch_q4gemv_fused_mt<8>(p, a, stream); break;
+            case 16: st = launch_q4gemv_fused_mt<16>(p, a, stream); break;
+        }
+        if (st != Q4_OK) return st;
+    }
+    return Q4_OK;
 }
 
 }  // namespace q4

@@ -59,6 +59,11 @@ struct GemvArgs {
     int zrow;    // zero-point bytes per row, ceil(nb / 2)
     int gshift;  // log2(g / 32): chunk index >> gshift = group index
     int CS;      // chunks per split
+    // fused variant only: gamma[K] (non-null: RMSNorm prologue, eps); swiglu != 0:
+    // rows 2i / 2i+1 are a gate / up pair and y[m][i] = silu(gate) * up (y has N / 2 columns)
+    const float *gamma;
+    float eps;
+    int swiglu;
 };
 
 template <int MT, int L>
@@ -69,9 +74,14 @@ struct GemvShape {
     static constexpr int ROWS_PER_CTA = ROWS_PER_WARP * kGemvWarps;
 };
 
-template <int MT, int L, bool ASYM, bool SPLIT>
+// FUSED (unsplit instances only): x is staged multiplied by a.gamma and every output
+// multiplied by 1 / sqrt(mean(x^2) + eps) when a.gamma is set (the RMSNorm prologue),
+// and with a.swiglu the gate / up row pairs (slots 2s, 2s + 1: lanes L apart) leave
+// silu(gate) * up.
+template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false>
 __global__ void __launch_bounds__(kGemvThreads)
 q4gemv_kernel(const GemvArgs a) {
+    static_assert(!(FUSED && SPLIT), "the fused variant is unsplit");
     using S = GemvShape<MT, L>;
     constexpr int R = S::R;
     constexpr int SLOTS = S::SLOTS;
@@ -96,15 +106,38 @@ q4gemv_kernel(const GemvArgs a) {
             const int cl = rem >> 3;
             const int f = rem & 7;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (m < a.M && cl < nchunks)
+            if (m < a.M && cl < nchunks) {
                 v = *reinterpret_cast<const float4 *>(a.x + static_cast<int64_t>(m) * a.K +
                                                       static_cast<int64_t>(c_begin + cl) * 32 + f * 4);
+                if (FUSED && a.gamma != nullptr) {
+                    const float4 gv = *reinterpret_cast<const float4 *>(a.gamma + static_cast<int64_t>(c_begin + cl) * 32 + f * 4);
+                    v.x *= gv.x; v.y *= gv.y; v.z *= gv.z; v.w *= gv.w;
+                }
+            }
             if (f & 1) {  // positions 4..7 of a word
                 v.x *= 0x1p-16f; v.y *= 0x1p-8f; v.z *= 0x1p-12f; v.w *= 0x1p-16f;
             } else {      // positions 0..3
                 v.y *= 0x1p-4f; v.z *= 0x1p-8f; v.w *= 0x1p-12f;
             }
             *reinterpret_cast<float4 *>(xs + (m * a.CS + cl) * kChunkFloats + f * 4) = v;
+        }
+    }
+    // (fused RMSNorm) per-warp sums of x^2 of every row of x, after the staged tile
+    [[maybe_unused]] float *nrm = smem + MT * a.CS * kChunkFloats;   // [kGemvWarps][MT]
+    if constexpr (FUSED) {
+        if (a.gamma != nullptr) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                float t = 0.f;
+                if (m < a.M)
+                    for (int k = tid; k < a.K; k += kGemvThreads) {
+                        const float v = a.x[static_cast<int64_t>(m) * a.K + k];
+                        t = fmaf(v, v, t);
+                    }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                if ((tid & 31) == 0) nrm[(tid >> 5) * MT + m] = t;
+            }
         }
     }
     __syncthreads();
@@ -207,7 +240,33 @@ q4gemv_kernel(const GemvArgs a) {
             for (int m = 0; m < MT; ++m)
                 acc[r][m] += __shfl_xor_sync(0xffffffffu, acc[r][m], off);
 
-    if constexpr (!SPLIT) {
+    if constexpr (FUSED) {
+        float rn[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            rn[m] = 1.f;
+            if (a.gamma != nullptr) {
+                float t = 0.f;
+                for (int w = 0; w < kGemvWarps; ++w) t += nrm[w * MT + m];
+                rn[m] = rsqrtf(t / static_cast<float>(a.K) + a.eps);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                const float v = acc[r][m] * rn[m];
+                const int64_t n = row0 + r * SLOTS;
+                const bool mine = ((r * MT + m) % L) == j && rvalid[r] && m < a.M;
+                if (a.swiglu) {
+                    const float up = __shfl_xor_sync(0xffffffffu, v, L);   // row n + 1: the next slot
+                    if (mine && (n & 1) == 0)
+                        a.y[static_cast<int64_t>(m) * (a.N / 2) + (n >> 1)] = v / (1.0f + expf(-v)) * up;
+                } else if (mine) {
+                    a.y[static_cast<int64_t>(m) * a.N + n] = v;
+                }
+            }
+    } else if constexpr (!SPLIT) {
 #pragma unroll
         for (int r = 0; r < R; ++r)
 #pragma unroll

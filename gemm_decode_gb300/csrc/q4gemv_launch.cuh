@@ -7,9 +7,9 @@
 
 namespace q4 {
 
-template <int MT, int L, bool ASYM, bool SPLIT>
+template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false>
 static int launch_gemv_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t stream) {
-    auto kern = q4gemv_kernel<MT, L, ASYM, SPLIT>;
+    auto kern = q4gemv_kernel<MT, L, ASYM, SPLIT, FUSED>;
     // Opt into the large shared-memory carve-out once per device.
     static bool configured[64] = {};
     int dev = 0;
@@ -64,6 +64,13 @@ int launch_q4gemv_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s) {
         case 32: return launch_gemv_l<MT, 32>(p, a, s);
         default: return Q4_ERR_UNSUPPORTED;
     }
+}
+
+// The fused variant: lanes per row 16 (gate / up pairs in neighbouring slots), no split.
+template <int MT>
+int launch_q4gemv_fused_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s) {
+    return p.asym ? launch_gemv_one<MT, 16, true, false, true>(p, a, s)
+                  : launch_gemv_one<MT, 16, false, false, true>(p, a, s);
 }
 
 }  // namespace q4

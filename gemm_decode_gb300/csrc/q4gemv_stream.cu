@@ -44,11 +44,11 @@ static unsigned int *stream_status_word() {
     return addr[dev];
 }
 
-int launch_stream_k896(const StreamArgs &a, int group, bool asym, cudaStream_t s);
-int launch_stream_k2048(const StreamArgs &a, int group, bool asym, cudaStream_t s);
-int launch_stream_k4096(const StreamArgs &a, int group, bool asym, cudaStream_t s);
-int launch_stream_k8192(const StreamArgs &a, int group, bool asym, cudaStream_t s);
-int launch_stream_k16384(const StreamArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_k896(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
+int launch_stream_k2048(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
+int launch_stream_k4096(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
+int launch_stream_k8192(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
+int launch_stream_k16384(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
 
 // ------------------------------------------------------------------ host side
 
@@ -91,8 +91,9 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
 static unsigned long long g_stream_timeout_ns = 1000ull * 1000 * 1000;
 void set_stream_wait_timeout_ns(unsigned long long ns) { g_stream_timeout_ns = ns; }
 
-int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
-                         float *y, int64_t N, int K, int group, cudaStream_t stream) {
+static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                             const float *gamma, float eps, int swiglu, bool fused, float *y, int64_t N, int K,
+                             int group, cudaStream_t stream) {
     const bool asym = zeros != nullptr;
     const int rg = stream_rg(K);
     if (rg == 0) return Q4_ERR_UNSUPPORTED;
@@ -107,20 +108,37 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
     a.timeout_ns = g_stream_timeout_ns;
     a.status = stream_status_word();
     a.bounds = bounds_counter();
+    a.gamma = gamma;
+    a.eps = eps;
+    a.swiglu = swiglu;
     if (a.status == nullptr) return Q4_ERR_CUDA;
     const int u = stream_u(K);
-    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym, fused);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
     switch (K) {
-        case 896: return launch_stream_k896(a, group, asym, stream);
-        case 2048: return launch_stream_k2048(a, group, asym, stream);
-        case 4096: return launch_stream_k4096(a, group, asym, stream);
-        case 8192: return launch_stream_k8192(a, group, asym, stream);
-        case 16384: return launch_stream_k16384(a, group, asym, stream);
+        case 896: return launch_stream_k896(a, group, asym, fused, stream);
+        case 2048: return launch_stream_k2048(a, group, asym, fused, stream);
+        case 4096: return launch_stream_k4096(a, group, asym, fused, stream);
+        case 8192: return launch_stream_k8192(a, group, asym, fused, stream);
+        case 16384: return launch_stream_k16384(a, group, asym, fused, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
+            if (fused)
+                return asym ? launch_stream<0, 0, 0, 8, true, true>(a, stream)
+                            : launch_stream<0, 0, 0, 8, false, true>(a, stream);
             return asym ? launch_stream<0, 0, 0, 8, true>(a, stream) : launch_stream<0, 0, 0, 8, false>(a, stream);
     }
+}
+
+int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                         float *y, int64_t N, int K, int group, cudaStream_t stream) {
+    return launch_stream_any(codes, scales, zeros, x, nullptr, 0.0f, 0, false, y, N, K, group, stream);
+}
+
+int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                               const float *gamma, float eps, int swiglu, float *y, int64_t N, int K, int group,
+                               cudaStream_t stream) {
+    return launch_stream_any(codes, scales, zeros, x, gamma, eps, swiglu, true, y, N, K, group, stream);
 }
 
 int read_and_clear_stream_status(unsigned int *v) {

@@ -24,7 +24,7 @@ struct StreamGeo {
     int RED_LD;   // floats per row of a partial-sum buffer
     int RED_B;    // bytes of one partial-sum buffer
     int D;        // ring slots
-    int OFF_RED, OFF_RING, OFF_BAR, OFF_FLAG, SMEM;
+    int OFF_RED, OFF_RING, OFF_BAR, OFF_FLAG, OFF_NORM, SMEM;
 };
 
 constexpr int kStreamNRed = 2;    // partial-sum buffers
@@ -38,7 +38,10 @@ __host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 12
 // SM), 8 otherwise.  Rows that span whole warps (K % 1024 == 0) need a power of two.
 __host__ __device__ constexpr int stream_u(int K) { return K == 896 ? 6 : 8; }
 
-__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym) {
+// fused: the fused-variant kernels also keep their RMSNorm sums (one float per consumer
+// warp) in 128 bytes after the abort flag.
+__host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym,
+                                                        bool fused = false) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
@@ -59,11 +62,13 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
     g.RED_B = g.ROWS * g.RED_LD * 4;
     g.D = D;
     // shared memory: x planes | partial sums [kStreamNRed] | ring [D] | barriers | abort flag
+    // | (fused) RMSNorm sums
     g.OFF_RED = stream_round128(g.C * 28 * 4);
     g.OFF_RING = stream_round128(g.OFF_RED + kStreamNRed * g.RED_B);
     g.OFF_BAR = g.OFF_RING + D * g.SLOT_B;
     g.OFF_FLAG = g.OFF_BAR + 8 * (2 * D + 2 * kStreamNRed);
-    g.SMEM = g.OFF_FLAG + 16;
+    g.OFF_NORM = g.OFF_FLAG + 16;
+    g.SMEM = g.OFF_NORM + (fused ? 128 : 0);
     return g;
 }
 
@@ -87,6 +92,11 @@ struct StreamArgs {
     unsigned long long timeout_ns;   // bound on every mbarrier wait
     unsigned int *status;            // device status word, set to 1 when a wait expires
     unsigned int *bounds;            // out-of-range access counter (bounds-checking builds)
+    // fused variants only: gamma[K] (non-null: RMSNorm prologue, eps), swiglu != 0:
+    // rows 2i / 2i+1 are a gate / up pair and y[i] = silu(gate) * up
+    const float *gamma;
+    float eps;
+    int swiglu;
     StreamGeo geo;                   // used when the instance does not fix K and g
 };
 
@@ -96,6 +106,10 @@ struct StreamArgs {
 bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const void *scales, const void *zeros);
 int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                          float *y, int64_t N, int K, int group, cudaStream_t stream);
+// The fused variant (q4gemv_fused_run): gamma may be null (no RMSNorm), swiglu 0 or 1.
+int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                               const float *gamma, float eps, int swiglu, float *y, int64_t N, int K, int group,
+                               cudaStream_t stream);
 void set_stream_wait_timeout_ns(unsigned long long ns);
 int read_and_clear_stream_status(unsigned int *v);
 

@@ -16,10 +16,11 @@ namespace {
 
 // The geometry an instance works with: compile-time when the instance fixes K, g
 // and RG (the tuned decode shapes), else the launcher's.
-template <int KC, int GC, int RGC, int UC, bool ASYM>
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
-        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM), ASYM);
+        constexpr StreamGeo g =
+            make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM), ASYM, FUSED);
         return g;
     } else {
         return rt;
@@ -29,13 +30,18 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 }  // namespace
 
 // UC: rows per consumer thread and block (compile-time in every instance; the host
-// geometry carries the same value).
-template <int KC, int GC, int RGC, int UC, bool ASYM>
-__global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
+// geometry carries the same value).  FUSED: the fused variant (q4gemv_fused_run):
+// x is multiplied elementwise by a.gamma while it is encoded and every output by
+// 1 / sqrt(mean(x^2) + eps) (the RMSNorm prologue, when a.gamma is set), and with
+// a.swiglu the gate / up row pairs leave silu(gate) * up.
+// (The fused K = 896 instance is held to three CTAs per SM, 80 registers, like the
+// plain one: its two extra registers would otherwise cost a third of the warps.)
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED>
+__global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, (FUSED && KC == 896) ? 3 : 1)
 q4gemv_stream_kernel(const StreamArgs a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
-    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM>(a.geo);
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, FUSED>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -143,14 +149,36 @@ q4gemv_stream_kernel(const StreamArgs a) {
     const int r = tid / C, c = tid - r * C;
     // encode x into planes (four consumer threads per chunk), then a consumer-only barrier
     uint32_t *planes = reinterpret_cast<uint32_t *>(smem);
+    [[maybe_unused]] float ssq = 0.0f;   // (fused RMSNorm) this thread's sum of x^2
     for (int base = 0; base < C; base += G.TC / 4) {
         const int i = base + (tid >> 2);
         const bool in_range = i < C;
         const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-        encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range, planes + (in_range ? i : 0) * kPlaneWords,
-                      tid & 3);
+        if (FUSED && a.gamma != nullptr)
+            encode_chunk4_gamma(a.x + (in_range ? i : 0) * 32, a.gamma + (in_range ? i : 0) * 32, in_range && x_ok,
+                                in_range, planes + (in_range ? i : 0) * kPlaneWords, tid & 3, ssq);
+        else
+            encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+                          planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
+    }
+    if constexpr (FUSED) {
+        if (a.gamma != nullptr) {   // per-warp sums of x^2 -> shared memory
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            if (lane == 0 && ib(warp < 32)) sts_f32(sbase + G.OFF_NORM + 4 * warp, ssq);
+        }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
+    // (fused RMSNorm) the row's 1 / sqrt(mean(x^2) + eps), the warp sums added in order
+    [[maybe_unused]] float rnorm = 1.0f;
+    if constexpr (FUSED) {
+        if (a.gamma != nullptr) {
+            float t = 0.0f;
+            for (int w = 0; w < G.NWC; ++w)
+                if (ib(w < 32)) t += lds_f32(sbase + G.OFF_NORM + 4 * w);
+            rnorm = rsqrtf(t / static_cast<float>(C * 32) + a.eps);
+        }
+    }
     Planes P;
     {
         const uint32_t pa = s_planes + c * kPlaneWords * 4;
@@ -200,6 +228,16 @@ q4gemv_stream_kernel(const StreamArgs a) {
                     if (ib(rho * G.RED_LD + p < G.ROWS * G.RED_LD)) acc += lds_f32(src + (rho * G.RED_LD + p) * 4);
             }
             for (int o = ql >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if constexpr (FUSED) {
+                acc *= rnorm;
+                if (a.swiglu) {
+                    // row rho + 1 (the up row of the pair) sits ql lanes further on
+                    const float up = __shfl_xor_sync(0xffffffffu, acc, ql);
+                    if (mine && q == 0 && (rho & 1) == 0 && row0 + rho + 1 < a.N)
+                        a.y[(row0 + rho) >> 1] = acc / (1.0f + expf(-acc)) * up;
+                    continue;
+                }
+            }
             if (mine && q == 0 && row0 + rho < a.N) a.y[row0 + rho] = acc;
         }
     };
@@ -285,7 +323,8 @@ q4gemv_stream_kernel(const StreamArgs a) {
         if (KC == 0 || G.WRED) {
             if (warp != (nbk - 1) % G.NWC) hi = 0;
         } else {
-            const int rpw = (G.ROWS + G.NWC - 1) / G.NWC;
+            int rpw = (G.ROWS + G.NWC - 1) / G.NWC;
+            if (FUSED && a.swiglu) rpw = (rpw + 1) & ~1;   // gate / up pairs stay in one warp
             lo = warp * rpw < G.ROWS ? warp * rpw : G.ROWS;
             hi = lo + rpw < G.ROWS ? lo + rpw : G.ROWS;
             while (ql * 2 * rpw <= 32 && ql < G.PARTS) ql *= 2;
@@ -300,9 +339,9 @@ q4gemv_stream_kernel(const StreamArgs a) {
     }
 }
 
-template <int KC, int GC, int RGC, int UC, bool ASYM>
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED = false>
 int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
-    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM>;
+    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM, FUSED>;
     const StreamGeo &g = a0.geo;
     const int T = g.TC + 32;
     static int configured[64] = {};   // largest dynamic shared memory set so far, per device
@@ -344,17 +383,23 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
 }
 
 
-// One translation unit per K instantiates the compile-time geometries of that K.
+template <int KV, int GV, int RGV, bool FUSED>
+int launch_stream_kg(const StreamArgs &a, bool asym, cudaStream_t s) {
+    constexpr int UV = stream_u(KV);
+    return asym ? launch_stream<KV, GV, RGV, UV, true, FUSED>(a, s) : launch_stream<KV, GV, RGV, UV, false, FUSED>(a, s);
+}
+
+// One translation unit per K instantiates the compile-time geometries of that K (plain
+// and fused).
 #define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
-    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, cudaStream_t s) {              \
-        constexpr int UV = stream_u(KV);                                                              \
+    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s) {  \
         switch (group) {                                                                              \
-            case 32: return asym ? launch_stream<KV, 32, RGV, UV, true>(a, s)                         \
-                                 : launch_stream<KV, 32, RGV, UV, false>(a, s);                       \
-            case 64: return asym ? launch_stream<KV, 64, RGV, UV, true>(a, s)                         \
-                                 : launch_stream<KV, 64, RGV, UV, false>(a, s);                       \
-            case 128: return asym ? launch_stream<KV, 128, RGV, UV, true>(a, s)                       \
-                                  : launch_stream<KV, 128, RGV, UV, false>(a, s);                     \
+            case 32: return fused ? launch_stream_kg<KV, 32, RGV, true>(a, asym, s)                    \
+                                  : launch_stream_kg<KV, 32, RGV, false>(a, asym, s);                  \
+            case 64: return fused ? launch_stream_kg<KV, 64, RGV, true>(a, asym, s)                    \
+                                  : launch_stream_kg<KV, 64, RGV, false>(a, asym, s);                  \
+            case 128: return fused ? launch_stream_kg<KV, 128, RGV, true>(a, asym, s)                  \
+                                   : launch_stream_kg<KV, 128, RGV, false>(a, asym, s);                \
             default: return Q4_ERR_UNSUPPORTED;                                                       \
         }                                                                                             \
     }

@@ -45,6 +45,8 @@ __device__ __forceinline__ void cp_wait() {
 // as sum of (byte0 + 256 byte1), plane 2), word 27 the chunk scale 2^(E-22).
 // `valid` false encodes zeros; `store` false skips the stores (the shuffles
 // still run: all lanes take part).
+__device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, uint32_t *pw, int q);
+
 __device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool store, uint32_t *pw, int q) {
     float v[8];
     if (valid) {
@@ -55,6 +57,34 @@ __device__ __forceinline__ void encode_chunk4(const float *xc, bool valid, bool 
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = 0.0f;
     }
+    encode_values8(v, store, pw, q);
+}
+
+// The same for the fused RMSNorm prologue: encodes x[k] * gamma[k] (gc: the chunk's
+// 32 gamma values) and adds this thread's sum of x[k]^2 to ssq.
+__device__ __forceinline__ void encode_chunk4_gamma(const float *xc, const float *gc, bool valid, bool store,
+                                                    uint32_t *pw, int q, float &ssq) {
+    float v[8];
+    if (valid) {
+        const float4 a = reinterpret_cast<const float4 *>(xc)[2 * q];
+        const float4 b = reinterpret_cast<const float4 *>(xc)[2 * q + 1];
+        const float4 ga = reinterpret_cast<const float4 *>(gc)[2 * q];
+        const float4 gb = reinterpret_cast<const float4 *>(gc)[2 * q + 1];
+        const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            ssq = fmaf(xv[i], xv[i], ssq);
+            v[i] = xv[i] * gv[i];
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    encode_values8(v, store, pw, q);
+}
+
+__device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, uint32_t *pw, int q) {
     float mx = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(v[i]));

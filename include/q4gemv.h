@@ -79,15 +79,44 @@ typedef struct {
  * K % g != 0. */
 Q4_API int q4gemv_pack_info(int64_t N, int64_t K, int32_t group, q4gemv_pack_info_t *out);
 
-/* Decode-time int4 GEMV on CUDA cores, 1 <= M <= 16 (M > 16: Q4_ERR_UNSUPPORTED).
+/* Decode-time int4 GEMV, 1 <= M <= 16 (M > 16: Q4_ERR_UNSUPPORTED):
+ * y[m][n] = sum_k (q[n][k] - z[n][k/g]) * s[n][k/g] * x[m][k]
+ * (gerbil GPU-engine kernel reference, "3. MatMulInt4": "Computes", "Dequantization").
  *   codes, scales_f16, zeros_u4_or_null : device, layout above
- *   x : device float [M][K];  y : device float [M][N] (written, not accumulated)
- * Kernel: codes streamed with 128-bit loads, exact in-register nibble decode, x held in
- * shared memory, f32 accumulation, warp-shuffle reduction, split-K over a thread-block
- * cluster (distributed shared memory) for long K / few rows. */
+ *   x : device float [M][K], 16-byte aligned;  y : device float [M][N] (written, not
+ *   accumulated)
+ * The library picks the kernel by shape: a TMA-streamed dp4a kernel for M = 1 on long
+ * matrices, the tcgen05 tensor-core GEMV for 3 <= M <= 16 on large ones (K split over a
+ * thread-block cluster when tiles are few), a register-resident dp4a kernel for M <= 2,
+ * and a general CUDA-core kernel (split-K over a cluster for long K / few rows) otherwise.
+ * Asynchronous on `stream`; allocates nothing. */
 Q4_API int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
                const float *x, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
                void *stream);
+
+/* Epilogues of q4gemv_fused_run. */
+#define Q4_EPILOGUE_NONE 0
+#define Q4_EPILOGUE_SWIGLU 1
+
+/* The decode GEMV with its prologue and epilogue fused in (gerbil GPU-engine kernel
+ * reference: "4. RMSNorm" -- its optimisation notes suggest fusing RMSNorm into the
+ * following MatMul -- and "9. SiLU" -- fusing the SwiGLU combine silu(gate) * up):
+ *   gamma : device float [K], 16-byte aligned, or NULL.  Non-NULL: the GEMV's input is
+ *           RMSNorm(x)[m][k] = x[m][k] / sqrt(mean_k x[m][k]^2 + eps) * gamma[k]
+ *           (eps >= 0; computed as (W . (x * gamma)) / sqrt(...) per row).
+ *   epilogue : Q4_EPILOGUE_NONE: y[M][N] as q4gemv_run.
+ *              Q4_EPILOGUE_SWIGLU: N even and weight rows 2i / 2i+1 hold the gate / up
+ *              projections of output i (interleaved); y[M][N/2] with
+ *              y[m][i] = silu(g) * u, silu(v) = v / (1 + exp(-v)).
+ * Other arguments as q4gemv_run.  With gamma NULL and no epilogue it is q4gemv_run.
+ * Kernels: the streamed kernel for M = 1 where q4gemv_run would use it (same speed),
+ * else a general CUDA-core kernel without K split, launched once per tile of rows of x
+ * whose activations fit in shared memory.  Q4_ERR_INVALID_ARG for an unknown
+ * epilogue, odd N with SwiGLU, or a negative or non-finite eps; Q4_ERR_MISALIGNED for
+ * an unaligned gamma. */
+Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                     const float *x, const float *gamma, float eps, float *y, int32_t M, int64_t N,
+                     int64_t K, int32_t group, int32_t epilogue, void *stream);
 
 /* Prefill-shaped int4 matmul on the tensor cores (tcgen05, bf16 operands, f32
  * accumulate in tensor memory), any M >= 1 (tiles of 128 rows; a partial tile is

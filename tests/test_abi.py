@@ -98,6 +98,26 @@ def test_gemv_argument_checks(L):
     del ok_shape
 
 
+def test_fused_gemv_argument_checks(L):
+    r = L.q4gemv_fused_run
+    NONE, SWIGLU = q4.Q4_EPILOGUE_NONE, q4.Q4_EPILOGUE_SWIGLU
+    # unknown epilogue, odd N with SwiGLU, a negative or NaN eps with gamma
+    assert r(A, A, None, A, A, 1e-6, A, 1, 64, 64, 32, 7, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, None, 0.0, A, 1, 63, 64, 32, SWIGLU, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, -1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, float("nan"), A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_INVALID_ARG
+    # the shape checks of q4gemv_run
+    assert r(A, A, None, A, A, 1e-6, A, 1, 64, 96, 64, NONE, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, 1e-6, A, 17, 64, 64, 32, NONE, None) == q4.Q4_ERR_UNSUPPORTED
+    # empty problems are no-ops
+    assert r(None, None, None, None, None, 1e-6, None, 0, 64, 64, 32, SWIGLU, None) == q4.Q4_OK
+    # null and misaligned pointers (gamma: 16-byte aligned)
+    assert r(A, A, None, None, A, 1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A, 1e-6, None, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, None, A, A + 4, 1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_MISALIGNED
+    assert r(A, A, None, A + 4, A, 1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_MISALIGNED
+
+
 def test_gemm_and_control_argument_checks(L):
     g = L.q4gemm_run
     assert g(A, A, None, A, A, 1, 64, 100, 32, None) == q4.Q4_ERR_INVALID_ARG
