@@ -125,7 +125,8 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
 }
 
 // The fused variant (q4gemv_fused_run): the streamed kernel for M = 1 where it applies,
-// else the general kernel's fused instance (16 lanes per row, no K split) over tiles of
+// the register-resident kernel's fused instances for other M = 1 shapes it serves
+// without a K split, else the general kernel's fused instance (16 lanes per row, no K split) over tiles of
 // rows of x as large as the shared memory holds (x of every row of the tile for all of
 // K, plus the RMSNorm sums), one launch per tile.
 int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
@@ -134,6 +135,23 @@ int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint
     if (stream_applies(M, N, K, group, codes, scales, zeros)) {
         const int st = launch_q4gemv_stream_fused(codes, scales, zeros, x, gamma, eps, swiglu, y, N, K, group, stream);
         if (st != Q4_ERR_UNSUPPORTED) return st;   // (the fused carve-up is 128 bytes larger)
+    }
+    {   // M = 1 on shorter matrices: the register-resident kernel's fused instances
+        XregPlan xp;
+        XregFusedArgs xa;
+        if (plan_q4gemv_xreg(M, N, K, group, scales, zeros, xp, xa, true)) {
+            xa.codes = codes;
+            xa.scales = scales;
+            xa.zeros = zeros;
+            xa.x = x;
+            xa.y = y;
+            xa.bounds = bounds_counter();
+            xa.gamma = gamma;
+            xa.eps = eps;
+            xa.swiglu = swiglu;
+            const int st = launch_q4gemv_xreg_fused(xp, xa, stream);
+            if (st != Q4_ERR_UNSUPPORTED) return st;
+        }
     }
     const int C = K / 32;
     const size_t budget = static_cast<size_t>(device_info().smem_optin) - 1024;

@@ -34,10 +34,8 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 // x is multiplied elementwise by a.gamma while it is encoded and every output by
 // 1 / sqrt(mean(x^2) + eps) (the RMSNorm prologue, when a.gamma is set), and with
 // a.swiglu the gate / up row pairs leave silu(gate) * up.
-// (The fused K = 896 instance is held to three CTAs per SM, 80 registers, like the
-// plain one: its two extra registers would otherwise cost a third of the warps.)
 template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED>
-__global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, (FUSED && KC == 896) ? 3 : 1)
+__global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgs a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
@@ -165,19 +163,24 @@ q4gemv_stream_kernel(const StreamArgs a) {
         if (a.gamma != nullptr) {   // per-warp sums of x^2 -> shared memory
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-            if (lane == 0 && ib(warp < 32)) sts_f32(sbase + G.OFF_NORM + 4 * warp, ssq);
+            if (lane == 0 && ib(warp < 31)) sts_f32(sbase + G.OFF_NORM + 4 * warp, ssq);
         }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
-    // (fused RMSNorm) the row's 1 / sqrt(mean(x^2) + eps), the warp sums added in order
-    [[maybe_unused]] float rnorm = 1.0f;
+    // (fused RMSNorm) the row's 1 / sqrt(mean(x^2) + eps), the warp sums added in order;
+    // every warp computes the same value and its lane 0 keeps it in word 31 of the norm
+    // area, where the warp's reductions read it (nothing stays live across the loop)
     if constexpr (FUSED) {
+        float rnorm = 1.0f;
         if (a.gamma != nullptr) {
             float t = 0.0f;
             for (int w = 0; w < G.NWC; ++w)
-                if (ib(w < 32)) t += lds_f32(sbase + G.OFF_NORM + 4 * w);
+                if (ib(w < 31)) t += lds_f32(sbase + G.OFF_NORM + 4 * w);
             rnorm = rsqrtf(t / static_cast<float>(C * 32) + a.eps);
         }
+        __syncwarp();   // every lane of the warp has read the sums before lane 0 writes word 31
+        if (lane == 0) sts_f32(sbase + G.OFF_NORM + 4 * 31, rnorm);
+        __syncwarp();
     }
     Planes P;
     {
@@ -229,7 +232,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             }
             for (int o = ql >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if constexpr (FUSED) {
-                acc *= rnorm;
+                acc *= lds_f32(sbase + G.OFF_NORM + 4 * 31);
                 if (a.swiglu) {
                     // row rho + 1 (the up row of the pair) sits ql lanes further on
                     const float up = __shfl_xor_sync(0xffffffffu, acc, ql);

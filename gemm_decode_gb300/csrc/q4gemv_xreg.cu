@@ -30,6 +30,7 @@
 // rounding of the per-chunk and per-row sums.  Codes equal to their zero point
 // contribute exactly 0.
 #include <cooperative_groups.h>
+#include <type_traits>
 
 #include "q4_common.cuh"
 #include "q4gemv_xreg.cuh"
@@ -44,9 +45,16 @@ using namespace xp;
 // Compile-time geometry: KC = chunks per row and G = group size when known at
 // compile time (0 = read from the arguments); U rows groups per ring iteration
 // and D ring slots.
-template <int MT, bool ASYM, int CTP, int RG, int KC, int G, int U, int D>
+// FUSED (M = 1, no K split): x is encoded multiplied by a.gamma and every output
+// multiplied by 1 / sqrt(mean(x^2) + eps) when a.gamma is set (the RMSNorm prologue);
+// with a.swiglu the gate / up row pairs leave silu(gate) * up.
+template <bool FUSED>
+using XregArgsOf = std::conditional_t<FUSED, XregFusedArgs, XregArgs>;
+
+template <int MT, bool ASYM, int CTP, int RG, int KC, int G, int U, int D, bool FUSED = false>
 __global__ void __launch_bounds__(CTP * RG)
-q4gemv_xreg_kernel(const XregArgs a) {
+q4gemv_xreg_kernel(const XregArgsOf<FUSED> a) {
+    static_assert(!FUSED || MT == 1, "the fused variant serves one row of x");
     constexpr int T = CTP * RG;
     constexpr bool WARPRED = CTP >= 32;
     constexpr int RED_LD = WARPRED ? CTP / 32 : CTP + 1;
@@ -154,6 +162,7 @@ q4gemv_xreg_kernel(const XregArgs a) {
 
     // ---- encode this CTA's x slice into planes (four threads per chunk and row of x) ----
     // (the round count is the same for every thread, so every lane reaches the shuffles)
+    [[maybe_unused]] float ssq = 0.0f;   // (fused RMSNorm) this thread's sum of x^2
     for (int base = 0; base < MT * CTP; base += T / 4) {
         const int i = base + (tid >> 2);
         const bool in_range = i < MT * CTP;
@@ -161,8 +170,25 @@ q4gemv_xreg_kernel(const XregArgs a) {
         const int m = ii / CTP, ci = ii - m * CTP;
         const int cc = split * CT + ci;
         const bool valid = in_range && m < a.M && ci < CT && cc < C;
-        encode_chunk4(a.x + static_cast<int64_t>(valid ? m : 0) * K + (valid ? cc : 0) * 32, valid, in_range,
-                      planes + (m * CTP + ci) * kPlaneWords, tid & 3);
+        bool done = false;
+        if constexpr (FUSED) {
+            if (a.gamma != nullptr) {
+                encode_chunk4_gamma(a.x + static_cast<int64_t>(valid ? m : 0) * K + (valid ? cc : 0) * 32,
+                                    a.gamma + (valid ? cc : 0) * 32, valid, in_range,
+                                    planes + (m * CTP + ci) * kPlaneWords, tid & 3, ssq);
+                done = true;
+            }
+        }
+        if (!done)
+            encode_chunk4(a.x + static_cast<int64_t>(valid ? m : 0) * K + (valid ? cc : 0) * 32, valid, in_range,
+                          planes + (m * CTP + ci) * kPlaneWords, tid & 3);
+    }
+    if constexpr (FUSED) {
+        if (a.gamma != nullptr) {   // per-warp sums of x^2 -> shared memory
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+            if ((tid & 31) == 0) reinterpret_cast<float *>(smem + a.off_norm)[tid >> 5] = ssq;
+        }
     }
     __syncthreads();
     // Load this thread's planes once.  The loads are volatile asm so the compiler
@@ -274,7 +300,40 @@ q4gemv_xreg_kernel(const XregArgs a) {
         const int nrows = nbat * ROWS_IT;
         constexpr int NTERMS = WARPRED ? CTP / 32 : CTP;
         const int64_t first_row = static_cast<int64_t>(g_begin + b0) * ROWS_IT;
-        if (nsplit == 1) {
+        if constexpr (FUSED) {
+            // the row's 1 / sqrt(mean(x^2) + eps) from the warp sums, in order
+            float rn = 1.0f;
+            if (a.gamma != nullptr) {
+                const float *nrm = reinterpret_cast<const float *>(smem + a.off_norm);
+                float t = 0.0f;
+                for (int w = 0; w < T / 32; ++w) t += nrm[w];
+                rn = rsqrtf(t / static_cast<float>(K) + a.eps);
+            }
+            if (a.swiglu) {   // rows 2i, 2i + 1 of the batch (first_row is even)
+                for (int i = tid; i < nrows / 2; i += T) {
+                    const float *sg = red + (2 * i) * RED_LD, *su = red + (2 * i + 1) * RED_LD;
+                    float gv = 0.0f, uv = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < NTERMS; ++q) {
+                        gv += sg[q];
+                        uv += su[q];
+                    }
+                    gv *= rn;
+                    uv *= rn;
+                    const int64_t n = first_row + 2 * i;
+                    if (n + 1 < a.N) a.y[n >> 1] = gv / (1.0f + expf(-gv)) * uv;
+                }
+            } else {
+                for (int i = tid; i < nrows; i += T) {
+                    const float *src = red + i * RED_LD;
+                    float v = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < NTERMS; ++q) v += src[q];
+                    const int64_t n = first_row + i;
+                    if (n < a.N) a.y[n] = v * rn;
+                }
+            }
+        } else if (nsplit == 1) {
             for (int i = tid; i < nrows * MT; i += T) {
                 const float *src = red + i * RED_LD;
                 float v = 0.0f;
@@ -320,9 +379,10 @@ static int rows_per_group(int ctp) {
     return 0;
 }
 
-template <int MT, bool ASYM, int CTP, int RG, int KC = 0, int G = 0, int U = kXregU, int D = kXregD>
-static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
-    auto kern = q4gemv_xreg_kernel<MT, ASYM, CTP, RG, KC, G, U, D>;
+template <int MT, bool ASYM, int CTP, int RG, int KC = 0, int G = 0, int U = kXregU, int D = kXregD,
+          bool FUSED = false>
+static int launch_one(const XregPlan &p, const XregArgsOf<FUSED> &a, cudaStream_t stream) {
+    auto kern = q4gemv_xreg_kernel<MT, ASYM, CTP, RG, KC, G, U, D, FUSED>;
     constexpr int T = CTP * RG;
     static bool configured[64] = {};
     int dev = 0;
@@ -369,7 +429,7 @@ static int launch_one(const XregPlan &p, const XregArgs &a, cudaStream_t stream)
     }
     if (resident < 1) return Q4_ERR_UNSUPPORTED;
     const int nsuper = static_cast<int>((a.N + U * RG - 1) / (U * RG));
-    XregArgs aa = a;
+    XregArgsOf<FUSED> aa = a;
     aa.nsuper = nsuper;
     const int grid_x = resident < nsuper ? resident : nsuper;
     cfg.gridDim = dim3(static_cast<unsigned>(grid_x), static_cast<unsigned>(p.S), 1);
@@ -396,14 +456,32 @@ static int launch_shape(const XregPlan &p, const XregArgs &a, cudaStream_t s) {
     return Q4_ERR_UNSUPPORTED;
 }
 
+template <bool ASYM>
+static int launch_shape_fused(const XregPlan &p, const XregFusedArgs &a, cudaStream_t s) {
+#define Q4_CASE(C, R) \
+    if (a.CTp == C) return launch_one<1, ASYM, C, R, 0, 0, kXregU, kXregD, true>(p, a, s);
+    Q4_XREG_SHAPES(Q4_CASE)
+#undef Q4_CASE
+    return Q4_ERR_UNSUPPORTED;
+}
+
+int launch_q4gemv_xreg_fused(const XregPlan &p, const XregFusedArgs &a, cudaStream_t stream) {
+    if (!p.fused || p.MT != 1 || p.S != 1 || p.special) return Q4_ERR_UNSUPPORTED;
+    XregFusedArgs aa = a;
+    aa.off_norm = p.off_norm;
+    return p.asym ? launch_shape_fused<true>(p, aa, stream) : launch_shape_fused<false>(p, aa, stream);
+}
+
 int launch_q4gemv_xreg(const XregPlan &p, const XregArgs &a, cudaStream_t stream) {
+    if (p.fused) return Q4_ERR_UNSUPPORTED;
     if (p.MT == 1) return p.asym ? launch_shape<1, true>(p, a, stream) : launch_shape<1, false>(p, a, stream);
     if (p.MT == 2) return p.asym ? launch_shape<2, true>(p, a, stream) : launch_shape<2, false>(p, a, stream);
     return Q4_ERR_UNSUPPORTED;
 }
 
 // Shared-memory layout of one instance (must match the carve-up in the kernel).
-static size_t xreg_smem(int MT, int CTp, int RG, int U, int D, int S, bool asym, XregArgs &a) {
+static size_t xreg_smem(int MT, int CTp, int RG, int U, int D, int S, bool asym, XregArgs &a, bool fused,
+                        int *off_norm_out) {
     const int T = CTp * RG;
     const int rows_it = U * RG;
     const bool warpred = CTp >= 32;
@@ -421,14 +499,17 @@ static size_t xreg_smem(int MT, int CTp, int RG, int U, int D, int S, bool asym,
     a.off_red = static_cast<int>(off_red);
     a.off_ring = static_cast<int>(off_ring);
     a.off_ysum = static_cast<int>(off_ysum);
-    return off_ysum + ysum_b;
+    const size_t off_norm = (off_ysum + ysum_b + 15) / 16 * 16;
+    *off_norm_out = static_cast<int>(off_norm);
+    return fused ? off_norm + static_cast<size_t>((T + 31) / 32) * 4 : off_ysum + ysum_b;
 }
 
 // Plan: K-slices S, threads per row CTp, rows per group RG.  Returns false when the
 // shape does not suit this kernel (the caller then uses the general kernel).
 bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, const void *zeros,
-                      XregPlan &p, XregArgs &a) {
+                      XregPlan &p, XregArgs &a, bool fused) {
     if (M < 1 || M > 2) return false;
+    if (fused && M != 1) return false;
     const int C = K / 32;
     const int nb = K / group;
     const int zrow = (nb + 1) / 2;
@@ -440,7 +521,7 @@ bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, co
     const DeviceInfo &d = device_info();
     const int MT = M;
     int S = (C + 255) / 256;
-    if (S > 8) return false;
+    if (S > 8 || (fused && S != 1)) return false;
     const int CT = (C + S - 1) / S;
     const int CTp = CT >= 32 ? (CT + 31) / 32 * 32 : CT;
     const int RG = rows_per_group(CTp);
@@ -449,13 +530,14 @@ bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, co
     if (asym && (static_cast<int64_t>(RG) * zrow) % 4 != 0) return false;
     if ((static_cast<int64_t>(RG) * nb) % 2 != 0) return false;
     // compile-time-geometry instances serve the long-N shapes they were built for
-    const bool special = S == 1 && ((C == 28 && group == 32) || (C == 128 && group == 128)) &&
+    const bool special = !fused && S == 1 && ((C == 28 && group == 32) || (C == 128 && group == 128)) &&
                          N >= 64 * kXregUSpecial * RG;
     const int U = special ? kXregUSpecial : kXregU;
     const int D = special ? kXregDSpecial : kXregD;
     const int T = CTp * RG;
     if (N < 4 * U * RG) return false;
-    const size_t smem = xreg_smem(MT, CTp, RG, U, D, S, asym, a);
+    int off_norm = 0;
+    const size_t smem = xreg_smem(MT, CTp, RG, U, D, S, asym, a, fused, &off_norm);
     if (smem > static_cast<size_t>(d.smem_optin) - 1024) return false;
     p.MT = MT;
     p.S = S;
@@ -465,6 +547,8 @@ bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, co
     p.asym = asym;
     p.warpred = CTp >= 32;
     p.special = special;
+    p.fused = fused;
+    p.off_norm = off_norm;
     a.M = M;
     a.N = static_cast<int>(N);
     a.K = K;

@@ -32,15 +32,30 @@ struct XregArgs {
     unsigned int *bounds;              // out-of-range access counter (bounds-checking builds)
 };
 
+// The fused variant's arguments (M = 1, no K split); the plain kernels keep their own
+// parameter type unchanged.  gamma[K] non-null: RMSNorm prologue with eps; swiglu != 0:
+// rows 2i / 2i+1 are a gate / up pair and y[i] = silu(gate) * up; off_norm: shared-memory
+// offset of the RMSNorm sums (one float per warp).
+struct XregFusedArgs : XregArgs {
+    const float *gamma;
+    float eps;
+    int swiglu;
+    int off_norm;
+};
+
 struct XregPlan {
     int MT, S, threads, grid_x;
     size_t smem;
     bool asym, warpred;
     bool special;   // use the compile-time-geometry instance
+    bool fused;     // the fused variant (q4gemv_fused_run)
+    int off_norm;   // (fused) shared-memory offset of the RMSNorm sums
 };
 
+// fused: plan the fused variant, which serves M = 1 without a K split (false otherwise).
 bool plan_q4gemv_xreg(int M, int64_t N, int K, int group, const void *scales, const void *zeros,
-                      XregPlan &p, XregArgs &a);
+                      XregPlan &p, XregArgs &a, bool fused = false);
 int launch_q4gemv_xreg(const XregPlan &p, const XregArgs &a, cudaStream_t stream);
+int launch_q4gemv_xreg_fused(const XregPlan &p, const XregFusedArgs &a, cudaStream_t stream);
 
 }  // namespace q4

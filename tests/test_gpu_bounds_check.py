@@ -86,3 +86,20 @@ def test_register_resident_kernel(torch, M, N, K, g, symmetric):
     w = synth.q4_weights(M * 3 + N + K, N, K, g, symmetric=symmetric, tag="bounds-xreg")
     x = synth.activations_f32(N + M, M, K)
     run_checked(torch, w, x, f"register-resident M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("N,K,g", [(1152, 896, 32), (896, 4864, 32), (9730, 896, 64), (4098, 14336, 128)])
+def test_fused_kernels(torch, N, K, g):
+    # the fused instances (RMSNorm and SwiGLU): register-resident (the first two) and
+    # streamed (a partial last block; runtime geometry for K = 14336)
+    w = synth.q4_weights(N + 5, N, K, g, tag="bounds-fused")
+    x = synth.activations_f32(N + 6, 1, K)
+    gamma = np.random.default_rng(N).uniform(0.5, 1.5, K).astype(np.float32)
+    y = torch.full((1, N // 2), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q4gemv_fused_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch),
+                        dev(gamma, torch), 1e-6, y, 1, N, K, g, epilogue=q4.Q4_EPILOGUE_SWIGLU)
+    assert q4.q4gemv_bounds_violations() == 0, f"fused N={N} K={K}: out-of-range accesses counted"
+    outs = sorted(set(np.random.default_rng(1).choice(N // 2, size=min(N // 2, 64), replace=False).tolist())
+                  | {0, N // 2 - 1})
+    ref, tol = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-6, g, True, outputs=outs)
+    assert np.all(np.abs(host(y)[:, outs] - ref) <= tol)
