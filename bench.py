@@ -743,8 +743,8 @@ def parse_args(argv=None):
     p.add_argument("--ref-seconds", type=float, default=90.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--controls", type=int, default=1)
-    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_8b", "down_8b", "tc_m16", "tc_lm05_m8",
-                                         "tc_down8b_m8", "f32_lm_head", "gemm_ffn", "gemm_gate"],
+    p.add_argument("--profile", choices=["none", "lm_head", "lm_head_fused", "lm_head_8b", "down_8b", "tc_m16",
+                                         "tc_lm05_m8", "tc_down8b_m8", "f32_lm_head", "gemm_ffn", "gemm_gate"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--sweep", action="store_true",
@@ -801,6 +801,17 @@ def run_profile_case(args):
         y = torch.empty((1, N), dtype=torch.float32, device="cuda")
         for i in range(7):
             q4.f32gemv_run(Ws[i % 2], x, y, 1, N, K)
+    elif args.profile == "lm_head_fused":
+        # the LM head through q4gemv_fused_run with the RMSNorm prologue
+        N, K, g, M = PROFILE_CASES["lm_head"]
+        w = synth.q4_weights(5, N, K, g)
+        reps = [(dev(w.codes), dev(w.scales), dev(w.zeros)) for _ in range(4)]
+        x = dev(synth.activations_f32(5, M, K))
+        gamma = dev(np.ones(K, np.float32))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        for i in range(7):
+            c, sc, z = reps[i % 4]
+            q4.q4gemv_fused_run(c, sc, z, x, gamma, 1e-6, y, M, N, K, g)
     else:
         N, K, g, M = PROFILE_CASES[args.profile]
         w = synth.q4_weights(5, N, K, g)

@@ -44,11 +44,11 @@ static unsigned int *stream_status_word() {
     return addr[dev];
 }
 
-int launch_stream_k896(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
-int launch_stream_k2048(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
-int launch_stream_k4096(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
-int launch_stream_k8192(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
-int launch_stream_k16384(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s);
+int launch_stream_k896(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_k2048(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_k4096(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_k8192(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_k16384(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 
 // ------------------------------------------------------------------ host side
 
@@ -116,16 +116,19 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
     a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym, fused);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
+    // fused instances: 1 = RMSNorm only, 3 = also SwiGLU (the norm stays a runtime choice)
+    const int fuse = fused ? (swiglu ? 3 : 1) : 0;
     switch (K) {
-        case 896: return launch_stream_k896(a, group, asym, fused, stream);
-        case 2048: return launch_stream_k2048(a, group, asym, fused, stream);
-        case 4096: return launch_stream_k4096(a, group, asym, fused, stream);
-        case 8192: return launch_stream_k8192(a, group, asym, fused, stream);
-        case 16384: return launch_stream_k16384(a, group, asym, fused, stream);
+        case 896: return launch_stream_k896(a, group, asym, fuse, stream);
+        case 2048: return launch_stream_k2048(a, group, asym, fuse, stream);
+        case 4096: return launch_stream_k4096(a, group, asym, fuse, stream);
+        case 8192: return launch_stream_k8192(a, group, asym, fuse, stream);
+        case 16384: return launch_stream_k16384(a, group, asym, fuse, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
-            if (fused)
-                return asym ? launch_stream<0, 0, 0, 8, true, true>(a, stream)
-                            : launch_stream<0, 0, 0, 8, false, true>(a, stream);
+            if (fuse == 3)
+                return asym ? launch_stream<0, 0, 0, 8, true, 3>(a, stream) : launch_stream<0, 0, 0, 8, false, 3>(a, stream);
+            if (fuse == 1)
+                return asym ? launch_stream<0, 0, 0, 8, true, 1>(a, stream) : launch_stream<0, 0, 0, 8, false, 1>(a, stream);
             return asym ? launch_stream<0, 0, 0, 8, true>(a, stream) : launch_stream<0, 0, 0, 8, false>(a, stream);
     }
 }

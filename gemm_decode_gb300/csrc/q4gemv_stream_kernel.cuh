@@ -30,16 +30,18 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 }  // namespace
 
 // UC: rows per consumer thread and block (compile-time in every instance; the host
-// geometry carries the same value).  FUSED: the fused variant (q4gemv_fused_run):
-// x is multiplied elementwise by a.gamma while it is encoded and every output by
-// 1 / sqrt(mean(x^2) + eps) (the RMSNorm prologue, when a.gamma is set), and with
-// a.swiglu the gate / up row pairs leave silu(gate) * up.
-template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED>
+// geometry carries the same value).  FUSE (the fused variant, q4gemv_fused_run): bit 0,
+// the RMSNorm prologue when a.gamma is set -- a first pass sums x^2 over the row, then
+// x is encoded as x * gamma / sqrt(mean(x^2) + eps), so the dot products and the
+// reduction are those of the plain kernel; bit 1, the SwiGLU epilogue when a.swiglu is
+// set -- the gate / up row pairs leave silu(gate) * up.
+template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgs a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
-    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, FUSED>(a.geo);
+    constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0;
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, FUSE != 0>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -147,41 +149,55 @@ q4gemv_stream_kernel(const StreamArgs a) {
     const int r = tid / C, c = tid - r * C;
     // encode x into planes (four consumer threads per chunk), then a consumer-only barrier
     uint32_t *planes = reinterpret_cast<uint32_t *>(smem);
-    [[maybe_unused]] float ssq = 0.0f;   // (fused RMSNorm) this thread's sum of x^2
-    for (int base = 0; base < C; base += G.TC / 4) {
-        const int i = base + (tid >> 2);
-        const bool in_range = i < C;
-        const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-        if (FUSED && a.gamma != nullptr)
-            encode_chunk4_gamma(a.x + (in_range ? i : 0) * 32, a.gamma + (in_range ? i : 0) * 32, in_range && x_ok,
-                                in_range, planes + (in_range ? i : 0) * kPlaneWords, tid & 3, ssq);
-        else
-            encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
-                          planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
-    }
-    if constexpr (FUSED) {
-        if (a.gamma != nullptr) {   // per-warp sums of x^2 -> shared memory
+    if constexpr (NORM) {
+        if (a.gamma != nullptr) {
+            // first pass: this thread's x^2 (the elements it encodes), warp sums in shared
+            // memory, a consumer barrier, the row's 1 / sqrt(mean(x^2) + eps)
+            float ssq = 0.0f;
+            for (int base = 0; base < C; base += G.TC / 4) {
+                const int i = base + (tid >> 2);
+                if (i < C && ib((i + 1) * 32 <= C * 32)) {
+                    const float4 *xc = reinterpret_cast<const float4 *>(a.x + i * 32) + 2 * (tid & 3);
+                    const float4 u = xc[0], v = xc[1];
+                    ssq = fmaf(u.x, u.x, fmaf(u.y, u.y, fmaf(u.z, u.z, fmaf(u.w, u.w, ssq))));
+                    ssq = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ssq))));
+                }
+            }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
-            if (lane == 0 && ib(warp < 31)) sts_f32(sbase + G.OFF_NORM + 4 * warp, ssq);
+            if (lane == 0 && ib(warp < 32)) sts_f32(sbase + G.OFF_NORM + 4 * warp, ssq);
+            asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
+            float t = 0.0f;
+            for (int w = 0; w < G.NWC; ++w)
+                if (ib(w < 32)) t += lds_f32(sbase + G.OFF_NORM + 4 * w);
+            const float rnorm = rsqrtf(t / static_cast<float>(C * 32) + a.eps);
+            for (int base = 0; base < C; base += G.TC / 4) {
+                const int i = base + (tid >> 2);
+                const bool in_range = i < C;
+                const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
+                encode_chunk4_gamma_scaled(a.x + (in_range ? i : 0) * 32, a.gamma + (in_range ? i : 0) * 32, rnorm,
+                                           in_range && x_ok, in_range, planes + (in_range ? i : 0) * kPlaneWords,
+                                           tid & 3);
+            }
+        } else {
+            for (int base = 0; base < C; base += G.TC / 4) {
+                const int i = base + (tid >> 2);
+                const bool in_range = i < C;
+                const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
+                encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+                              planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
+            }
+        }
+    } else {
+        for (int base = 0; base < C; base += G.TC / 4) {
+            const int i = base + (tid >> 2);
+            const bool in_range = i < C;
+            const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
+            encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+                          planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
         }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
-    // (fused RMSNorm) the row's 1 / sqrt(mean(x^2) + eps), the warp sums added in order;
-    // every warp computes the same value and its lane 0 keeps it in word 31 of the norm
-    // area, where the warp's reductions read it (nothing stays live across the loop)
-    if constexpr (FUSED) {
-        float rnorm = 1.0f;
-        if (a.gamma != nullptr) {
-            float t = 0.0f;
-            for (int w = 0; w < G.NWC; ++w)
-                if (ib(w < 31)) t += lds_f32(sbase + G.OFF_NORM + 4 * w);
-            rnorm = rsqrtf(t / static_cast<float>(C * 32) + a.eps);
-        }
-        __syncwarp();   // every lane of the warp has read the sums before lane 0 writes word 31
-        if (lane == 0) sts_f32(sbase + G.OFF_NORM + 4 * 31, rnorm);
-        __syncwarp();
-    }
     Planes P;
     {
         const uint32_t pa = s_planes + c * kPlaneWords * 4;
@@ -231,8 +247,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
                     if (ib(rho * G.RED_LD + p < G.ROWS * G.RED_LD)) acc += lds_f32(src + (rho * G.RED_LD + p) * 4);
             }
             for (int o = ql >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if constexpr (FUSED) {
-                acc *= lds_f32(sbase + G.OFF_NORM + 4 * 31);
+            if constexpr (SWIG) {
                 if (a.swiglu) {
                     // row rho + 1 (the up row of the pair) sits ql lanes further on
                     const float up = __shfl_xor_sync(0xffffffffu, acc, ql);
@@ -327,7 +342,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             if (warp != (nbk - 1) % G.NWC) hi = 0;
         } else {
             int rpw = (G.ROWS + G.NWC - 1) / G.NWC;
-            if (FUSED && a.swiglu) rpw = (rpw + 1) & ~1;   // gate / up pairs stay in one warp
+            if (SWIG && a.swiglu) rpw = (rpw + 1) & ~1;   // gate / up pairs stay in one warp
             lo = warp * rpw < G.ROWS ? warp * rpw : G.ROWS;
             hi = lo + rpw < G.ROWS ? lo + rpw : G.ROWS;
             while (ql * 2 * rpw <= 32 && ql < G.PARTS) ql *= 2;
@@ -342,9 +357,9 @@ q4gemv_stream_kernel(const StreamArgs a) {
     }
 }
 
-template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED = false>
+template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE = 0>
 int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
-    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM, FUSED>;
+    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM, FUSE>;
     const StreamGeo &g = a0.geo;
     const int T = g.TC + 32;
     static int configured[64] = {};   // largest dynamic shared memory set so far, per device
@@ -386,23 +401,25 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
 }
 
 
-template <int KV, int GV, int RGV, bool FUSED>
-int launch_stream_kg(const StreamArgs &a, bool asym, cudaStream_t s) {
+template <int KV, int GV, int RGV>
+int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
     constexpr int UV = stream_u(KV);
-    return asym ? launch_stream<KV, GV, RGV, UV, true, FUSED>(a, s) : launch_stream<KV, GV, RGV, UV, false, FUSED>(a, s);
+    switch (fuse) {
+        case 0: return asym ? launch_stream<KV, GV, RGV, UV, true, 0>(a, s) : launch_stream<KV, GV, RGV, UV, false, 0>(a, s);
+        case 1: return asym ? launch_stream<KV, GV, RGV, UV, true, 1>(a, s) : launch_stream<KV, GV, RGV, UV, false, 1>(a, s);
+        case 3: return asym ? launch_stream<KV, GV, RGV, UV, true, 3>(a, s) : launch_stream<KV, GV, RGV, UV, false, 3>(a, s);
+        default: return Q4_ERR_UNSUPPORTED;
+    }
 }
 
-// One translation unit per K instantiates the compile-time geometries of that K (plain
-// and fused).
+// One translation unit per K instantiates the compile-time geometries of that K (plain,
+// RMSNorm, RMSNorm + SwiGLU).
 #define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
-    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, bool fused, cudaStream_t s) {  \
+    int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s) {    \
         switch (group) {                                                                              \
-            case 32: return fused ? launch_stream_kg<KV, 32, RGV, true>(a, asym, s)                    \
-                                  : launch_stream_kg<KV, 32, RGV, false>(a, asym, s);                  \
-            case 64: return fused ? launch_stream_kg<KV, 64, RGV, true>(a, asym, s)                    \
-                                  : launch_stream_kg<KV, 64, RGV, false>(a, asym, s);                  \
-            case 128: return fused ? launch_stream_kg<KV, 128, RGV, true>(a, asym, s)                  \
-                                   : launch_stream_kg<KV, 128, RGV, false>(a, asym, s);                \
+            case 32: return launch_stream_kg<KV, 32, RGV>(a, asym, fuse, s);                          \
+            case 64: return launch_stream_kg<KV, 64, RGV>(a, asym, fuse, s);                          \
+            case 128: return launch_stream_kg<KV, 128, RGV>(a, asym, fuse, s);                        \
             default: return Q4_ERR_UNSUPPORTED;                                                       \
         }                                                                                             \
     }

@@ -84,6 +84,26 @@ __device__ __forceinline__ void encode_chunk4_gamma(const float *xc, const float
     encode_values8(v, store, pw, q);
 }
 
+// The same with the RMSNorm factor folded in: encodes x[k] * gamma[k] * r.
+__device__ __forceinline__ void encode_chunk4_gamma_scaled(const float *xc, const float *gc, float r, bool valid,
+                                                           bool store, uint32_t *pw, int q) {
+    float v[8];
+    if (valid) {
+        const float4 a = reinterpret_cast<const float4 *>(xc)[2 * q];
+        const float4 b = reinterpret_cast<const float4 *>(xc)[2 * q + 1];
+        const float4 ga = reinterpret_cast<const float4 *>(gc)[2 * q];
+        const float4 gb = reinterpret_cast<const float4 *>(gc)[2 * q + 1];
+        const float xv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = xv[i] * gv[i] * r;
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+    }
+    encode_values8(v, store, pw, q);
+}
+
 __device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, uint32_t *pw, int q) {
     float mx = 0.0f;
 #pragma unroll
