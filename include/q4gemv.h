@@ -109,9 +109,11 @@ Q4_API int q4gemv_run(const void *codes, const void *scales_f16, const void *zer
  *              projections of output i (interleaved); y[M][N/2] with
  *              y[m][i] = silu(g) * u, silu(v) = v / (1 + exp(-v)).
  * Other arguments as q4gemv_run.  With gamma NULL and no epilogue it is q4gemv_run.
- * Kernels: the streamed kernel for M = 1 where q4gemv_run would use it (same speed),
- * else a general CUDA-core kernel without K split, launched once per tile of rows of x
- * whose activations fit in shared memory.  Q4_ERR_INVALID_ARG for an unknown
+ * Kernels: fused instances of the streamed kernel (M = 1 where q4gemv_run would use it),
+ * of the register-resident kernel (other M = 1 shapes it serves without a K split), else
+ * of the general CUDA-core kernel without K split, launched once per tile of rows of x
+ * whose activations fit in shared memory (Q4_ERR_UNSUPPORTED when not even one row
+ * fits: K above about 50 000 on those shapes).  Q4_ERR_INVALID_ARG for an unknown
  * epilogue, odd N with SwiGLU, or a negative or non-finite eps; Q4_ERR_MISALIGNED for
  * an unaligned gamma. */
 Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
