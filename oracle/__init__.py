@@ -102,6 +102,10 @@ def lib() -> ctypes.CDLL:
             L.orc_silu.restype = ctypes.c_double
             L.orc_swiglu.argtypes = [_f64p, _f64p, _i64, _f64p]
             L.orc_swiglu.restype = None
+            L.orc_q40_weight.argtypes = [_u8p, _i64, _i64, _i64]
+            L.orc_q40_weight.restype = ctypes.c_float
+            L.orc_q40_gemv.argtypes = [_u8p, _f32p, _i64, _i64, _i64, _f32p, _f64p]
+            L.orc_q40_gemv.restype = None
             _lib = L
         return _lib
 
@@ -378,3 +382,44 @@ def q4_gemv_fused(codes, scales, zeros, x, gamma, eps: float, g: int, swiglu_epi
     bound = (SILU_SLOPE_MAX * bg * (np.abs(up) + bu) + (sg + SILU_SLOPE_MAX * bg) * bu
              + 2.0 ** -20 * np.abs(h) + 1e-6)
     return h, bound
+
+
+# --------------------------------------------------------------------------
+# the second format: Q4_0 blocks (32 elements in 18 bytes)
+# --------------------------------------------------------------------------
+
+def q40_weight(blocks, K: int, n: int, k: int) -> float:
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    return lib().orc_q40_weight(_ptr(blocks, _u8p), K, n, k)
+
+
+def q40_gemv(blocks, x):
+    """y[M,N] (float32) and bound[M,N] (float64) for Q4_0 blocks uint8 [N, K/32, 18]."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    N = blocks.shape[0]
+    assert blocks.shape == (N, K // 32, 18)
+    y = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    lib().orc_q40_gemv(_ptr(blocks, _u8p), _ptr(x, _f32p), M, N, K, _ptr(y, _f32p), _ptr(b, _f64p))
+    return y, b
+
+
+def q40_gemv_rows(blocks, x, rows):
+    """The Q4_0 oracle on selected output rows only."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    rows = [int(r) for r in rows]
+    y = np.empty((M, len(rows)), np.float32)
+    b = np.empty((M, len(rows)), np.float64)
+    yr = np.empty((M, 1), np.float32)
+    br = np.empty((M, 1), np.float64)
+    row_bytes = (K // 32) * 18
+    for j, n in enumerate(rows):
+        lib().orc_q40_gemv(_ptr(blocks, _u8p, n * row_bytes), _ptr(x, _f32p), M, 1, K,
+                           _ptr(yr, _f32p), _ptr(br, _f64p))
+        y[:, j] = yr[:, 0]
+        b[:, j] = br[:, 0]
+    return y, b

@@ -283,6 +283,45 @@ void orc_swiglu(const double *gate, const double *up, int64_t n, double *out)
         out[i] = orc_silu(gate[i]) * up[i];
 }
 
+/* ---------------------------------------------------------------------- */
+/* A second format: 32-element blocks of 18 bytes.                        */
+/* ---------------------------------------------------------------------- */
+
+/* cera wgpu_gemv_bench.rs, block geometry: Q4_0 holds 32 elements in 18 bytes.
+ * Read here as: a binary16 scale d (bytes 0-1, little-endian), then 16 bytes of
+ * 4-bit codes with element 2j in the low nibble of byte 2 + j and element 2j + 1
+ * in the high nibble (the INT4 packing of the kernel reference page), zero point 8
+ * (the symmetric convention).  A row of K elements is K/32 consecutive blocks.
+ * w[n][k] = (q - 8) * d, exact in binary32 as for the MatMulNBits weights. */
+float orc_q40_weight(const uint8_t *blocks, int64_t K, int64_t n, int64_t k)
+{
+    const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 18;
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    int64_t e = k % 32;
+    uint8_t byte = blk[2 + e / 2];
+    int q = (e % 2 == 0) ? (byte & 0x0f) : (byte >> 4);
+    return (float)(q - 8) * orc_f16_to_f32(dbits);
+}
+
+/* y[m][n] = sum_k W[n][k] * x[m][k] over Q4_0 weights; bound as for the GEMV. */
+void orc_q40_gemv(const uint8_t *blocks, const float *x, int64_t M, int64_t N,
+                  int64_t K, float *y, double *bound)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (double)orc_q40_weight(blocks, K, n, k) * (double)x[m * K + k];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[m * N + n] = (float)acc;
+            if (bound)
+                bound[m * N + n] = mag;
+        }
+    }
+}
+
 /* Read probe (webgpu-bench README, "read-bandwidth"; Refractometer
  * "a) bandwidth"): the sum of every binary32 element of a buffer, in
  * binary64.  The probe kernel's own partial sums are compared against it. */

@@ -74,6 +74,24 @@ def q4_weights(seed: int, N: int, K: int, group: int, scale_range=SCALE_05B,
     return Q4Weights(codes, scales, zeros, N, K, group)
 
 
+def q40_blocks(seed: int, N: int, K: int, scale_range=SCALE_05B, tag: str = "q40") -> np.ndarray:
+    """Q4_0-format weights, uint8 [N, K/32, 18]: per block the binary16 scale bits
+    (little-endian) from U[scale_range], then 16 bytes of uniform random codes."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nblk = K // 32
+    r = _rng(seed, tag + ":scales")
+    lo, hi = scale_range
+    d = r.uniform(lo, hi, size=(N, nblk)).astype(np.float32).astype(np.float16).view(np.uint16)
+    r = _rng(seed, tag + ":codes")
+    codes = np.frombuffer(r.bytes(N * nblk * 16), np.uint8).reshape(N, nblk, 16)
+    out = np.empty((N, nblk, 18), np.uint8)
+    out[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (d >> 8).astype(np.uint8)
+    out[:, :, 2:] = codes
+    return out
+
+
 def activations_f32(seed: int, M: int, K: int, tag: str = "x") -> np.ndarray:
     return _rng(seed, tag).standard_normal((M, K), dtype=np.float32)
 

@@ -48,6 +48,12 @@ MUTANTS = {
     "swiglu_swapped": ("out[i] = orc_silu(gate[i]) * up[i];", "out[i] = orc_silu(up[i]) * gate[i];"),
     "gemv_f64_dropped_first_term": ("double p = w * x[m * K + k];",
                                     "double p = (k == 0) ? 0.0 : w * x[m * K + k];"),
+    "q40_scale_byte_order": ("uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));",
+                             "uint16_t dbits = (uint16_t)(blk[1] | (blk[0] << 8));"),
+    "q40_nibble_order": ("int q = (e % 2 == 0) ? (byte & 0x0f) : (byte >> 4);",
+                         "int q = (e % 2 == 1) ? (byte & 0x0f) : (byte >> 4);"),
+    "q40_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 18;",
+                        "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 16;"),
 }
 
 

@@ -349,3 +349,54 @@ def test_fused_swiglu_pairs_even_rows_with_odd_rows():
     # the selected-outputs form agrees with the full one
     hs, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-5, g, True, outputs=[4, 1])
     np.testing.assert_array_equal(hs, h[:, [4, 1]])
+
+
+# ---------------------------------------------------------------------------
+# The second format: Q4_0 blocks (32 elements in 18 bytes: binary16 scale, then
+# 16 bytes of 4-bit codes, zero point 8).
+# ---------------------------------------------------------------------------
+
+def _q40_from_matmulnbits(codes, scales):
+    """Repack symmetric g = 32 MatMulNBits weights into Q4_0 blocks (pure byte moves)."""
+    N, half = codes.shape
+    nblk = half // 16
+    out = np.empty((N, nblk, 18), np.uint8)
+    out[:, :, 0] = (scales & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (scales >> 8).astype(np.uint8)
+    out[:, :, 2:] = codes.reshape(N, nblk, 16)
+    return out
+
+
+def test_q40_hand_worked_block():
+    # the 1x32 example: codes q_k = k mod 16 (bytes 10 32 54 76 98 BA DC FE twice),
+    # d = 0.5 (binary16 0x3800), zero point 8: x = 1 gives -8, x_k = k gives 216
+    blk = np.zeros((1, 1, 18), np.uint8)
+    blk[0, 0, 0], blk[0, 0, 1] = 0x00, 0x38
+    blk[0, 0, 2:] = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE] * 2
+    assert [oracle.q40_weight(blk, 32, 0, k) for k in (0, 1, 15, 16, 31)] == [-4.0, -3.5, 3.5, -4.0, 3.5]
+    y, _ = oracle.q40_gemv(blk, np.ones((1, 32), np.float32))
+    assert y[0, 0] == -8.0
+    y, _ = oracle.q40_gemv(blk, np.arange(32, dtype=np.float32).reshape(1, 32))
+    assert y[0, 0] == 216.0
+
+
+def test_q40_equals_symmetric_g32_after_repacking():
+    # Q4_0 is the symmetric g = 32 format with scale and codes interleaved per block:
+    # the same numbers through the two oracles agree bit for bit
+    N, K = 9, 320
+    w = synth.q4_weights(51, N, K, 32, symmetric=True)
+    blocks = _q40_from_matmulnbits(w.codes, w.scales)
+    x = synth.activations_f32(52, 3, K)
+    y1, b1 = oracle.q4_gemv(w.codes, w.scales, None, x, 32)
+    y2, b2 = oracle.q40_gemv(blocks, x)
+    np.testing.assert_array_equal(y1, y2)
+    np.testing.assert_array_equal(b1, b2)
+    y3, _ = oracle.q40_gemv_rows(blocks, x, [8, 0, 3])
+    np.testing.assert_array_equal(y3, y2[:, [8, 0, 3]])
+
+
+def test_q40_generator_layout():
+    b = synth.q40_blocks(3, 4, 64)
+    assert b.shape == (4, 2, 18) and b.dtype == np.uint8
+    d = (b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float32)
+    assert np.all((d >= 0.004) & (d <= 0.021))
