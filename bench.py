@@ -399,6 +399,7 @@ def run_gpu(args, rank, world, local_rank):
         detail["decode_8b"] = run_decode_8b(args, torch, q4)
         detail["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas,
                                                           stream)
+        detail["q4_0_format"] = run_q40(args, torch, q4)
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -989,6 +990,37 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
                 "gate|up (its output feeds down); the separate norm and activation launches this replaces "
                 "are not in the plain step"}
     return out
+
+
+def run_q40(args, torch, q4):
+    """The second format (Q4_0 blocks, 18 bytes per 32 weights: 0.5625 B per weight):
+    microseconds per q4_0_gemv_run call and GB/s from back-to-back launches over rotating
+    replicas, next to q4gemv_run on the symmetric group-32 layout of the same shape."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(40)
+    stream = torch.cuda.Stream()
+    out = []
+    for name, N, K, M in [("lm_head", 151936, 896, 1), ("qo_proj", 4096, 4096, 1), ("down_proj", 896, 4864, 1),
+                          ("lm_head", 151936, 896, 4)]:
+        nblk = K // 32
+        wbytes = N * nblk * 18
+        nrep = int(min(64, max(2, -(-6 * L2_BYTES // wbytes))))
+        reps = []
+        for _ in range(nrep):
+            b = torch.randint(0, 256, (N, nblk, 18), dtype=torch.uint8, device="cuda", generator=gen)
+            d = torch.empty((N, nblk), dtype=torch.float16, device="cuda").uniform_(0.005, 0.02, generator=gen)
+            b[:, :, 0:2] = d.view(torch.uint8).view(N, nblk, 2)
+            reps.append(b)
+        x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        st = _time_launches(torch, stream, lambda i: q4.q4_0_gemv_run(reps[i % nrep], x, y, M, N, K, stream=stream),
+                            max(nrep, 100))
+        byts = wbytes + 4 * M * K + 4 * M * N
+        out.append({"name": name, "M": M, "N": N, "K": K, "us_per_call": round(st["us"], 3),
+                    "gbs": round(byts / st["us"] / 1e3, 1), "t2n_over_tn": round(st["t2n_over_tn"], 3)})
+        del reps
+        torch.cuda.empty_cache()
+    return {"kernel": "general CUDA-core kernel, Q4_0 instances (nine 16-bit loads per block)", "cells": out}
 
 
 def run_decode_8b(args, torch, q4):

@@ -16,7 +16,7 @@ import threading
 
 __all__ = [
     "Q4Error", "lib", "library_path", "exported_names",
-    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemm_run", "f32gemv_run",
+    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4_0_gemv_run", "q4gemm_run", "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
     "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_fused_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i32, _i64, _i64,
                                            _i32, _i32, _vp]
             L.q4gemm_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
+            L.q4_0_gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_status_string.argtypes = [ctypes.c_int]
             L.q4gemv_status_string.restype = ctypes.c_char_p
@@ -87,7 +88,7 @@ def lib() -> ctypes.CDLL:
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
             L.q4gemv_bounds_violations.argtypes = [_vp]
-            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemm_run", "f32gemv_run",
+            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4_0_gemv_run", "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
                       "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations"):
@@ -167,6 +168,16 @@ def q4gemv_fused_run(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M=No
                                 float(eps), _addr(y), M, N, K, int(group), int(epilogue), _stream(stream))
     if check:
         _check(st, "q4gemv_fused_run")
+    return st
+
+
+def q4_0_gemv_run(blocks, x, y, M=None, N=None, K=None, stream=None, check=True) -> int:
+    M = int(x.shape[0] if M is None else M)
+    K = int(x.shape[1] if K is None else K)
+    N = int(blocks.shape[0] if N is None else N)
+    st = lib().q4_0_gemv_run(_addr(blocks), _addr(x), _addr(y), M, N, K, _stream(stream))
+    if check:
+        _check(st, "q4_0_gemv_run")
     return st
 
 

@@ -20,6 +20,13 @@ extern template int launch_q4gemv_fused_mt<2>(const GemvPlan &, const GemvArgs &
 extern template int launch_q4gemv_fused_mt<4>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 extern template int launch_q4gemv_fused_mt<8>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 extern template int launch_q4gemv_fused_mt<16>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+template <int MT>
+int launch_q40_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s);
+extern template int launch_q40_mt<1>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q40_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q40_mt<4>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q40_mt<8>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+extern template int launch_q40_mt<16>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 
 static int rows_per_cta(int MT, int L) {
     const int R = (MT <= 2) ? 2 : 1;
@@ -201,6 +208,39 @@ int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint
         if (st != Q4_OK) return st;
     }
     return Q4_OK;
+}
+
+// The Q4_0 GEMV (q4_0_gemv_run): the general kernel's Q4_0 instances with the plan of a
+// symmetric g = 32 GEMV of the same shape.
+int launch_q40gemv(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
+    GemvPlan p;
+    int st = plan_gemv(M, N, K, false, p);
+    if (st != Q4_OK) return st;
+    GemvArgs a;
+    a.codes = blocks;
+    a.scales = nullptr;
+    a.zeros = nullptr;
+    a.x = x;
+    a.y = y;
+    a.M = M;
+    a.N = static_cast<int>(N);
+    a.K = K;
+    a.C = K / 32;
+    a.nb = K / 32;
+    a.zrow = (a.nb + 1) / 2;
+    a.gshift = 0;
+    a.CS = p.CS;
+    a.gamma = nullptr;
+    a.eps = 0.0f;
+    a.swiglu = 0;
+    switch (p.MT) {
+        case 1: return launch_q40_mt<1>(p, a, stream);
+        case 2: return launch_q40_mt<2>(p, a, stream);
+        case 4: return launch_q40_mt<4>(p, a, stream);
+        case 8: return launch_q40_mt<8>(p, a, stream);
+        case 16: return launch_q40_mt<16>(p, a, stream);
+        default: return Q4_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace q4

@@ -78,10 +78,15 @@ struct GemvShape {
 // multiplied by 1 / sqrt(mean(x^2) + eps) when a.gamma is set (the RMSNorm prologue),
 // and with a.swiglu the gate / up row pairs (slots 2s, 2s + 1: lanes L apart) leave
 // silu(gate) * up.
-template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false>
+// Q40: the weights are Q4_0 blocks (cera wgpu_gemv_bench.rs block geometry: 32
+// elements in 18 bytes), read as a binary16 scale followed by the 16 code bytes of one
+// chunk in the packing above, zero point 8; a.codes points at the blocks [N][K/32][18]
+// (2-byte aligned), a.scales is unused.  Scale and codes come in as nine 16-bit loads.
+template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false, bool Q40 = false>
 __global__ void __launch_bounds__(kGemvThreads)
 q4gemv_kernel(const GemvArgs a) {
     static_assert(!(FUSED && SPLIT), "the fused variant is unsplit");
+    static_assert(!(Q40 && (ASYM || FUSED)), "Q4_0 blocks are symmetric and not fused");
     using S = GemvShape<MT, L>;
     constexpr int R = S::R;
     constexpr int SLOTS = S::SLOTS;
@@ -176,7 +181,17 @@ q4gemv_kernel(const GemvArgs a) {
             const int grp = c >> a.gshift;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                if (cl < nchunks) {
+                if (Q40 && cl < nchunks) {
+                    const uint16_t *hw = reinterpret_cast<const uint16_t *>(
+                        a.codes + (rowc[r] * a.C + c) * 18);   // block c of row rowc[r]
+                    sc[r][u] = ldg_u16(hw);
+                    uint32_t h[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) h[i] = ldg_u16(hw + 1 + i);
+                    cw[r][u] = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                          h[6] | (h[7] << 16));
+                    zq[r][u] = 8u;
+                } else if (cl < nchunks) {
                     cw[r][u] = ldg_stream(a.codes + rowc[r] * pitch + static_cast<int64_t>(c) * 16);
                     sc[r][u] = ldg_u16(a.scales + rowc[r] * a.nb + grp);
                     if (ASYM) {

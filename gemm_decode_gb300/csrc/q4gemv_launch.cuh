@@ -7,9 +7,9 @@
 
 namespace q4 {
 
-template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false>
+template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false, bool Q40 = false>
 static int launch_gemv_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t stream) {
-    auto kern = q4gemv_kernel<MT, L, ASYM, SPLIT, FUSED>;
+    auto kern = q4gemv_kernel<MT, L, ASYM, SPLIT, FUSED, Q40>;
     // Opt into the large shared-memory carve-out once per device.
     static bool configured[64] = {};
     int dev = 0;
@@ -71,6 +71,24 @@ template <int MT>
 int launch_q4gemv_fused_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s) {
     return p.asym ? launch_gemv_one<MT, 16, true, false, true>(p, a, s)
                   : launch_gemv_one<MT, 16, false, false, true>(p, a, s);
+}
+
+// Q4_0 blocks: the plan's lanes per row and split, symmetric.
+template <int MT, int L>
+static int launch_q40_l(const GemvPlan &p, const GemvArgs &a, cudaStream_t s) {
+    return p.S > 1 ? launch_gemv_one<MT, L, false, true, false, true>(p, a, s)
+                   : launch_gemv_one<MT, L, false, false, false, true>(p, a, s);
+}
+
+template <int MT>
+int launch_q40_mt(const GemvPlan &p, const GemvArgs &a, cudaStream_t s) {
+    switch (p.L) {
+        case 4: return launch_q40_l<MT, 4>(p, a, s);
+        case 8: return launch_q40_l<MT, 8>(p, a, s);
+        case 16: return launch_q40_l<MT, 16>(p, a, s);
+        case 32: return launch_q40_l<MT, 32>(p, a, s);
+        default: return Q4_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace q4

@@ -4,4 +4,5 @@
 namespace q4 {
 template int launch_q4gemv_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 template int launch_q4gemv_fused_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
+template int launch_q40_mt<2>(const GemvPlan &, const GemvArgs &, cudaStream_t);
 }  // namespace q4

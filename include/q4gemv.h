@@ -120,6 +120,18 @@ Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const voi
                      const float *x, const float *gamma, float eps, float *y, int32_t M, int64_t N,
                      int64_t K, int32_t group, int32_t epilogue, void *stream);
 
+/* GEMV over a second weight format, Q4_0 blocks (cera wgpu_gemv_bench.rs, block
+ * geometry: Q4_0 holds 32 elements in 18 bytes), 1 <= M <= 16:
+ * y[m][n] = sum_k (q[n][k] - 8) * d[n][k/32] * x[m][k].
+ *   blocks : device, [N][K/32][18] bytes, 2-byte aligned: per block the binary16 scale d
+ *            (little-endian), then 16 bytes of 4-bit codes, element 2j in the low nibble
+ *            of byte j and element 2j+1 in the high nibble (zero point 8)
+ *   x : device float [M][K], 16-byte aligned;  y : device float [M][N]
+ * K a multiple of 32.  Runs the general CUDA-core kernel's Q4_0 instances (the plan of
+ * the symmetric group-32 GEMV of the same shape).  Asynchronous; allocates nothing. */
+Q4_API int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K,
+                  void *stream);
+
 /* Prefill-shaped int4 matmul on the tensor cores (tcgen05, bf16 operands, f32
  * accumulate in tensor memory), any M >= 1 (tiles of 128 rows; a partial tile is
  * padded and masked).

@@ -118,6 +118,17 @@ def test_fused_gemv_argument_checks(L):
     assert r(A, A, None, A + 4, A, 1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_MISALIGNED
 
 
+def test_q40_argument_checks(L):
+    r = L.q4_0_gemv_run
+    assert r(A, A, A, 1, 64, 48, None) == q4.Q4_ERR_INVALID_ARG      # K not a multiple of 32
+    assert r(A, A, A, -1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, A, 17, 64, 64, None) == q4.Q4_ERR_UNSUPPORTED
+    assert r(None, None, None, 0, 64, 64, None) == q4.Q4_OK
+    assert r(None, A, A, 1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A + 1, A, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED    # blocks: 2-byte aligned
+    assert r(A + 2, A + 4, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED  # x: 16-byte aligned
+
+
 def test_gemm_and_control_argument_checks(L):
     g = L.q4gemm_run
     assert g(A, A, None, A, A, 1, 64, 100, 32, None) == q4.Q4_ERR_INVALID_ARG
