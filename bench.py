@@ -1020,7 +1020,9 @@ def run_q40(args, torch, q4):
                     "gbs": round(byts / st["us"] / 1e3, 1), "t2n_over_tn": round(st["t2n_over_tn"], 3)})
         del reps
         torch.cuda.empty_cache()
-    return {"kernel": "general CUDA-core kernel, Q4_0 instances (nine 16-bit loads per block)", "cells": out}
+    return {"kernel": "streamed kernel's Q4_0 instances (M = 1, long matrices: whole 18-byte blocks by bulk copy, "
+                      "codes read as five 32-bit words shifted to the 2-byte offset), else the general kernel's "
+                      "(nine 16-bit loads per block)", "cells": out}
 
 
 def run_decode_8b(args, torch, q4):

@@ -210,9 +210,11 @@ int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint
     return Q4_OK;
 }
 
-// The Q4_0 GEMV (q4_0_gemv_run): the general kernel's Q4_0 instances with the plan of a
-// symmetric g = 32 GEMV of the same shape.
+// The Q4_0 GEMV (q4_0_gemv_run): the streamed kernel's Q4_0 instances for M = 1 on long
+// matrices, else the general kernel's Q4_0 instances with the plan of a symmetric g = 32
+// GEMV of the same shape.
 int launch_q40gemv(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
+    if (stream_q40_applies(M, N, K, blocks)) return launch_q4gemv_stream_q40(blocks, x, y, N, K, stream);
     GemvPlan p;
     int st = plan_gemv(M, N, K, false, p);
     if (st != Q4_OK) return st;

@@ -91,8 +91,9 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
 static unsigned long long g_stream_timeout_ns = 1000ull * 1000 * 1000;
 void set_stream_wait_timeout_ns(unsigned long long ns) { g_stream_timeout_ns = ns; }
 
+// fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks)
 static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
-                             const float *gamma, float eps, int swiglu, bool fused, float *y, int64_t N, int K,
+                             const float *gamma, float eps, int swiglu, int fuse, float *y, int64_t N, int K,
                              int group, cudaStream_t stream) {
     const bool asym = zeros != nullptr;
     const int rg = stream_rg(K);
@@ -113,11 +114,11 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
     a.swiglu = swiglu;
     if (a.status == nullptr) return Q4_ERR_CUDA;
     const int u = stream_u(K);
-    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym, fused);
+    const bool q40 = fuse == 4;
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, q40), asym, fuse == 1 || fuse == 3,
+                            q40);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
-    // fused instances: 1 = RMSNorm only, 3 = also SwiGLU (the norm stays a runtime choice)
-    const int fuse = fused ? (swiglu ? 3 : 1) : 0;
     switch (K) {
         case 896: return launch_stream_k896(a, group, asym, fuse, stream);
         case 2048: return launch_stream_k2048(a, group, asym, fuse, stream);
@@ -125,6 +126,7 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
         case 8192: return launch_stream_k8192(a, group, asym, fuse, stream);
         case 16384: return launch_stream_k16384(a, group, asym, fuse, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
+            if (fuse == 4) return launch_stream<0, 0, 0, 8, false, 4>(a, stream);
             if (fuse == 3)
                 return asym ? launch_stream<0, 0, 0, 8, true, 3>(a, stream) : launch_stream<0, 0, 0, 8, false, 3>(a, stream);
             if (fuse == 1)
@@ -135,13 +137,29 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
 
 int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                          float *y, int64_t N, int K, int group, cudaStream_t stream) {
-    return launch_stream_any(codes, scales, zeros, x, nullptr, 0.0f, 0, false, y, N, K, group, stream);
+    return launch_stream_any(codes, scales, zeros, x, nullptr, 0.0f, 0, 0, y, N, K, group, stream);
 }
 
 int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                                const float *gamma, float eps, int swiglu, float *y, int64_t N, int K, int group,
                                cudaStream_t stream) {
-    return launch_stream_any(codes, scales, zeros, x, gamma, eps, swiglu, true, y, N, K, group, stream);
+    // fused instances: 1 = RMSNorm only, 3 = also SwiGLU (the norm stays a runtime choice)
+    return launch_stream_any(codes, scales, zeros, x, gamma, eps, swiglu, swiglu ? 3 : 1, y, N, K, group, stream);
+}
+
+bool stream_q40_applies(int M, int64_t N, int K, const void *blocks) {
+    if (M != 1 || N < 4096 || K % 32 != 0 || !aligned(blocks, 16)) return false;
+    const int rg = stream_rg(K);
+    if (rg == 0) return false;
+    const int u = stream_u(K);
+    const StreamGeo g = make_stream_geo(K, 32, rg, u, stream_slots(K, 32, rg, u, false, true), false, false, true);
+    if (g.ROWS % 8 != 0) return false;   // every block of rows starts 16-byte aligned
+    if (K < 2048 && (N + g.ROWS - 1) / g.ROWS < device_info().sms) return false;
+    return stream_geo_ok(g, false);
+}
+
+int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream) {
+    return launch_stream_any(blocks, nullptr, nullptr, x, nullptr, 0.0f, 0, 4, y, N, K, 32, stream);
 }
 
 int read_and_clear_stream_status(unsigned int *v) {

@@ -39,9 +39,11 @@ __host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 12
 __host__ __device__ constexpr int stream_u(int K) { return K == 896 ? 6 : 8; }
 
 // fused: the fused-variant kernels also keep their RMSNorm sums (one float per consumer
-// warp) in 128 bytes after the abort flag.
+// warp) in 128 bytes after the abort flag.  q40: the weights are Q4_0 blocks (32 codes and
+// their binary16 scale in 18 bytes), so a block of rows is one stretch of ROWS * C * 18
+// bytes (group 32, no zero points).
 __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym,
-                                                        bool fused = false) {
+                                                        bool fused = false, bool q40 = false) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
@@ -52,10 +54,12 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
     g.ROWS = U * RG;
     g.TC = g.C * RG;
     g.NWC = g.TC / 32;
-    g.CODE_B = g.ROWS * g.C * 16;
-    g.SC_B = g.ROWS * g.NB * 2;
-    g.Z_B = asym ? g.ROWS * g.ZROW : 0;
-    g.SLOT_B = stream_round128(g.CODE_B + g.SC_B + g.Z_B);
+    g.CODE_B = g.ROWS * g.C * (q40 ? 18 : 16);
+    g.SC_B = q40 ? 0 : g.ROWS * g.NB * 2;
+    g.Z_B = asym && !q40 ? g.ROWS * g.ZROW : 0;
+    // (Q4_0: 16 bytes of slack, as the 2-byte-aligned code reads fetch up to 2 bytes past
+    // a slot's last block)
+    g.SLOT_B = stream_round128(g.CODE_B + g.SC_B + g.Z_B + (q40 ? 16 : 0));
     g.WRED = g.C % 32 == 0 ? 1 : 0;
     g.PARTS = g.WRED ? g.C / 32 : g.C;
     g.RED_LD = g.PARTS + 1;
@@ -75,9 +79,9 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
 // Ring slots: three (one more block in flight) when they fit the shared-memory
 // budget without lowering the CTAs an SM holds, else two.
 __host__ __device__ constexpr int stream_ctas_per_sm(int smem) { return kStreamSmemPerSM / (smem + 1024); }
-__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym) {
-    const int s2 = make_stream_geo(K, G, RG, U, 2, asym).SMEM;
-    const int s3 = make_stream_geo(K, G, RG, U, 3, asym).SMEM;
+__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym, bool q40 = false) {
+    const int s2 = make_stream_geo(K, G, RG, U, 2, asym, false, q40).SMEM;
+    const int s3 = make_stream_geo(K, G, RG, U, 3, asym, false, q40).SMEM;
     return (s3 <= kStreamSmemBudget && stream_ctas_per_sm(s3) >= stream_ctas_per_sm(s2)) ? 3 : 2;
 }
 
@@ -110,6 +114,9 @@ int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uin
 int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                                const float *gamma, float eps, int swiglu, float *y, int64_t N, int K, int group,
                                cudaStream_t stream);
+// Q4_0 blocks (q4_0_gemv_run): whether the streamed kernel serves the problem, and the launch.
+bool stream_q40_applies(int M, int64_t N, int K, const void *blocks);
+int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream);
 void set_stream_wait_timeout_ns(unsigned long long ns);
 int read_and_clear_stream_status(unsigned int *v);
 

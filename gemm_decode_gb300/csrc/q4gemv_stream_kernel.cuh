@@ -16,11 +16,11 @@ namespace {
 
 // The geometry an instance works with: compile-time when the instance fixes K, g
 // and RG (the tuned decode shapes), else the launcher's.
-template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED>
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED, bool Q40 = false>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
         constexpr StreamGeo g =
-            make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM), ASYM, FUSED);
+            make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM, Q40), ASYM, FUSED, Q40);
         return g;
     } else {
         return rt;
@@ -34,14 +34,16 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 // the RMSNorm prologue when a.gamma is set -- a first pass sums x^2 over the row, then
 // x is encoded as x * gamma / sqrt(mean(x^2) + eps), so the dot products and the
 // reduction are those of the plain kernel; bit 1, the SwiGLU epilogue when a.swiglu is
-// set -- the gate / up row pairs leave silu(gate) * up.
+// set -- the gate / up row pairs leave silu(gate) * up.  FUSE = 4: the weights are Q4_0
+// blocks (a.codes; 18 bytes per 32 codes: binary16 scale, then the codes; zero point 8).
 template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgs a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
-    constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0;
-    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, FUSE != 0>(a.geo);
+    constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0, Q40 = (FUSE & 4) != 0;
+    static_assert(!Q40 || (!ASYM && (KC == 0 || GC == 32) && FUSE == 4), "Q4_0: group 32, symmetric, not fused");
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -106,6 +108,16 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 const unsigned char *src_z = ASYM ? a.zeros + row0 * G.ZROW : nullptr;
                 if (!ib(row0 >= 0 && rows >= 1 && row0 + rows <= a.N && s < D)) {
                     mbar_arrive(full(s));   // (checking builds) keep the ring moving, copy nothing
+                } else if constexpr (Q40) {
+                    // Q4_0: one stretch of rows * C * 18 bytes (a 16-byte multiple for a whole
+                    // block of rows); its largest 16-byte multiple by bulk copy, the at most
+                    // 15 bytes left by plain copies, published by the arrive below
+                    const unsigned char *src = a.codes + row0 * (C * 18);
+                    const int cb = rows * C * 18, cb16 = cb & ~15;
+                    unsigned char *sl = smem + G.OFF_RING + s * G.SLOT_B;
+                    for (int j = cb16; j < cb; ++j) sl[j] = src[j];
+                    mbar_expect_tx(full(s), cb16);
+                    bulk_copy(dst, src, cb16, full(s));
                 } else if (rows == G.ROWS) {
                     mbar_expect_tx(full(s), G.CODE_B + G.SC_B + G.Z_B);
                     bulk_copy(dst, src_c, G.CODE_B, full(s));
@@ -279,11 +291,31 @@ q4gemv_stream_kernel(const StreamArgs a) {
         float v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const bool c_ok = ib(off_c + u * str_c + 16 <= static_cast<uint32_t>(G.CODE_B));
-            const bool s_ok = ib(off_s + u * str_s + 2 <= static_cast<uint32_t>(G.CODE_B + G.SC_B));
+            uint4 cw;
+            uint32_t sh;
+            if constexpr (Q40) {
+                // block (r + RG u) * C + c: its scale at 18 * block, its 16 code bytes from
+                // 18 * block + 2 (2-byte aligned): five words from the 4-byte boundary below,
+                // shifted by 0 or 16 bits (the fifth word may reach 4 bytes past the block,
+                // inside the slot's 16 bytes of slack after its last block)
+                const uint32_t boff = static_cast<uint32_t>((r * C + c) * 18) + u * static_cast<uint32_t>(G.RG * C * 18);
+                const bool b_ok = ib(boff + 18 <= static_cast<uint32_t>(G.CODE_B));
+                const uint32_t cstart = boff + 2, base = cstart & ~3u, shift = (cstart & 3u) * 8u;
+                uint32_t w[5] = {0u, 0u, 0u, 0u, 0u};
+                if (b_ok) {
+#pragma unroll
+                    for (int i = 0; i < 5; ++i) w[i] = lds_u32(sl + base + 4 * i);
+                }
+                cw = make_uint4(__funnelshift_r(w[0], w[1], shift), __funnelshift_r(w[1], w[2], shift),
+                                __funnelshift_r(w[2], w[3], shift), __funnelshift_r(w[3], w[4], shift));
+                sh = b_ok ? lds_u16(sl + boff) : 0u;
+            } else {
+                const bool c_ok = ib(off_c + u * str_c + 16 <= static_cast<uint32_t>(G.CODE_B));
+                const bool s_ok = ib(off_s + u * str_s + 2 <= static_cast<uint32_t>(G.CODE_B + G.SC_B));
+                cw = c_ok ? lds128(sl + off_c + u * str_c) : make_uint4(0u, 0u, 0u, 0u);
+                sh = s_ok ? lds_u16(sl + off_s + u * str_s) : 0u;
+            }
             const bool z_ok = !ASYM || ib(off_z + u * str_z + 1 <= static_cast<uint32_t>(G.CODE_B + G.SC_B + G.Z_B));
-            const uint4 cw = c_ok ? lds128(sl + off_c + u * str_c) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t sh = s_ok ? lds_u16(sl + off_s + u * str_s) : 0u;
             const int z = ASYM ? (z_ok ? static_cast<int>((lds_u8(sl + off_z + u * str_z) >> zsh) & 0xFu) : 8) : 8;
             const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sh)));
             v[u] = (sc * P.f) * chunk_dot(cw, z, P);
@@ -404,6 +436,10 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
 template <int KV, int GV, int RGV>
 int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
     constexpr int UV = stream_u(KV);
+    if (fuse == 4) {   // Q4_0 blocks: group 32, symmetric
+        if constexpr (GV == 32) return asym ? Q4_ERR_UNSUPPORTED : launch_stream<KV, 32, RGV, UV, false, 4>(a, s);
+        return Q4_ERR_UNSUPPORTED;
+    }
     switch (fuse) {
         case 0: return asym ? launch_stream<KV, GV, RGV, UV, true, 0>(a, s) : launch_stream<KV, GV, RGV, UV, false, 0>(a, s);
         case 1: return asym ? launch_stream<KV, GV, RGV, UV, true, 1>(a, s) : launch_stream<KV, GV, RGV, UV, false, 1>(a, s);

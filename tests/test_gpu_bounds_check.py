@@ -103,3 +103,15 @@ def test_fused_kernels(torch, N, K, g):
                   | {0, N // 2 - 1})
     ref, tol = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-6, g, True, outputs=outs)
     assert np.all(np.abs(host(y)[:, outs] - ref) <= tol)
+
+
+@pytest.mark.parametrize("N,K", [(9765, 896), (40003, 608)])
+def test_q40_streamed_kernel(torch, N, K):
+    blocks = synth.q40_blocks(N + 7, N, K)
+    x = synth.activations_f32(N + 8, 1, K)
+    y = torch.full((1, N), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q4_0_gemv_run(dev(blocks, torch), dev(x, torch), y, 1, N, K)
+    assert q4.q4gemv_bounds_violations() == 0, f"Q4_0 N={N} K={K}: out-of-range accesses counted"
+    rows = sorted(set(np.random.default_rng(3).choice(N, 64, replace=False).tolist()) | {0, N - 1})
+    y_ref, bound = oracle.q40_gemv_rows(blocks, x, rows)
+    assert_within_bound(host(y)[:, rows], y_ref, bound, f"Q4_0 bounds N={N} K={K}")

@@ -77,3 +77,16 @@ def test_deterministic_and_empty(torch):
     x = synth.activations_f32(12, 4, 2048)
     np.testing.assert_array_equal(run(torch, blocks, x), run(torch, blocks, x))
     assert q4.q4_0_gemv_run(None, None, None, 0, 64, 64, check=False) == q4.Q4_OK
+
+
+@pytest.mark.parametrize("N,K", [(9765, 896), (8195, 2048), (4901, 4096), (4101, 14336), (40003, 608)])
+def test_streamed_kernel(torch, N, K):
+    # M = 1 on long matrices: the streamed kernel's Q4_0 instances (a block of rows is one
+    # stretch of 18-byte blocks).  9765 x 896: a last block of 21 rows, 8 bytes past a
+    # 16-byte multiple; 14336 and 608: the runtime geometry, 608 with 19 chunks per row
+    blocks = synth.q40_blocks(N + K, N, K)
+    x = synth.activations_f32(N - K, 1, K)
+    y = run(torch, blocks, x)
+    rows = sorted(set(np.random.default_rng(4).choice(N, 300, replace=False).tolist()) | set(range(N - 70, N)) | {0})
+    y_ref, bound = oracle.q40_gemv_rows(blocks, x, rows)
+    assert_within_bound(y[:, rows], y_ref, bound, f"Q4_0 streamed N={N} K={K}")
