@@ -127,8 +127,10 @@ Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const voi
  *            (little-endian), then 16 bytes of 4-bit codes, element 2j in the low nibble
  *            of byte j and element 2j+1 in the high nibble (zero point 8)
  *   x : device float [M][K], 16-byte aligned;  y : device float [M][N]
- * K a multiple of 32.  Runs the general CUDA-core kernel's Q4_0 instances (the plan of
- * the symmetric group-32 GEMV of the same shape).  Asynchronous; allocates nothing. */
+ * K a multiple of 32.  M = 1 with N >= 4096 and blocks 16-byte aligned runs the
+ * TMA-streamed kernel's Q4_0 instances where its ring of row blocks fits shared memory;
+ * every other shape the general CUDA-core kernel's (the plan of the symmetric group-32
+ * GEMV of the same shape).  Asynchronous; allocates nothing. */
 Q4_API int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K,
                   void *stream);
 
