@@ -106,6 +106,10 @@ def lib() -> ctypes.CDLL:
             L.orc_q40_weight.restype = ctypes.c_float
             L.orc_q40_gemv.argtypes = [_u8p, _f32p, _i64, _i64, _i64, _f32p, _f64p]
             L.orc_q40_gemv.restype = None
+            L.orc_q80_weight.argtypes = [_u8p, _i64, _i64, _i64]
+            L.orc_q80_weight.restype = ctypes.c_float
+            L.orc_q80_gemv.argtypes = [_u8p, _f32p, _i64, _i64, _i64, _f32p, _f64p]
+            L.orc_q80_gemv.restype = None
             _lib = L
         return _lib
 
@@ -419,6 +423,47 @@ def q40_gemv_rows(blocks, x, rows):
     row_bytes = (K // 32) * 18
     for j, n in enumerate(rows):
         lib().orc_q40_gemv(_ptr(blocks, _u8p, n * row_bytes), _ptr(x, _f32p), M, 1, K,
+                           _ptr(yr, _f32p), _ptr(br, _f64p))
+        y[:, j] = yr[:, 0]
+        b[:, j] = br[:, 0]
+    return y, b
+
+
+# --------------------------------------------------------------------------
+# the third format: Q8_0 blocks (32 elements in 34 bytes)
+# --------------------------------------------------------------------------
+
+def q80_weight(blocks, K: int, n: int, k: int) -> float:
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    return lib().orc_q80_weight(_ptr(blocks, _u8p), K, n, k)
+
+
+def q80_gemv(blocks, x):
+    """y[M,N] (float32) and bound[M,N] (float64) for Q8_0 blocks uint8 [N, K/32, 34]."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    N = blocks.shape[0]
+    assert blocks.shape == (N, K // 32, 34)
+    y = np.empty((M, N), np.float32)
+    b = np.empty((M, N), np.float64)
+    lib().orc_q80_gemv(_ptr(blocks, _u8p), _ptr(x, _f32p), M, N, K, _ptr(y, _f32p), _ptr(b, _f64p))
+    return y, b
+
+
+def q80_gemv_rows(blocks, x, rows):
+    """The Q8_0 oracle on selected output rows only."""
+    x = np.ascontiguousarray(x, np.float32)
+    M, K = x.shape
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    rows = [int(r) for r in rows]
+    y = np.empty((M, len(rows)), np.float32)
+    b = np.empty((M, len(rows)), np.float64)
+    yr = np.empty((M, 1), np.float32)
+    br = np.empty((M, 1), np.float64)
+    row_bytes = (K // 32) * 34
+    for j, n in enumerate(rows):
+        lib().orc_q80_gemv(_ptr(blocks, _u8p, n * row_bytes), _ptr(x, _f32p), M, 1, K,
                            _ptr(yr, _f32p), _ptr(br, _f64p))
         y[:, j] = yr[:, 0]
         b[:, j] = br[:, 0]

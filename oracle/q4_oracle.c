@@ -322,6 +322,45 @@ void orc_q40_gemv(const uint8_t *blocks, const float *x, int64_t M, int64_t N,
     }
 }
 
+/* ---------------------------------------------------------------------- */
+/* A third format: 32-element blocks of 34 bytes.                         */
+/* ---------------------------------------------------------------------- */
+
+/* cera wgpu_gemv_bench.rs, block geometry: Q8_0 holds 32 elements in 34 bytes.
+ * Read here as: a binary16 scale d (bytes 0-1, little-endian, as for Q4_0), then
+ * 32 signed 8-bit codes in two's complement, element j of the block at byte 2 + j;
+ * no zero point.  A row of K elements is K/32 consecutive blocks.
+ * w[n][k] = q * d: |q| <= 128 (8 bits) times an 11-bit significand is exact in
+ * binary32. */
+float orc_q80_weight(const uint8_t *blocks, int64_t K, int64_t n, int64_t k)
+{
+    const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 34;
+    uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));
+    int q = blk[2 + k % 32];
+    if (q >= 128)
+        q -= 256;
+    return (float)q * orc_f16_to_f32(dbits);
+}
+
+/* y[m][n] = sum_k W[n][k] * x[m][k] over Q8_0 weights; bound as for the GEMV. */
+void orc_q80_gemv(const uint8_t *blocks, const float *x, int64_t M, int64_t N,
+                  int64_t K, float *y, double *bound)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double p = (double)orc_q80_weight(blocks, K, n, k) * (double)x[m * K + k];
+                acc += p;
+                mag += fabs(p);
+            }
+            y[m * N + n] = (float)acc;
+            if (bound)
+                bound[m * N + n] = mag;
+        }
+    }
+}
+
 /* Read probe (webgpu-bench README, "read-bandwidth"; Refractometer
  * "a) bandwidth"): the sum of every binary32 element of a buffer, in
  * binary64.  The probe kernel's own partial sums are compared against it. */

@@ -92,6 +92,30 @@ def q40_blocks(seed: int, N: int, K: int, scale_range=SCALE_05B, tag: str = "q40
     return out
 
 
+# Q8_0 codes span -128..127, sixteen times the int4 span: scales a sixteenth of the
+# 0.5B-class range keep the weights of the same magnitude.
+SCALE_Q80 = (0.005 / 16, 0.02 / 16)
+
+
+def q80_blocks(seed: int, N: int, K: int, scale_range=SCALE_Q80, tag: str = "q80") -> np.ndarray:
+    """Q8_0-format weights, uint8 [N, K/32, 34]: per block the binary16 scale bits
+    (little-endian) from U[scale_range], then 32 uniform random bytes (the codes,
+    read as two's-complement int8)."""
+    if K % 32:
+        raise ValueError("K must be a multiple of 32")
+    nblk = K // 32
+    r = _rng(seed, tag + ":scales")
+    lo, hi = scale_range
+    d = r.uniform(lo, hi, size=(N, nblk)).astype(np.float32).astype(np.float16).view(np.uint16)
+    r = _rng(seed, tag + ":codes")
+    codes = np.frombuffer(r.bytes(N * nblk * 32), np.uint8).reshape(N, nblk, 32)
+    out = np.empty((N, nblk, 34), np.uint8)
+    out[:, :, 0] = (d & 0xFF).astype(np.uint8)
+    out[:, :, 1] = (d >> 8).astype(np.uint8)
+    out[:, :, 2:] = codes
+    return out
+
+
 def activations_f32(seed: int, M: int, K: int, tag: str = "x") -> np.ndarray:
     return _rng(seed, tag).standard_normal((M, K), dtype=np.float32)
 

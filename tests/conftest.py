@@ -50,6 +50,35 @@ def load_golden(name):
     return d
 
 
+def load_golden_blocks(name):
+    """Parse a hand-worked block-format fixture: N, K, the raw bytes of every block
+    in row order (uint8 [N, K/32, bytes per block]), the (x_kind, y) cases and the
+    expected weights of the row(s)."""
+    d = {"cases": [], "blocks": []}
+    xkind = None
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key in ("N", "K"):
+                d[key] = int(vals[0])
+            elif key == "block":
+                d["blocks"].append([int(v, 16) for v in vals])
+            elif key == "x":
+                xkind = vals[0]
+            elif key == "y":
+                d["cases"].append((xkind, np.array([float(v) for v in vals], np.float32)))
+            elif key == "weights":
+                d["weights"] = np.array([float(v) for v in vals], np.float32)
+            else:
+                raise ValueError(f"unknown golden key {key!r} in {name}")
+    N, K = d["N"], d["K"]
+    d["blocks"] = np.array(d["blocks"], np.uint8).reshape(N, K // 32, -1)
+    return d
+
+
 def golden_x(kind, K):
     if kind == "ones":
         return np.ones((1, K), np.float32)

@@ -54,6 +54,12 @@ MUTANTS = {
                          "int q = (e % 2 == 1) ? (byte & 0x0f) : (byte >> 4);"),
     "q40_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 18;",
                         "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 16;"),
+    "q80_unsigned_codes": ("    if (q >= 128)\n        q -= 256;\n", "\n"),
+    "q80_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 34;",
+                        "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 32;"),
+    "q80_code_offset": ("int q = blk[2 + k % 32];", "int q = blk[1 + k % 32];"),
+    "q80_scale_byte_order": ("uint16_t dbits = (uint16_t)(blk[0] | (blk[1] << 8));\n    int q = blk",
+                             "uint16_t dbits = (uint16_t)(blk[1] | (blk[0] << 8));\n    int q = blk"),
 }
 
 

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from conftest import GOLDEN_FILES, golden_x, load_golden, pack_codes, pack_zeros
+from conftest import GOLDEN_FILES, golden_x, load_golden, load_golden_blocks, pack_codes, pack_zeros
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -400,3 +400,94 @@ def test_q40_generator_layout():
     assert b.shape == (4, 2, 18) and b.dtype == np.uint8
     d = (b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float32)
     assert np.all((d >= 0.004) & (d <= 0.021))
+
+
+# ---------------------------------------------------------------------------
+# The third format: Q8_0 blocks (32 elements in 34 bytes: binary16 scale, then
+# 32 two's-complement int8 codes, no zero point).
+# ---------------------------------------------------------------------------
+
+def test_q80_hand_worked_blocks():
+    d = load_golden_blocks("hand_q8_0_1x64.txt")
+    blocks, K = d["blocks"], d["K"]
+    assert blocks.shape == (1, 2, 34)
+    w = np.array([oracle.q80_weight(blocks, K, 0, k) for k in range(K)], np.float32)
+    np.testing.assert_array_equal(w, d["weights"])
+    for kind, y_expect in d["cases"]:
+        y, _ = oracle.q80_gemv(blocks, golden_x(kind, K))
+        np.testing.assert_array_equal(y[0], y_expect)
+
+
+def test_q80_equals_q40_on_the_int4_range():
+    # Q8_0 codes restricted to -8..7 are Q4_0 codes q + 8 with the same scale: the two
+    # oracles agree bit for bit, products, sums and bounds alike
+    N, K = 7, 192
+    r = np.random.default_rng(61)
+    q = r.integers(-8, 8, size=(N, K))
+    d = r.uniform(0.005, 0.02, size=(N, K // 32)).astype(np.float16).view(np.uint16)
+    b8 = np.empty((N, K // 32, 34), np.uint8)
+    b8[:, :, 0], b8[:, :, 1] = d & 0xFF, d >> 8
+    b8[:, :, 2:] = (q.reshape(N, K // 32, 32) & 0xFF).astype(np.uint8)
+    codes = pack_codes(q + 8).reshape(N, K // 32, 16)
+    b4 = np.empty((N, K // 32, 18), np.uint8)
+    b4[:, :, 0], b4[:, :, 1] = d & 0xFF, d >> 8
+    b4[:, :, 2:] = codes
+    x = synth.activations_f32(62, 3, K)
+    y8, m8 = oracle.q80_gemv(b8, x)
+    y4, m4 = oracle.q40_gemv(b4, x)
+    np.testing.assert_array_equal(y8, y4)
+    np.testing.assert_array_equal(m8, m4)
+
+
+def test_q80_weights_against_numpy_views():
+    # brute force: every weight of a small matrix decoded by numpy's own int8 and
+    # little-endian binary16 views of the same bytes
+    N, K = 3, 96
+    blocks = synth.q80_blocks(63, N, K)
+    d = blocks[:, :, :2].copy().view("<f2")[..., 0].astype(np.float64)
+    q = blocks[:, :, 2:].view(np.int8).astype(np.float64)
+    w = (q * d[:, :, None]).reshape(N, K)
+    got = np.array([[oracle.q80_weight(blocks, K, n, k) for k in range(K)] for n in range(N)], np.float64)
+    np.testing.assert_array_equal(got, w)
+    assert q.min() < -100 and q.max() > 100      # both signs and the far ends exercised
+
+
+def test_q80_gemv_against_exact_sums():
+    # y is one rounding of the exact sum (math.fsum) up to the f64 accumulation error
+    N, K, M = 5, 320, 2
+    blocks = synth.q80_blocks(64, N, K)
+    x = synth.activations_f32(65, M, K)
+    d = blocks[:, :, :2].copy().view("<f2")[..., 0].astype(np.float64)
+    w = (blocks[:, :, 2:].view(np.int8).astype(np.float64) * d[:, :, None]).reshape(N, K)
+    y, bound = oracle.q80_gemv(blocks, x)
+    for m in range(M):
+        for n in range(N):
+            p = [w[n, k] * float(x[m, k]) for k in range(K)]
+            exact = math.fsum(p)
+            mag = math.fsum(abs(v) for v in p)
+            assert abs(float(y[m, n]) - exact) <= abs(exact) * 2.0 ** -23 + K * 2.0 ** -52 * mag
+            assert abs(bound[m, n] - mag) <= K * 2.0 ** -52 * mag
+    ys, bs = oracle.q80_gemv_rows(blocks, x, [4, 0, 2])
+    np.testing.assert_array_equal(ys, y[:, [4, 0, 2]])
+    np.testing.assert_array_equal(bs, bound[:, [4, 0, 2]])
+
+
+def test_q80_one_hot_and_linearity():
+    N, K = 4, 64
+    blocks = synth.q80_blocks(66, N, K)
+    for k in (0, 31, 32, 63):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        y, _ = oracle.q80_gemv(blocks, x)
+        np.testing.assert_array_equal(y[0], [oracle.q80_weight(blocks, K, n, k) for n in range(N)])
+    x = synth.activations_f32(67, 1, K)
+    y1, _ = oracle.q80_gemv(blocks, x)
+    y2, _ = oracle.q80_gemv(blocks, x * np.float32(8.0))
+    np.testing.assert_array_equal(y2, y1 * np.float32(8.0))
+
+
+def test_q80_generator_layout():
+    b = synth.q80_blocks(3, 4, 64)
+    assert b.shape == (4, 2, 34) and b.dtype == np.uint8
+    d = (b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float32)
+    assert np.all((d >= 0.0003) & (d <= 0.00126))
