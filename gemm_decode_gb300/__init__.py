@@ -105,11 +105,19 @@ def exported_names():
 
 # ------------------------------------------------------------------ marshalling
 
-def _addr(t):
+def _addr(t, name="argument", esize=0):
+    """Address of an array argument: None and integer addresses pass through as given;
+    a tensor must be contiguous (the library reads packed row-major arrays) and, where
+    esize is set, hold elements of esize bytes.  Metadata checks only: where the memory
+    lives and how large it is stay the caller's responsibility, as in the C ABI."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: a contiguous tensor is required (got strides {tuple(t.stride())})")
+    if esize and t.element_size() != esize:
+        raise ValueError(f"{name}: {esize}-byte elements expected, got {t.dtype}")
     return t.data_ptr()
 
 
@@ -154,8 +162,9 @@ def _mnk_q4(codes, x, M, N, K):
 def q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M=None, N=None, K=None, group=32,
                stream=None, check=True) -> int:
     M, N, K = _mnk_q4(codes, x, M, N, K)
-    st = lib().q4gemv_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(x),
-                          _addr(y), M, N, K, int(group), _stream(stream))
+    st = lib().q4gemv_run(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                          _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(x, "x", 4),
+                          _addr(y, "y", 4), M, N, K, int(group), _stream(stream))
     if check:
         _check(st, "q4gemv_run")
     return st
@@ -164,8 +173,10 @@ def q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M=None, N=None, K=None
 def q4gemv_fused_run(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M=None, N=None, K=None, group=32,
                      epilogue=Q4_EPILOGUE_NONE, stream=None, check=True) -> int:
     M, N, K = _mnk_q4(codes, x, M, N, K)
-    st = lib().q4gemv_fused_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(x), _addr(gamma),
-                                float(eps), _addr(y), M, N, K, int(group), int(epilogue), _stream(stream))
+    st = lib().q4gemv_fused_run(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                                _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(x, "x", 4),
+                                _addr(gamma, "gamma", 4), float(eps), _addr(y, "y", 4), M, N, K, int(group),
+                                int(epilogue), _stream(stream))
     if check:
         _check(st, "q4gemv_fused_run")
     return st
@@ -175,7 +186,8 @@ def q4_0_gemv_run(blocks, x, y, M=None, N=None, K=None, stream=None, check=True)
     M = int(x.shape[0] if M is None else M)
     K = int(x.shape[1] if K is None else K)
     N = int(blocks.shape[0] if N is None else N)
-    st = lib().q4_0_gemv_run(_addr(blocks), _addr(x), _addr(y), M, N, K, _stream(stream))
+    st = lib().q4_0_gemv_run(_addr(blocks, "blocks", 1), _addr(x, "x", 4), _addr(y, "y", 4), M, N, K,
+                             _stream(stream))
     if check:
         _check(st, "q4_0_gemv_run")
     return st
@@ -184,8 +196,9 @@ def q4_0_gemv_run(blocks, x, y, M=None, N=None, K=None, stream=None, check=True)
 def q4gemm_run(codes, scales_f16, zeros_u4_or_null, a_bf16, c, M=None, N=None, K=None, group=32,
                stream=None, check=True) -> int:
     M, N, K = _mnk_q4(codes, a_bf16, M, N, K)
-    st = lib().q4gemm_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null), _addr(a_bf16),
-                          _addr(c), M, N, K, int(group), _stream(stream))
+    st = lib().q4gemm_run(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                          _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(a_bf16, "a_bf16", 2),
+                          _addr(c, "c", 4), M, N, K, int(group), _stream(stream))
     if check:
         _check(st, "q4gemm_run")
     return st
@@ -195,7 +208,7 @@ def f32gemv_run(W, x, y, M=None, N=None, K=None, stream=None, check=True) -> int
     M = int(x.shape[0] if M is None else M)
     N = int(W.shape[0] if N is None else N)
     K = int(W.shape[1] if K is None else K)
-    st = lib().f32gemv_run(_addr(W), _addr(x), _addr(y), M, N, K, _stream(stream))
+    st = lib().f32gemv_run(_addr(W, "W", 4), _addr(x, "x", 4), _addr(y, "y", 4), M, N, K, _stream(stream))
     if check:
         _check(st, "f32gemv_run")
     return st
@@ -205,8 +218,9 @@ def q4_dequant_f32_run(codes, scales_f16, zeros_u4_or_null, w, N=None, K=None, g
                        stream=None, check=True) -> int:
     N = int(codes.shape[0] if N is None else N)
     K = int(codes.shape[1] * 2 if K is None else K)
-    st = lib().q4_dequant_f32_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null),
-                                  _addr(w), N, K, int(group), _stream(stream))
+    st = lib().q4_dequant_f32_run(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                                  _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(w, "w", 4),
+                                  N, K, int(group), _stream(stream))
     if check:
         _check(st, "q4_dequant_f32_run")
     return st
@@ -216,8 +230,9 @@ def q4_dequant_bf16_run(codes, scales_f16, zeros_u4_or_null, wb, N=None, K=None,
                         stream=None, check=True) -> int:
     N = int(codes.shape[0] if N is None else N)
     K = int(codes.shape[1] * 2 if K is None else K)
-    st = lib().q4_dequant_bf16_run(_addr(codes), _addr(scales_f16), _addr(zeros_u4_or_null),
-                                   _addr(wb), N, K, int(group), _stream(stream))
+    st = lib().q4_dequant_bf16_run(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                                   _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(wb, "wb", 2),
+                                   N, K, int(group), _stream(stream))
     if check:
         _check(st, "q4_dequant_bf16_run")
     return st
@@ -245,7 +260,7 @@ def q4gemv_set_overlapped_launch(enable: bool) -> int:
 
 def vec4_read_probe_run(buf, nbytes, partial, blocks=0, stream=None, check=True):
     used = _i32(0)
-    st = lib().vec4_read_probe_run(_addr(buf), int(nbytes), _addr(partial), int(blocks),
+    st = lib().vec4_read_probe_run(_addr(buf, "buf"), int(nbytes), _addr(partial, "partial", 4), int(blocks),
                                    ctypes.byref(used), _stream(stream))
     if check:
         _check(st, "vec4_read_probe_run")

@@ -168,3 +168,32 @@ def test_bounds_violations_query_without_checks(L):
     # the product library is built without -DQ4_BOUNDS_CHECK: the query answers -1 and
     # touches no device
     assert L.q4gemv_bounds_violations(None) == -1
+
+
+def test_binding_rejects_strided_and_mistyped_tensors(L):
+    # the binding's checks read tensor metadata only and raise before the library is
+    # called, so CPU tensors serve here and nothing is launched
+    torch = pytest.importorskip("torch")
+    codes = torch.zeros((8, 32), dtype=torch.uint8)
+    scales = torch.zeros((8, 2), dtype=torch.int16)
+    x = torch.zeros((1, 64), dtype=torch.float32)
+    y = torch.zeros((1, 8), dtype=torch.float32)
+    strided_x = torch.zeros((1, 128), dtype=torch.float32)[:, ::2]
+    with pytest.raises(ValueError, match="x: a contiguous tensor"):
+        q4.q4gemv_run(codes, scales, None, strided_x, y, 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="y: 4-byte elements"):
+        q4.q4gemv_run(codes, scales, None, x, y.to(torch.float64), 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="scales_f16: 2-byte elements"):
+        q4.q4gemv_run(codes, scales.to(torch.float32), None, x, y, 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="codes: 1-byte elements"):
+        q4.q4gemm_run(codes.to(torch.int16), scales, None, x.to(torch.bfloat16), y, 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="a_bf16: 2-byte elements"):
+        q4.q4gemm_run(codes, scales, None, x, y, 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="gamma: a contiguous tensor"):
+        q4.q4gemv_fused_run(codes, scales, None, x, strided_x[0], 1e-6, y, 1, 8, 64, 32)
+    with pytest.raises(ValueError, match="blocks: 1-byte elements"):
+        q4.q4_0_gemv_run(torch.zeros((8, 2, 9), dtype=torch.int16), x, y, 1, 8, 64)
+    with pytest.raises(ValueError, match="W: a contiguous tensor"):
+        q4.f32gemv_run(torch.zeros((64, 8), dtype=torch.float32).t(), x, y, 1, 8, 64)
+    with pytest.raises(ValueError, match="wb: 2-byte elements"):
+        q4.q4_dequant_bf16_run(codes, scales, None, torch.zeros((8, 64)), 8, 64, 32)
