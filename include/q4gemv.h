@@ -56,7 +56,7 @@ typedef enum {
     Q4_ERR_UNSUPPORTED = 2, /* valid but outside what a kernel serves (e.g. M > 16 in q4gemv_run) */
     Q4_ERR_MISALIGNED = 3,  /* a pointer violates the alignment stated above */
     Q4_ERR_CUDA = 4,        /* the CUDA runtime refused or failed a launch */
-    Q4_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (tensor-core path) */
+    Q4_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (mbarrier pipelines) */
 } q4_status;
 
 /* Byte sizes of one packed weight matrix (all byte counts). */

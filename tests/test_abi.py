@@ -7,6 +7,7 @@ pointer here is ever dereferenced.
 """
 import ctypes
 import os
+import subprocess
 
 import pytest
 
@@ -31,7 +32,6 @@ def test_library_exports_every_declared_function(L):
 
 
 def test_only_declared_functions_are_exported(L):
-    import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", q4.library_path()],
                          capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
@@ -39,7 +39,6 @@ def test_only_declared_functions_are_exported(L):
 
 
 def test_library_links_no_oracle():
-    import subprocess
     out = subprocess.run(["nm", "-D", q4.library_path()], capture_output=True, text=True).stdout
     assert "orc_" not in out
 
@@ -197,3 +196,18 @@ def test_binding_rejects_strided_and_mistyped_tensors(L):
         q4.f32gemv_run(torch.zeros((64, 8), dtype=torch.float32).t(), x, y, 1, 8, 64)
     with pytest.raises(ValueError, match="wb: 2-byte elements"):
         q4.q4_dequant_bf16_run(codes, scales, None, torch.zeros((8, 64)), 8, 64, 32)
+
+
+def test_plain_c_client_links_and_runs(L, tmp_path):
+    # the header is plain C (and valid C++); a C99 program that includes nothing else
+    # links the library and gets the documented results from the calls that need no GPU
+    inc = os.path.join(ROOT, "include")
+    libdir = os.path.dirname(q4.library_path())
+    exe = str(tmp_path / "abi_client")
+    subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", inc,
+                    os.path.join(ROOT, "tests", "abi_client.c"), "-o", exe, "-L", libdir, "-l:libq4gemv.so",
+                    "-Wl,-rpath," + libdir], check=True, capture_output=True, text=True)
+    subprocess.run(["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", "c++",
+                    os.path.join(inc, "q4gemv.h")], check=True, capture_output=True, text=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
