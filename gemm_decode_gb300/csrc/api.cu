@@ -70,7 +70,7 @@ int check_q4_args(const void *codes, const void *scales, int64_t N, int64_t K, i
 __device__ unsigned int g_bounds_violations = 0;
 
 unsigned int *bounds_counter() {
-    static unsigned int *addr[64] = {};
+    static std::atomic<unsigned int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     if (addr[dev] == nullptr) {

@@ -157,7 +157,7 @@ struct Plan {
 template <int MT, int L, bool SPLIT>
 int launch_one(const Plan &p, const F32Args &a, cudaStream_t stream) {
     auto kern = f32gemv_kernel<MT, L, SPLIT>;
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {

@@ -316,13 +316,13 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
 
 // ------------------------------------------------------------------ host side
 
-static unsigned long long g_timeout_ns = 1000ull * 1000 * 1000;   // 1 s per wait
+static std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};   // 1 s per wait
 
 unsigned long long gemm_wait_timeout_ns() { return g_timeout_ns; }
 
 // Address of the tensor-core status word, for kernels in other translation units.
 unsigned int *gemm_status_word() {
-    static unsigned int *addr[64] = {};
+    static std::atomic<unsigned int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     if (addr[dev] == nullptr) {
@@ -343,7 +343,7 @@ void set_gemm_wait_timeout_ns(unsigned long long ns) {
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
     if (fn == nullptr) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -379,7 +379,7 @@ size_t gemm_smem_bytes(int nh, int stages) {
 
 template <int NH, int STAGES>
 static int launch_tc(const CUtensorMap &map, const GemmArgs &g, int M, int64_t N, cudaStream_t stream) {
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = gemm_smem_bytes(NH, STAGES);

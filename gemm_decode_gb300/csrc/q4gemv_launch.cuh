@@ -11,7 +11,7 @@ template <int MT, int L, bool ASYM, bool SPLIT, bool FUSED = false, bool Q40 = f
 static int launch_gemv_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t stream) {
     auto kern = q4gemv_kernel<MT, L, ASYM, SPLIT, FUSED, Q40>;
     // Opt into the large shared-memory carve-out once per device.
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {

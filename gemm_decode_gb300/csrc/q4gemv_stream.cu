@@ -29,7 +29,7 @@ namespace q4 {
 __device__ unsigned int g_stream_status = 0;
 
 static unsigned int *stream_status_word() {
-    static unsigned int *addr[64] = {};
+    static std::atomic<unsigned int *> addr[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     if (addr[dev] == nullptr) {
@@ -88,7 +88,7 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
     return stream_geo_ok(g, asym);
 }
 
-static unsigned long long g_stream_timeout_ns = 1000ull * 1000 * 1000;
+static std::atomic<unsigned long long> g_stream_timeout_ns{1000ull * 1000 * 1000};
 void set_stream_wait_timeout_ns(unsigned long long ns) { g_stream_timeout_ns = ns; }
 
 // fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks)

@@ -394,7 +394,7 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
     auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM, FUSE>;
     const StreamGeo &g = a0.geo;
     const int T = g.TC + 32;
-    static int configured[64] = {};   // largest dynamic shared memory set so far, per device
+    static std::atomic<int> configured[64];   // largest dynamic shared memory set so far, per device
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && configured[dev] < g.SMEM) {

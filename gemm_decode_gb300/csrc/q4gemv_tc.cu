@@ -549,7 +549,7 @@ template <int MP, bool SPLIT, int TMV>
 static int launch_tc(const CUtensorMap &map, const TcArgs &g, cudaStream_t stream) {
     auto kern = q4gemv_tc_kernel<MP, SPLIT, TMV>;
     constexpr size_t smem = tc_smem_bytes<MP, TMV>();
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !configured[dev]) {

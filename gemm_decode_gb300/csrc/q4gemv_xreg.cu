@@ -384,7 +384,7 @@ template <int MT, bool ASYM, int CTP, int RG, int KC = 0, int G = 0, int U = kXr
 static int launch_one(const XregPlan &p, const XregArgsOf<FUSED> &a, cudaStream_t stream) {
     auto kern = q4gemv_xreg_kernel<MT, ASYM, CTP, RG, KC, G, U, D, FUSED>;
     constexpr int T = CTP * RG;
-    static bool configured[64] = {};
+    static std::atomic<bool> configured[64];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !configured[dev]) {
