@@ -401,6 +401,10 @@ def run_gpu(args, rank, world, local_rank):
                                                           stream)
         detail["q4_0_format"] = run_q40(args, torch, q4)
 
+    probe = detail.get("controls", {}).get("vec4_read_probe_1GiB", {}).get("gbs")
+    if probe:   # the same kernel's rate against this GPU's own streaming read (the vec4 probe)
+        roofline["frac_of_read_probe"] = round(roofline["achieved"] / probe, 4)
+        roofline["read_probe_gbs"] = probe
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
