@@ -54,6 +54,16 @@ MUTANTS = {
                          "int q = (e % 2 == 1) ? (byte & 0x0f) : (byte >> 4);"),
     "q40_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 18;",
                         "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 16;"),
+    "gemm_a_transposed": ("double p = w * (double)orc_bf16_to_f32(a_bf16[m * K + k]);",
+                          "double p = w * (double)orc_bf16_to_f32(a_bf16[k * M + m]);"),
+    "gemm_dropped_last_term": ("                double p = w * (double)orc_bf16_to_f32(a_bf16[m * K + k]);",
+                               "                double p = (k == K - 1) ? 0.0 : w * (double)orc_bf16_to_f32(a_bf16[m * K + k]);"),
+    "gemm_output_transposed": ("            c[m * N + n] = (float)acc;", "            c[n * M + m] = (float)acc;"),
+    "dequant_bf16_transposed": ("            wb[n * K + k] = orc_f32_to_bf16(", "            wb[k * N + n] = orc_f32_to_bf16("),
+    "f32_control_bound_of_w": ("                double p = (double)W[n * K + k] * (double)x[m * K + k];\n                acc += p;\n                mag += fabs(p);",
+                               "                double p = (double)W[n * K + k] * (double)x[m * K + k];\n                acc += p;\n                mag += fabs((double)W[n * K + k]);"),
+    "probe_sum_skips_last": ("    for (int64_t i = 0; i < n; ++i)\n        acc += (double)buf[i];",
+                             "    for (int64_t i = 0; i + 1 < n; ++i)\n        acc += (double)buf[i];"),
     "q80_unsigned_codes": ("    if (q >= 128)\n        q -= 256;\n", "\n"),
     "q80_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 34;",
                         "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 32;"),

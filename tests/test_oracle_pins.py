@@ -491,3 +491,22 @@ def test_q80_generator_layout():
     assert b.shape == (4, 2, 34) and b.dtype == np.uint8
     d = (b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)).view(np.float16).astype(np.float32)
     assert np.all((d >= 0.0003) & (d <= 0.00126))
+
+
+# ---------------------------------------------------------------------------
+# The read probe's reference: the binary64 sum of a binary32 buffer.
+# ---------------------------------------------------------------------------
+
+def test_probe_sum_closed_forms_and_exact_sum():
+    # 1 + 2 + ... + n is exact in binary64 and equals n (n + 1) / 2
+    for n in (1, 2, 5, 1000, 4097):
+        assert oracle.sum_f32(np.arange(1, n + 1, dtype=np.float32)) == n * (n + 1) / 2
+    assert oracle.sum_f32(np.zeros(0, np.float32)) == 0.0
+    # against the exactly rounded sum (math.fsum) within the binary64 accumulation error
+    buf = synth.uniform_f32(9, 100003)
+    exact = math.fsum(float(v) for v in buf)
+    assert abs(oracle.sum_f32(buf) - exact) <= len(buf) * 2.0 ** -52 * float(np.abs(buf).sum())
+    # a single large element placed last must be counted
+    buf = np.ones(64, np.float32)
+    buf[-1] = 1024.0
+    assert oracle.sum_f32(buf) == 63 + 1024
