@@ -64,6 +64,17 @@ MUTANTS = {
                                "                double p = (double)W[n * K + k] * (double)x[m * K + k];\n                acc += p;\n                mag += fabs((double)W[n * K + k]);"),
     "probe_sum_skips_last": ("    for (int64_t i = 0; i < n; ++i)\n        acc += (double)buf[i];",
                              "    for (int64_t i = 0; i + 1 < n; ++i)\n        acc += (double)buf[i];"),
+    "f16_inf_as_nan": ("        v = frac ? NAN : INFINITY;", "        v = NAN;"),
+    "f16_sign_dropped": ("    return (float)(sign ? -v : v);", "    return (float)v;"),
+    "bf16_widen_shift": ("    uint32_t u = (uint32_t)b << 16;", "    uint32_t u = (uint32_t)b << 15;"),
+    "bf16_round_down_always": ("    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))",
+                               "    if (0)"),
+    "bf16_nan_not_quiet": ("        return (uint16_t)((u >> 16) | 0x0040u);", "        return (uint16_t)(u >> 16);"),
+    "rmsnorm_sum_of_abs": ("            ss += v * v;", "            ss += fabs(v);"),
+    "rmsnorm_no_sqrt": ("double rms = sqrt(ss / (double)K + eps);", "double rms = ss / (double)K + eps;"),
+    "gemv_f64_bound_signed": ("                double p = w * x[m * K + k];\n                acc += p;\n                mag += fabs(p);",
+                              "                double p = w * x[m * K + k];\n                acc += p;\n                mag += p;"),
+    "q40_zero_point": ("    return (float)(q - 8) * orc_f16_to_f32(dbits);", "    return (float)(q - 7) * orc_f16_to_f32(dbits);"),
     "q80_unsigned_codes": ("    if (q >= 128)\n        q -= 256;\n", "\n"),
     "q80_block_pitch": ("const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 34;",
                         "const uint8_t *blk = blocks + (n * (K / 32) + k / 32) * 32;"),

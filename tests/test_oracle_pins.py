@@ -82,6 +82,19 @@ def test_bf16_rounding_against_torch():
         back, torch.from_numpy(ref[:500].view(np.int16)).view(torch.bfloat16).float().numpy())
 
 
+def test_bf16_nan_stays_nan():
+    # a NaN (signalling ones included: the bit patterns go to the routine unchanged) rounds
+    # to a bfloat16 NaN, never to an infinity, as torch's conversion does
+    import ctypes
+    L = oracle.lib()
+    for bits in (0x7F800001, 0x7FA00000, 0xFF800001, 0x7FC00000, 0x7FFFFFFF):
+        f = ctypes.c_float.from_buffer_copy(np.uint32(bits).tobytes())
+        out = L.orc_f32_to_bf16(f)
+        assert (out & 0x7F80) == 0x7F80 and (out & 0x7F) != 0, hex(bits)
+        ref = torch.from_numpy(np.array([bits], np.uint32).view(np.float32)).to(torch.bfloat16)
+        assert torch.isnan(ref).all()
+
+
 # ------------------------------------------------ definition via numpy routines
 
 def _random_integer_problem(seed, N, K, g, symmetric):
