@@ -99,3 +99,45 @@ def test_planted_mistake_is_caught(name, tmp_path):
                         os.path.join(HERE, "test_oracle_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+# Plausible slips in the Python layer of the oracle (row-subset offsets, the SwiGLU
+# pairing and tolerance).  The mutated source is executed over the real module's
+# namespace by a plugin loaded before the pin suite is collected.
+PY_MUTANTS = {
+    "rows_zero_pitch": ("                          None if zeros is None else _ptr(zeros, _u8p, n * zrow),\n"
+                        "                          _ptr(x, _f32p), M, 1, K, g, _ptr(yr, _f32p), _ptr(br, _f64p))",
+                        "                          None if zeros is None else _ptr(zeros, _u8p, n * (nb // 2)),\n"
+                        "                          _ptr(x, _f32p), M, 1, K, g, _ptr(yr, _f32p), _ptr(br, _f64p))"),
+    "gemm_rows_a_offset": ("_ptr(a_bf16, _u16p, int(m) * K), 1, 1, K, g,", "_ptr(a_bf16, _u16p, int(m) * (K // 2)), 1, 1, K, g,"),
+    "f32_rows_offset": ("lib().orc_f32_gemv(_ptr(W, _f32p, int(n) * K), _ptr(x, _f32p), M, 1, K,",
+                        "lib().orc_f32_gemv(_ptr(W, _f32p, int(n) * (K - 1)), _ptr(x, _f32p), M, 1, K,"),
+    "fused_pairs_swapped": ("        rows += [2 * i, 2 * i + 1]", "        rows += [2 * i + 1, 2 * i]"),
+    "fused_bound_drops_up_error": ("    bound = (SILU_SLOPE_MAX * bg * (np.abs(up) + bu) + (sg + SILU_SLOPE_MAX * bg) * bu",
+                                   "    bound = (SILU_SLOPE_MAX * bg * (np.abs(up) + bu) + 0 * bu"),
+    "fused_bound_drops_gate_error": ("    bound = (SILU_SLOPE_MAX * bg * (np.abs(up) + bu) + (sg + SILU_SLOPE_MAX * bg) * bu",
+                                     "    bound = ((sg + SILU_SLOPE_MAX * bg) * bu"),
+    "silu_slope_too_small": ("SILU_SLOPE_MAX = 1.1 ", "SILU_SLOPE_MAX = 1.0 "),
+    "q40_rows_pitch": ("    row_bytes = (K // 32) * 18", "    row_bytes = (K // 32) * 16"),
+    "q80_rows_pitch": ("    row_bytes = (K // 32) * 34", "    row_bytes = (K // 32) * 32"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_mistake_in_the_python_layer_is_caught(name, tmp_path):
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    old, new = PY_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    mutated = tmp_path / "mutated_oracle_source.py"
+    mutated.write_text(src.replace(old, new))
+    (tmp_path / "oracle_mutation_plugin.py").write_text(
+        "import sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import oracle\n"
+        f"exec(compile(open({str(mutated)!r}).read(), oracle.__file__, 'exec'), oracle.__dict__)\n")
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join([str(tmp_path), os.environ.get("PYTHONPATH", "")]))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        "-p", "oracle_mutation_plugin", os.path.join(HERE, "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert "passed" in r.stdout or "failed" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

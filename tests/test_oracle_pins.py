@@ -234,6 +234,24 @@ def test_sampled_rows_match_full():
     yt, bt = oracle.q4_gemv_threaded(w.codes, w.scales, w.zeros, x, 128, 3)
     np.testing.assert_array_equal(yt, y)
     np.testing.assert_array_equal(bt, b)
+    np.testing.assert_array_equal(br, b[:, rows])
+
+
+def test_sampled_matmul_and_control_elements_match_full():
+    # the element-sampling forms used at full sizes agree with the whole computation
+    w = synth.q4_weights(18, 40, 256, 64)
+    a = synth.activations_bf16(18, 5, 256)
+    c, cb = oracle.q4_gemm(w.codes, w.scales, w.zeros, a, 64)
+    ms, ns = [4, 0, 2], [39, 0, 17]
+    cs, csb = oracle.q4_gemm_rows(w.codes, w.scales, w.zeros, a, 64, ms, ns)
+    np.testing.assert_array_equal(cs, c[np.ix_(ms, ns)])
+    np.testing.assert_array_equal(csb, cb[np.ix_(ms, ns)])
+    W = synth.dense_f32(19, 30, 200)
+    x = synth.activations_f32(19, 3, 200)
+    y, yb = oracle.f32_gemv(W, x)
+    ys, ysb = oracle.f32_gemv_rows(W, x, [29, 3, 0])
+    np.testing.assert_array_equal(ys, y[:, [29, 3, 0]])
+    np.testing.assert_array_equal(ysb, yb[:, [29, 3, 0]])
 
 
 # ---------------------------------------------------------------- brute force
@@ -362,6 +380,37 @@ def test_fused_swiglu_pairs_even_rows_with_odd_rows():
     # the selected-outputs form agrees with the full one
     hs, _ = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-5, g, True, outputs=[4, 1])
     np.testing.assert_array_equal(hs, h[:, [4, 1]])
+
+
+def test_silu_slope_bound():
+    # the constant the SwiGLU tolerance uses bounds |d silu / dv| everywhere and is
+    # nearly attained (the maximum, about 1.0998, sits near v = 2.4)
+    v = np.linspace(-40.0, 40.0, 80001)
+    s = np.array([oracle.silu(t) for t in v])
+    slope = np.abs(np.diff(s) / np.diff(v))
+    assert slope.max() <= oracle.SILU_SLOPE_MAX
+    assert slope.max() >= oracle.SILU_SLOPE_MAX - 0.005
+    assert 2.3 < v[np.argmax(slope)] < 2.5
+
+
+def test_swiglu_tolerance_covers_every_pair_within_its_bounds():
+    # gate and up moved anywhere within their own GEMV bounds move silu(gate) * up by at
+    # most the stated SwiGLU bound (the mean value theorem with the slope bound above);
+    # the corners of the box are the extreme points of the product's second factor
+    N, K, g = 128, 256, 32
+    w = synth.q4_weights(47, N, K, g)
+    x = synth.activations_f32(48, 2, K)
+    gamma = np.random.default_rng(10).uniform(0.5, 1.5, K).astype(np.float32)
+    y, b = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-6, g, False)
+    h, bound = oracle.q4_gemv_fused(w.codes, w.scales, w.zeros, x, gamma, 1e-6, g, True)
+    gate, up, bg, bu = y[:, 0::2], y[:, 1::2], b[:, 0::2], b[:, 1::2]
+    worst = 0.0
+    r = np.random.default_rng(11)
+    for dg, du in [(-1, -1), (-1, 1), (1, -1), (1, 1), (0, 1), (1, 0)] + [tuple(t) for t in r.uniform(-1, 1, (8, 2))]:
+        moved = oracle.swiglu(gate + dg * bg, up + du * bu)
+        worst = max(worst, float(np.max(np.abs(moved - h) / bound)))
+    assert worst <= 1.0
+    assert worst >= 0.3    # the bound is not vacuous: some pair comes close to it
 
 
 # ---------------------------------------------------------------------------
