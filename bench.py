@@ -400,6 +400,7 @@ def run_gpu(args, rank, world, local_rank):
         detail["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas,
                                                           stream)
         detail["q4_0_format"] = run_q40(args, torch, q4)
+        detail["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream)
 
     probe = detail.get("controls", {}).get("vec4_read_probe_1GiB", {}).get("gbs")
     if probe:   # the same kernel's rate against this GPU's own streaming read (the vec4 probe)
@@ -1018,6 +1019,43 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
                 "gate|up (its output feeds down); the separate norm and activation launches this replaces "
                 "are not in the plain step"}
     return out
+
+
+def run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
+    """The same seven projections, each with its own x and y as in the timed step, issued
+    through q4gemv_grouped_run: the six K = 896 matrices (q, k, v, gate, up, LM head) as
+    one streamed launch in which each has CTAs of its own, down (K = 4864) as a second.
+    A CUDA graph of back-to-back steps over the replicas; the outputs are checked against
+    the separate calls' within the GEMV tolerance by the tests, not here."""
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in shapes]
+    byK = {}
+    for p, (_, N, K) in enumerate(shapes):
+        byK.setdefault(K, []).append(p)
+
+    def step(r):
+        for K, ps in byK.items():
+            q4.q4gemv_grouped_run([(*reps[r][p], xs[p], ys[p], shapes[p][1]) for p in ps], K, group, stream=stream)
+
+    n = max(replicas, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for r in range(replicas):
+            step(r)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            step(i % replicas)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    byts = step_bytes(shapes, 1, group)
+    return {"calls_per_step": len(byK), "groups": {str(K): [shapes[p][0] for p in ps] for K, ps in byK.items()},
+            "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
 
 
 def run_q40(args, torch, q4):

@@ -16,7 +16,8 @@ import threading
 
 __all__ = [
     "Q4Error", "lib", "library_path", "exported_names",
-    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4_0_gemv_run", "q4gemm_run", "f32gemv_run",
+    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run", "q4gemm_run",
+    "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
     "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
@@ -55,6 +56,11 @@ class _PackInfo(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class _Segment(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales_f16", ctypes.c_void_p), ("zeros_u4_or_null", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
 _lock = threading.Lock()
 _lib = None
 _vp, _i32, _i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
@@ -76,6 +82,7 @@ def lib() -> ctypes.CDLL:
                                            _i32, _i32, _vp]
             L.q4gemm_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
             L.q4_0_gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
+            L.q4gemv_grouped_run.argtypes = [ctypes.POINTER(_Segment), _i32, _i64, _i32, _vp]
             L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_status_string.argtypes = [ctypes.c_int]
             L.q4gemv_status_string.restype = ctypes.c_char_p
@@ -88,7 +95,8 @@ def lib() -> ctypes.CDLL:
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
             L.q4gemv_bounds_violations.argtypes = [_vp]
-            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4_0_gemv_run", "q4gemm_run", "f32gemv_run",
+            for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run",
+                      "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
                       "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations"):
@@ -179,6 +187,21 @@ def q4gemv_fused_run(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M=No
                                 int(epilogue), _stream(stream))
     if check:
         _check(st, "q4gemv_fused_run")
+    return st
+
+
+def q4gemv_grouped_run(segments, K, group=32, stream=None, check=True) -> int:
+    """segments: (codes, scales_f16, zeros_or_None, x, y[, N]) per matrix, M = 1 each;
+    N defaults to codes.shape[0]."""
+    arr = (_Segment * max(1, len(segments)))()
+    for i, sg in enumerate(segments):
+        codes, scales, zeros, x, y = sg[:5]
+        N = int(sg[5]) if len(sg) > 5 else int(codes.shape[0])
+        arr[i] = _Segment(_addr(codes, "codes", 1), _addr(scales, "scales_f16", 2), _addr(zeros, "zeros_u4_or_null", 1),
+                          _addr(x, "x", 4), _addr(y, "y", 4), N)
+    st = lib().q4gemv_grouped_run(arr, len(segments), int(K), int(group), _stream(stream))
+    if check:
+        _check(st, "q4gemv_grouped_run")
     return st
 
 

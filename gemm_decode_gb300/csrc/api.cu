@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "q4_common.cuh"
+#include "q4gemv_stream.cuh"
 
 namespace q4 {
 
@@ -158,6 +159,56 @@ int q4gemv_fused_run(const void *codes, const void *scales_f16, const void *zero
                                static_cast<const uint8_t *>(zeros_u4_or_null), x, gamma, eps,
                                epilogue == Q4_EPILOGUE_SWIGLU ? 1 : 0, y, M, N, static_cast<int>(K), group,
                                static_cast<cudaStream_t>(stream));
+}
+
+int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, int32_t group, void *stream) {
+    if (count < 0 || (count > 0 && segs == nullptr)) return Q4_ERR_INVALID_ARG;
+    int st = check_shape(1, 1, K, group);
+    if (st != Q4_OK) return st;
+    // every check before any launch
+    for (int32_t i = 0; i < count; ++i) {
+        const q4gemv_segment_t &sg = segs[i];
+        if (sg.N < 0) return Q4_ERR_INVALID_ARG;
+        if (sg.N == 0) continue;
+        if ((st = check_shape(1, sg.N, K, group)) != Q4_OK) return st;
+        if ((st = check_q4_args(sg.codes, sg.scales_f16, sg.N, K, group)) != Q4_OK) return st;
+        if (sg.x == nullptr || sg.y == nullptr) return Q4_ERR_INVALID_ARG;
+        if (!aligned(sg.x, 16) || !aligned(sg.y, 4)) return Q4_ERR_MISALIGNED;
+    }
+    // runs of up to kStreamMaxSeg non-empty matrices: one streamed launch where it applies,
+    // else one q4gemv_run per matrix
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t i = 0;
+    while (i < count) {
+        q4::StreamSeg run[q4::kStreamMaxSeg];
+        int32_t idx[q4::kStreamMaxSeg];
+        int n = 0;
+        for (; i < count && n < q4::kStreamMaxSeg; ++i) {
+            const q4gemv_segment_t &sg = segs[i];
+            if (sg.N == 0) continue;
+            run[n].codes = static_cast<const uint8_t *>(sg.codes);
+            run[n].scales = static_cast<const uint16_t *>(sg.scales_f16);
+            run[n].zeros = static_cast<const uint8_t *>(sg.zeros_u4_or_null);
+            run[n].x = sg.x;
+            run[n].y = sg.y;
+            run[n].N = sg.N;
+            run[n].nblocks = 0;
+            run[n].cta_begin = 0;
+            idx[n++] = i;
+        }
+        if (n == 0) break;
+        if (q4::stream_grouped_applies(run, n, static_cast<int>(K), group)) {
+            st = q4::launch_q4gemv_stream_grouped(run, n, static_cast<int>(K), group, s);
+            if (st != Q4_OK) return st;
+            continue;
+        }
+        for (int j = 0; j < n; ++j) {
+            const q4gemv_segment_t &sg = segs[idx[j]];
+            st = q4gemv_run(sg.codes, sg.scales_f16, sg.zeros_u4_or_null, sg.x, sg.y, 1, sg.N, K, group, stream);
+            if (st != Q4_OK) return st;
+        }
+    }
+    return Q4_OK;
 }
 
 int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K, void *stream) {

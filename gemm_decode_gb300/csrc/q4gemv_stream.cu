@@ -49,6 +49,11 @@ int launch_stream_k2048(const StreamArgs &a, int group, bool asym, int fuse, cud
 int launch_stream_k4096(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_k8192(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_k16384(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_grouped_k896(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_grouped_k2048(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_grouped_k4096(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_grouped_k8192(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_grouped_k16384(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 
 // ------------------------------------------------------------------ host side
 
@@ -160,6 +165,101 @@ bool stream_q40_applies(int M, int64_t N, int K, const void *blocks) {
 
 int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream) {
     return launch_stream_any(blocks, nullptr, nullptr, x, nullptr, 0.0f, 0, 4, y, N, K, 32, stream);
+}
+
+// ---- grouped launches (several matrices of the same K, one launch) ----
+
+bool stream_grouped_applies(const StreamSeg *segs, int nseg, int K, int group) {
+    if (nseg < 1 || nseg > kStreamMaxSeg) return false;
+    if (group != 32 && group != 64 && group != 128) return false;
+    if (K != 896 && K != 2048 && K != 4096 && K != 8192 && K != 16384) return false;   // compile-time geometries
+    const bool asym = segs[0].zeros != nullptr;
+    const int rg = stream_rg(K);
+    if (rg == 0) return false;
+    const int u = stream_u(K);
+    const StreamGeo g = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);
+    if (!stream_geo_ok(g, asym)) return false;
+    int64_t blocks = 0;
+    for (int i = 0; i < nseg; ++i) {
+        const StreamSeg &sg = segs[i];
+        if (sg.N < 1 || (sg.zeros != nullptr) != asym) return false;
+        if (!aligned(sg.codes, 16) || !aligned(sg.scales, 16) || (asym && !aligned(sg.zeros, 16))) return false;
+        blocks += (sg.N + g.ROWS - 1) / g.ROWS;
+    }
+    // short rows: at least one block of rows per SM over the whole group, as for one matrix
+    if (K < 2048 && blocks < device_info().sms) return false;
+    return blocks < (int64_t(1) << 30);
+}
+
+int stream_assign_ctas(StreamGroupArgs &a, int grid_max) {
+    const int rows = a.geo.ROWS;
+    int64_t total = 0;
+    for (int i = 0; i < a.nseg; ++i) {
+        a.seg[i].nblocks = static_cast<int>((a.seg[i].N + rows - 1) / rows);
+        total += a.seg[i].nblocks;
+    }
+    int c[kStreamMaxSeg] = {};
+    int grid = 0;
+    if (total <= grid_max) {   // a CTA per block of rows
+        for (int i = 0; i < a.nseg; ++i) {
+            c[i] = a.seg[i].nblocks;
+            grid += c[i];
+        }
+    } else {
+        // one CTA each, then one at a time to the matrix with the most blocks per CTA
+        // (which minimises the largest share any CTA gets)
+        for (int i = 0; i < a.nseg; ++i) c[i] = 1;
+        grid = a.nseg;
+        while (grid < grid_max) {
+            int best = -1;
+            for (int i = 0; i < a.nseg; ++i)
+                if (c[i] < a.seg[i].nblocks &&
+                    (best < 0 || static_cast<int64_t>(a.seg[i].nblocks) * c[best] >
+                                     static_cast<int64_t>(a.seg[best].nblocks) * c[i]))
+                    best = i;
+            if (best < 0) break;
+            ++c[best];
+            ++grid;
+        }
+    }
+    int begin = 0;
+    for (int i = 0; i < a.nseg; ++i) {
+        a.seg[i].cta_begin = begin;
+        begin += c[i];
+    }
+    return grid;
+}
+
+int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int group, cudaStream_t stream) {
+    if (!stream_grouped_applies(segs, nseg, K, group)) return Q4_ERR_UNSUPPORTED;
+    const bool asym = segs[0].zeros != nullptr;
+    StreamGroupArgs a{};
+    a.codes = segs[0].codes;   // (the base fields are unused by the grouped instances)
+    a.scales = segs[0].scales;
+    a.zeros = segs[0].zeros;
+    a.x = segs[0].x;
+    a.y = segs[0].y;
+    a.N = segs[0].N;
+    a.nblocks = 0;
+    a.timeout_ns = g_stream_timeout_ns;
+    a.status = stream_status_word();
+    a.bounds = bounds_counter();
+    a.gamma = nullptr;
+    a.eps = 0.0f;
+    a.swiglu = 0;
+    if (a.status == nullptr) return Q4_ERR_CUDA;
+    const int rg = stream_rg(K), u = stream_u(K);
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym), asym);
+    a.nseg = nseg;
+    for (int i = 0; i < nseg; ++i) a.seg[i] = segs[i];
+    switch (K) {
+        case 896: return launch_stream_grouped_k896(a, group, asym, stream);
+        case 2048: return launch_stream_grouped_k2048(a, group, asym, stream);
+        case 4096: return launch_stream_grouped_k4096(a, group, asym, stream);
+        case 8192: return launch_stream_grouped_k8192(a, group, asym, stream);
+        case 16384: return launch_stream_grouped_k16384(a, group, asym, stream);
+        default: return Q4_ERR_UNSUPPORTED;
+    }
 }
 
 int read_and_clear_stream_status(unsigned int *v) {

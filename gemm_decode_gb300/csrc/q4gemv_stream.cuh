@@ -1,6 +1,8 @@
 // q4gemv_stream.cuh -- launch interface of the TMA-streamed M = 1 int4 GEMV.
 #pragma once
 
+#include <type_traits>
+
 #include "q4_common.cuh"
 
 namespace q4 {
@@ -104,6 +106,29 @@ struct StreamArgs {
     StreamGeo geo;                   // used when the instance does not fix K and g
 };
 
+// Grouped launches: several matrices of the same K and group (each with its own x and y,
+// M = 1) streamed by one launch.  Every CTA serves one matrix: matrix s owns the CTAs
+// [cta_begin, next cta_begin) and splits its blocks of rows over them as a single
+// launch would, so a CTA encodes one x and never switches.
+constexpr int kStreamMaxSeg = 8;
+struct StreamSeg {
+    const uint8_t *codes;
+    const uint16_t *scales;
+    const uint8_t *zeros;
+    const float *x;
+    float *y;
+    int64_t N;
+    int nblocks;     // blocks of rows of this matrix
+    int cta_begin;   // first CTA of this matrix
+};
+struct StreamGroupArgs : StreamArgs {
+    StreamSeg seg[kStreamMaxSeg];
+    int nseg;
+};
+// The kernel's argument type: the grouped instances (FUSE bit 3) take the segment table.
+template <int FUSE>
+using StreamArgsOf = std::conditional_t<(FUSE & 8) != 0, StreamGroupArgs, StreamArgs>;
+
 // True when the streamed kernel serves this problem (M = 1, enough rows, a row
 // geometry whose blocks are whole warps and 16-byte multiples, 16-byte aligned
 // arrays, and a carve-up that fits the shared memory of one CTA).
@@ -117,6 +142,14 @@ int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, con
 // Q4_0 blocks (q4_0_gemv_run): whether the streamed kernel serves the problem, and the launch.
 bool stream_q40_applies(int M, int64_t N, int K, const void *blocks);
 int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream);
+// Grouped: whether one streamed launch serves these matrices (same K and group, all with or
+// all without zero points, every one streamable on its own alignment), and the launch.
+bool stream_grouped_applies(const StreamSeg *segs, int nseg, int K, int group);
+// Shares out at most grid_max CTAs over the matrices of a (sets every nblocks and
+// cta_begin; each matrix gets at least one CTA and at most one per block of rows, the
+// rest go where the blocks per CTA are highest) and returns the grid.
+int stream_assign_ctas(StreamGroupArgs &a, int grid_max);
+int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int group, cudaStream_t stream);
 void set_stream_wait_timeout_ns(unsigned long long ns);
 int read_and_clear_stream_status(unsigned int *v);
 

@@ -36,13 +36,15 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 // reduction are those of the plain kernel; bit 1, the SwiGLU epilogue when a.swiglu is
 // set -- the gate / up row pairs leave silu(gate) * up.  FUSE = 4: the weights are Q4_0
 // blocks (a.codes; 18 bytes per 32 codes: binary16 scale, then the codes; zero point 8).
+// FUSE = 8: a grouped launch (a.seg: several matrices, each served by its own CTAs).
 template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
-q4gemv_stream_kernel(const StreamArgs a) {
+q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
-    constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0, Q40 = (FUSE & 4) != 0;
+    constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0, Q40 = (FUSE & 4) != 0, GROUPED = (FUSE & 8) != 0;
     static_assert(!Q40 || (!ASYM && (KC == 0 || GC == 32) && FUSE == 4), "Q4_0: group 32, symmetric, not fused");
+    static_assert(!GROUPED || FUSE == 8, "grouped launches are plain");
     const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40>(a.geo);
     const int D = G.D;
     const int C = G.C;
@@ -62,10 +64,37 @@ q4gemv_stream_kernel(const StreamArgs a) {
     const int warp = tid >> 5, lane = tid & 31;
     const unsigned long long limit = a.timeout_ns;
 
+    // the matrix this CTA serves (a grouped launch: the segment whose CTA range holds it)
+    const uint8_t *w_codes = a.codes;
+    const uint16_t *w_scales = a.scales;
+    const uint8_t *w_zeros = a.zeros;
+    const float *w_x = a.x;
+    float *w_y = a.y;
+    int64_t w_N = a.N;
+    int w_nblocks = a.nblocks;
+    int cta = static_cast<int>(blockIdx.x), gsz = static_cast<int>(gridDim.x);
+    if constexpr (GROUPED) {
+        int first = 0, last = gsz;
+#pragma unroll
+        for (int g = 0; g < kStreamMaxSeg; ++g) {
+            if (g < a.nseg && a.seg[g].cta_begin <= cta) {
+                w_codes = a.seg[g].codes;
+                w_scales = a.seg[g].scales;
+                w_zeros = a.seg[g].zeros;
+                w_x = a.seg[g].x;
+                w_y = a.seg[g].y;
+                w_N = a.seg[g].N;
+                w_nblocks = a.seg[g].nblocks;
+                first = a.seg[g].cta_begin;
+                last = g + 1 < a.nseg ? a.seg[g + 1].cta_begin : gsz;
+            }
+        }
+        cta -= first;
+        gsz = last - first;
+    }
     // blocks of this CTA (contiguous range)
-    const int gsz = static_cast<int>(gridDim.x);
-    const int b_begin = static_cast<int>(static_cast<int64_t>(a.nblocks) * blockIdx.x / gsz);
-    const int b_end = static_cast<int>(static_cast<int64_t>(a.nblocks) * (blockIdx.x + 1) / gsz);
+    const int b_begin = static_cast<int>(static_cast<int64_t>(w_nblocks) * cta / gsz);
+    const int b_end = static_cast<int>(static_cast<int64_t>(w_nblocks) * (cta + 1) / gsz);
     const int nbk = b_end - b_begin;
 
     if (tid == 0) {
@@ -101,18 +130,18 @@ q4gemv_stream_kernel(const StreamArgs a) {
                     break;
                 }
                 const int64_t row0 = static_cast<int64_t>(b_begin + i) * G.ROWS;
-                const int rows = static_cast<int>(a.N - row0 < G.ROWS ? a.N - row0 : G.ROWS);
+                const int rows = static_cast<int>(w_N - row0 < G.ROWS ? w_N - row0 : G.ROWS);
                 const uint32_t dst = s_ring + s * G.SLOT_B;
-                const unsigned char *src_c = a.codes + row0 * (C * 16);
-                const unsigned char *src_s = reinterpret_cast<const unsigned char *>(a.scales) + row0 * (G.NB * 2);
-                const unsigned char *src_z = ASYM ? a.zeros + row0 * G.ZROW : nullptr;
-                if (!ib(row0 >= 0 && rows >= 1 && row0 + rows <= a.N && s < D)) {
+                const unsigned char *src_c = w_codes + row0 * (C * 16);
+                const unsigned char *src_s = reinterpret_cast<const unsigned char *>(w_scales) + row0 * (G.NB * 2);
+                const unsigned char *src_z = ASYM ? w_zeros + row0 * G.ZROW : nullptr;
+                if (!ib(row0 >= 0 && rows >= 1 && row0 + rows <= w_N && s < D)) {
                     mbar_arrive(full(s));   // (checking builds) keep the ring moving, copy nothing
                 } else if constexpr (Q40) {
                     // Q4_0: one stretch of rows * C * 18 bytes (a 16-byte multiple for a whole
                     // block of rows); its largest 16-byte multiple by bulk copy, the at most
                     // 15 bytes left by plain copies, published by the arrive below
-                    const unsigned char *src = a.codes + row0 * (C * 18);
+                    const unsigned char *src = w_codes + row0 * (C * 18);
                     const int cb = rows * C * 18, cb16 = cb & ~15;
                     unsigned char *sl = smem + G.OFF_RING + s * G.SLOT_B;
                     for (int j = cb16; j < cb; ++j) sl[j] = src[j];
@@ -169,7 +198,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             for (int base = 0; base < C; base += G.TC / 4) {
                 const int i = base + (tid >> 2);
                 if (i < C && ib((i + 1) * 32 <= C * 32)) {
-                    const float4 *xc = reinterpret_cast<const float4 *>(a.x + i * 32) + 2 * (tid & 3);
+                    const float4 *xc = reinterpret_cast<const float4 *>(w_x + i * 32) + 2 * (tid & 3);
                     const float4 u = xc[0], v = xc[1];
                     ssq = fmaf(u.x, u.x, fmaf(u.y, u.y, fmaf(u.z, u.z, fmaf(u.w, u.w, ssq))));
                     ssq = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ssq))));
@@ -187,7 +216,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 const int i = base + (tid >> 2);
                 const bool in_range = i < C;
                 const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-                encode_chunk4_gamma_scaled(a.x + (in_range ? i : 0) * 32, a.gamma + (in_range ? i : 0) * 32, rnorm,
+                encode_chunk4_gamma_scaled(w_x + (in_range ? i : 0) * 32, a.gamma + (in_range ? i : 0) * 32, rnorm,
                                            in_range && x_ok, in_range, planes + (in_range ? i : 0) * kPlaneWords,
                                            tid & 3);
             }
@@ -196,7 +225,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 const int i = base + (tid >> 2);
                 const bool in_range = i < C;
                 const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-                encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+                encode_chunk4(w_x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
                               planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
             }
         }
@@ -205,7 +234,7 @@ q4gemv_stream_kernel(const StreamArgs a) {
             const int i = base + (tid >> 2);
             const bool in_range = i < C;
             const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-            encode_chunk4(a.x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+            encode_chunk4(w_x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
                           planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
         }
     }
@@ -263,12 +292,12 @@ q4gemv_stream_kernel(const StreamArgs a) {
                 if (a.swiglu) {
                     // row rho + 1 (the up row of the pair) sits ql lanes further on
                     const float up = __shfl_xor_sync(0xffffffffu, acc, ql);
-                    if (mine && q == 0 && (rho & 1) == 0 && row0 + rho + 1 < a.N)
-                        a.y[(row0 + rho) >> 1] = acc / (1.0f + expf(-acc)) * up;
+                    if (mine && q == 0 && (rho & 1) == 0 && row0 + rho + 1 < w_N)
+                        w_y[(row0 + rho) >> 1] = acc / (1.0f + expf(-acc)) * up;
                     continue;
                 }
             }
-            if (mine && q == 0 && row0 + rho < a.N) a.y[row0 + rho] = acc;
+            if (mine && q == 0 && row0 + rho < w_N) w_y[row0 + rho] = acc;
         }
     };
 
@@ -433,6 +462,55 @@ int launch_stream(const StreamArgs &a0, cudaStream_t stream) {
 }
 
 
+// A grouped launch: the CTAs a full grid holds (resident CTAs per SM x SMs) are shared out
+// over the matrices (stream_assign_ctas), then one launch serves them all.
+template <int KC, int GC, int RGC, int UC, bool ASYM>
+int launch_stream_grouped(StreamGroupArgs &a, cudaStream_t stream) {
+    auto kern = q4gemv_stream_kernel<KC, GC, RGC, UC, ASYM, 8>;
+    const StreamGeo &g = a.geo;
+    const int T = g.TC + 32;
+    static std::atomic<int> configured[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && configured[dev] < g.SMEM) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             device_info().smem_optin);
+        if (e != cudaSuccess) {
+            set_cuda_error(e);
+            return Q4_ERR_CUDA;
+        }
+        configured[dev] = device_info().smem_optin;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T, g.SMEM);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    if (per_sm < 1) return Q4_ERR_UNSUPPORTED;
+    const int grid = stream_assign_ctas(a, per_sm * device_info().sms);
+    if (grid < 1) return Q4_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(T), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(g.SMEM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    add_overlap_attr(cfg, attr);
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const StreamGroupArgs &>(a));
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+template <int KV, int GV, int RGV>
+int launch_stream_grouped_kg(StreamGroupArgs &a, bool asym, cudaStream_t s) {
+    constexpr int UV = stream_u(KV);
+    return asym ? launch_stream_grouped<KV, GV, RGV, UV, true>(a, s) : launch_stream_grouped<KV, GV, RGV, UV, false>(a, s);
+}
+
 template <int KV, int GV, int RGV>
 int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
     constexpr int UV = stream_u(KV);
@@ -449,13 +527,21 @@ int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
 }
 
 // One translation unit per K instantiates the compile-time geometries of that K (plain,
-// RMSNorm, RMSNorm + SwiGLU).
+// RMSNorm, RMSNorm + SwiGLU, Q4_0, grouped).
 #define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
     int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s) {    \
         switch (group) {                                                                              \
             case 32: return launch_stream_kg<KV, 32, RGV>(a, asym, fuse, s);                          \
             case 64: return launch_stream_kg<KV, 64, RGV>(a, asym, fuse, s);                          \
             case 128: return launch_stream_kg<KV, 128, RGV>(a, asym, fuse, s);                        \
+            default: return Q4_ERR_UNSUPPORTED;                                                       \
+        }                                                                                             \
+    }                                                                                                 \
+    int launch_stream_grouped_k##KV(StreamGroupArgs &a, int group, bool asym, cudaStream_t s) {       \
+        switch (group) {                                                                              \
+            case 32: return launch_stream_grouped_kg<KV, 32, RGV>(a, asym, s);                        \
+            case 64: return launch_stream_grouped_kg<KV, 64, RGV>(a, asym, s);                        \
+            case 128: return launch_stream_grouped_kg<KV, 128, RGV>(a, asym, s);                      \
             default: return Q4_ERR_UNSUPPORTED;                                                       \
         }                                                                                             \
     }

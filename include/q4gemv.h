@@ -120,6 +120,31 @@ Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const voi
                      const float *x, const float *gamma, float eps, float *y, int32_t M, int64_t N,
                      int64_t K, int32_t group, int32_t epilogue, void *stream);
 
+/* One matrix of a grouped GEMV: its packed weights (as for q4gemv_run), its own input
+ * x[K] (device, 16-byte aligned) and output y[N] (device, 4-byte aligned), N >= 0 rows
+ * (N == 0: skipped, pointers unused). */
+typedef struct {
+    const void *codes;
+    const void *scales_f16;
+    const void *zeros_u4_or_null;
+    const float *x;
+    float *y;
+    int64_t N;
+} q4gemv_segment_t;
+
+/* Several M = 1 GEMVs of the same K and group, y_i = W_i x_i, issued as few launches as
+ * possible (gerbil GPU-engine kernel reference, section "2. MatMul", its optimisation
+ * notes: batch the small Q, K, V projections into one kernel; cera wgpu_gemv_bench.rs,
+ * its note on sharing one compute pass: every boundary between dispatches costs time of
+ * its own).  Runs of up to 8 matrices that the TMA-streamed kernel serves (K in {896,
+ * 2048, 4096, 8192, 16384}; all with or all without zero points; codes, scales and zeros
+ * 16-byte aligned) are one launch, in which each matrix gets its own CTAs in proportion
+ * to its rows; any other matrix runs as its own q4gemv_run.  The outputs equal those of
+ * separate calls within the GEMV's tolerance.  segs: host array of count entries (read
+ * during the call only).  Every entry is checked as q4gemv_run checks its arguments
+ * before anything is launched.  Asynchronous; allocates nothing. */
+Q4_API int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, int32_t group, void *stream);
+
 /* GEMV over a second weight format, Q4_0 blocks (cera wgpu_gemv_bench.rs, block
  * geometry: Q4_0 holds 32 elements in 18 bytes), 1 <= M <= 16:
  * y[m][n] = sum_k (q[n][k] - 8) * d[n][k/32] * x[m][k].

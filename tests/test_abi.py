@@ -117,6 +117,21 @@ def test_fused_gemv_argument_checks(L):
     assert r(A, A, None, A + 4, A, 1e-6, A, 1, 64, 64, 32, NONE, None) == q4.Q4_ERR_MISALIGNED
 
 
+def test_grouped_argument_checks(L):
+    r = L.q4gemv_grouped_run
+    S = q4._Segment
+    assert r(None, 0, 896, 32, None) == q4.Q4_OK
+    assert r(None, 2, 896, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r((S * 1)(S(A, A, None, A, A, 4)), -1, 896, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r((S * 1)(S(A, A, None, A, A, 4)), 1, 96, 64, None) == q4.Q4_ERR_INVALID_ARG     # K % g != 0
+    assert r((S * 1)(S(A, A, None, A, A, -1)), 1, 896, 32, None) == q4.Q4_ERR_INVALID_ARG
+    assert r((S * 1)(S(None, None, None, None, None, 0)), 1, 896, 32, None) == q4.Q4_OK    # empty entry
+    assert r((S * 1)(S(A, A, None, None, A, 4)), 1, 896, 32, None) == q4.Q4_ERR_INVALID_ARG
+    # a bad entry anywhere rejects the whole call before any launch
+    assert r((S * 2)(S(A, A, None, A, A, 4), S(A, A, None, A + 4, A, 4)), 2, 896, 32, None) == q4.Q4_ERR_MISALIGNED
+    assert r((S * 2)(S(A, A, None, A, A, 4), S(A + 8, A, None, A, A, 4)), 2, 896, 32, None) == q4.Q4_ERR_MISALIGNED
+
+
 def test_q40_argument_checks(L):
     r = L.q4_0_gemv_run
     assert r(A, A, A, 1, 64, 48, None) == q4.Q4_ERR_INVALID_ARG      # K not a multiple of 32

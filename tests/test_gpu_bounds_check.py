@@ -115,3 +115,20 @@ def test_q40_streamed_kernel(torch, N, K):
     rows = sorted(set(np.random.default_rng(3).choice(N, 64, replace=False).tolist()) | {0, N - 1})
     y_ref, bound = oracle.q40_gemv_rows(blocks, x, rows)
     assert_within_bound(host(y)[:, rows], y_ref, bound, f"Q4_0 bounds N={N} K={K}")
+
+
+@pytest.mark.parametrize("K,g", [(896, 32), (4096, 128)])
+def test_grouped_streamed_kernel(torch, K, g):
+    # several matrices in one streamed launch, each with its own CTAs, x and y; partial
+    # last blocks and a matrix smaller than one block
+    specs = [4099, 37, 1, 9001]
+    ws = [synth.q4_weights(K + N, N, K, g, tag="bounds-grouped") for N in specs]
+    xs = [synth.activations_f32(N + 5, 1, K) for N in specs]
+    ys = [torch.full((1, N), float("nan"), dtype=torch.float32, device="cuda") for N in specs]
+    segs = [(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y, w.N)
+            for w, x, y in zip(ws, xs, ys)]
+    q4.q4gemv_grouped_run(segs, K, g)
+    assert q4.q4gemv_bounds_violations() == 0, f"grouped K={K}: out-of-range accesses counted"
+    for w, x, y in zip(ws, xs, ys):
+        y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, g)
+        assert_within_bound(host(y), y_ref, bound, f"grouped K={K} N={w.N}")
