@@ -400,7 +400,10 @@ def run_gpu(args, rank, world, local_rank):
         detail["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas,
                                                           stream)
         detail["q4_0_format"] = run_q40(args, torch, q4)
-        detail["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream)
+        try:   # a detail figure: its failure is recorded, the measured step stands
+            detail["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream)
+        except Exception as e:   # noqa: BLE001
+            detail["grouped_step"] = {"error": f"{type(e).__name__}: {e}"}
 
     probe = detail.get("controls", {}).get("vec4_read_probe_1GiB", {}).get("gbs")
     if probe:   # the same kernel's rate against this GPU's own streaming read (the vec4 probe)
