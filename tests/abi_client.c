@@ -51,6 +51,15 @@ int main(void)
     expect(q4gemm_run(A, A, NULL, A, F, 1, 64, 100, 32, NULL) == Q4_ERR_INVALID_ARG, "gemm K % g != 0");
     expect(f32gemv_run(F, F, F, 17, 64, 64, NULL) == Q4_ERR_UNSUPPORTED, "f32 M > 16");
 
+    {
+        q4gemv_segment_t segs[2] = {{A, A, NULL, F, F, 64}, {A, A, NULL, (const float *)((char *)A + 4), F, 64}};
+        expect(q4gemv_grouped_run(segs, 2, 896, 32, NULL) == Q4_ERR_MISALIGNED, "grouped: x 4 B off");
+        expect(q4gemv_grouped_run(NULL, 0, 896, 32, NULL) == Q4_OK, "grouped: empty list");
+        expect(q4gemv_grouped_run(NULL, 1, 896, 32, NULL) == Q4_ERR_INVALID_ARG, "grouped: null list");
+        segs[1].N = 0;   /* an empty entry is skipped, but the first still fails on K % g */
+        expect(q4gemv_grouped_run(segs, 2, 100, 32, NULL) == Q4_ERR_INVALID_ARG, "grouped: K % g != 0");
+    }
+
     /* empty problems: Q4_OK, pointers unused */
     expect(q4gemv_run(NULL, NULL, NULL, NULL, NULL, 0, 64, 64, 32, NULL) == Q4_OK, "M = 0");
     expect(q4gemv_run(NULL, NULL, NULL, NULL, NULL, 3, 0, 64, 32, NULL) == Q4_OK, "N = 0");
