@@ -21,7 +21,7 @@ __all__ = [
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
     "q4gemv_device_status", "q4gemm_set_wait_timeout_ns", "q4gemv_set_overlapped_launch",
-    "q4gemv_bounds_violations",
+    "q4gemv_bounds_violations", "q4gemv_grouped_split",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
     "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT", "Q4_EPILOGUE_NONE", "Q4_EPILOGUE_SWIGLU",
 ]
@@ -95,11 +95,13 @@ def lib() -> ctypes.CDLL:
             L.q4gemm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
             L.q4gemv_set_overlapped_launch.argtypes = [ctypes.c_int]
             L.q4gemv_bounds_violations.argtypes = [_vp]
+            L.q4gemv_grouped_split.argtypes = [ctypes.POINTER(_i64), _i32, _i64, _i32, _i32,
+                                               ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run",
                       "q4gemm_run", "f32gemv_run",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
-                      "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations"):
+                      "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations", "q4gemv_grouped_split"):
                 getattr(L, f).restype = ctypes.c_int
             _lib = L
         return _lib
@@ -274,6 +276,19 @@ def q4gemv_bounds_violations(stream=None) -> int:
     """Out-of-range accesses counted since the last call (bounds-checking builds), -1
     in a library built without the checks."""
     return lib().q4gemv_bounds_violations(_stream(stream) if stream is not None else None)
+
+
+def q4gemv_grouped_split(Ns, K, group, grid_max):
+    """Host-only test export: (grid, nblocks per matrix, first CTA per matrix) of the CTA
+    split a grouped launch makes; raises Q4Error on a negated status."""
+    n = len(Ns)
+    arr = (_i64 * max(1, n))(*[int(v) for v in Ns])
+    nb = (_i32 * max(1, n))()
+    cb = (_i32 * max(1, n))()
+    grid = lib().q4gemv_grouped_split(arr, n, int(K), int(group), int(grid_max), nb, cb)
+    if grid < 0:
+        raise Q4Error(-grid, "q4gemv_grouped_split")
+    return grid, list(nb[:n]), list(cb[:n])
 
 
 def q4gemv_set_overlapped_launch(enable: bool) -> int:

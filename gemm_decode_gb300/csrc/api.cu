@@ -211,6 +211,14 @@ int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, i
     return Q4_OK;
 }
 
+int q4gemv_grouped_split(const int64_t *N, int32_t count, int64_t K, int32_t group, int32_t grid_max,
+                         int32_t *nblocks, int32_t *cta_begin) {
+    if (N == nullptr || nblocks == nullptr || cta_begin == nullptr || count < 1) return -Q4_ERR_INVALID_ARG;
+    const int st = check_shape(1, 1, K, group);
+    if (st != Q4_OK) return -st;
+    return q4::stream_grouped_split(N, count, static_cast<int>(K), group, grid_max, nblocks, cta_begin);
+}
+
 int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K, void *stream) {
     if (M < 0 || N < 0 || K < 32 || K % 32 != 0) return Q4_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return Q4_OK;

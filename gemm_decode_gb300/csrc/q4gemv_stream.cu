@@ -230,6 +230,25 @@ int stream_assign_ctas(StreamGroupArgs &a, int grid_max) {
     return grid;
 }
 
+int stream_grouped_split(const int64_t *N, int count, int K, int group, int grid_max, int *nblocks, int *cta_begin) {
+    const int rg = stream_rg(K);
+    if (rg == 0 || count < 1 || count > kStreamMaxSeg || grid_max < count) return -Q4_ERR_UNSUPPORTED;
+    StreamGroupArgs a{};
+    const int u = stream_u(K);
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, true), true);
+    a.nseg = count;
+    for (int i = 0; i < count; ++i) {
+        if (N[i] < 1) return -Q4_ERR_INVALID_ARG;
+        a.seg[i].N = N[i];
+    }
+    const int grid = stream_assign_ctas(a, grid_max);
+    for (int i = 0; i < count; ++i) {
+        nblocks[i] = a.seg[i].nblocks;
+        cta_begin[i] = a.seg[i].cta_begin;
+    }
+    return grid;
+}
+
 int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int group, cudaStream_t stream) {
     if (!stream_grouped_applies(segs, nseg, K, group)) return Q4_ERR_UNSUPPORTED;
     const bool asym = segs[0].zeros != nullptr;

@@ -239,6 +239,14 @@ Q4_API int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, i
  * This is a debugging substitute for a memory checker; the pages have no counterpart. */
 Q4_API int q4gemv_bounds_violations(void *stream);
 
+/* Test export (host only, no device call): the CTA split a grouped launch makes for
+ * count (1..8) matrices of N[i] >= 1 rows at K and group, given grid_max resident CTAs
+ * (CTAs per SM x SMs).  Fills nblocks[i] (blocks of rows of matrix i) and cta_begin[i]
+ * (its first CTA; its CTAs run to the next matrix's first, or to the grid) and returns
+ * the grid; a negated status for bad arguments or a K without a streamed geometry. */
+Q4_API int q4gemv_grouped_split(const int64_t *N, int32_t count, int64_t K, int32_t group, int32_t grid_max,
+                                int32_t *nblocks, int32_t *cta_begin);
+
 #ifdef __cplusplus
 }
 #endif

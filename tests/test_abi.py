@@ -226,3 +226,44 @@ def test_plain_c_client_links_and_runs(L, tmp_path):
                     os.path.join(inc, "q4gemv.h")], check=True, capture_output=True, text=True)
     out = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert out.returncode == 0 and out.stdout.strip() == "ok", out.stdout + out.stderr
+
+
+def test_grouped_cta_split(L):
+    # the split the grouped launch makes, computed on the host by the library's own code:
+    # every block of every matrix goes to exactly one CTA (the kernel's split of a matrix's
+    # blocks over its CTAs), every CTA gets at least one block, all grid_max CTAs are used
+    # when there are more blocks, and moving a CTA between matrices never lowers the
+    # largest share
+    import random
+    rng = random.Random(5)
+    rows = {896: 48, 4096: 32}
+    for _ in range(400):
+        K = rng.choice([896, 4096])
+        count = rng.randint(1, 8)
+        Ns = [rng.choice([1, 7, 48, 128, 896, 4864, rng.randint(1, 200000)]) for _ in range(count)]
+        grid_max = rng.choice([152, 304, 456])
+        grid, nb, cb = q4.q4gemv_grouped_split(Ns, K, 32, grid_max)
+        assert nb == [-(-n // rows[K]) for n in Ns]
+        ends = cb[1:] + [grid]
+        c = [e - b for b, e in zip(cb, ends)]
+        assert cb[0] == 0 and all(1 <= ci <= nbi for ci, nbi in zip(c, nb))
+        assert grid == (sum(nb) if sum(nb) <= grid_max else grid_max)
+        for i in range(count):
+            covered = []
+            for k in range(c[i]):
+                b0, b1 = nb[i] * k // c[i], nb[i] * (k + 1) // c[i]
+                assert b1 > b0
+                covered += range(b0, b1)
+            assert covered == list(range(nb[i]))
+        worst = max(n / ci for n, ci in zip(nb, c))
+        for i in range(count):
+            for j in range(count):
+                if i != j and c[i] > 1 and c[j] < nb[j]:
+                    c2 = list(c)
+                    c2[i] -= 1
+                    c2[j] += 1
+                    assert max(n / ci for n, ci in zip(nb, c2)) >= worst - 1e-12
+    with pytest.raises(q4.Q4Error):
+        q4.q4gemv_grouped_split([100], 1000, 32, 152)     # K % g != 0
+    with pytest.raises(q4.Q4Error):
+        q4.q4gemv_grouped_split([0], 896, 32, 152)
