@@ -138,8 +138,9 @@ typedef struct {
  * its note on sharing one compute pass: every boundary between dispatches costs time of
  * its own).  Runs of up to 8 matrices that the TMA-streamed kernel serves (K in {896,
  * 2048, 4096, 8192, 16384}; all with or all without zero points; codes, scales and zeros
- * 16-byte aligned) are one launch, in which each matrix gets its own CTAs in proportion
- * to its rows; any other matrix runs as its own q4gemv_run.  The outputs equal those of
+ * 16-byte aligned; for K = 896 at least one block of 48 rows per SM over the run) are one
+ * launch, in which each matrix gets its own CTAs in proportion to its rows; the matrices
+ * of any other run each go through q4gemv_run.  The outputs equal those of
  * separate calls within the GEMV's tolerance.  segs: host array of count entries (read
  * during the call only).  Every entry is checked as q4gemv_run checks its arguments
  * before anything is launched.  Asynchronous; allocates nothing. */
