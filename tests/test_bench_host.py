@@ -81,6 +81,21 @@ def test_reference_arm_runs_the_oracle(tmp_path):
     line = json.loads(out.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+    assert "row slices" in line["cpu_baseline"]["sample"]
+
+
+def test_reference_arm_shares_many_steps_over_cores():
+    # with at least four steps per core, whole steps go to one worker thread per core
+    steps = 4 * (os.cpu_count() or 1)
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", str(steps), "--warmup", "1",
+                          "--ref-seconds", "2"], cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr
+    import json
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["steps"] == steps and line["value"] > 0
+    assert "worker threads" in line["cpu_baseline"]["sample"]
+    assert line["cpu_baseline"]["cores"] == (os.cpu_count() or 1)
 
 
 def test_sweep_checkpoint_round_trip(tmp_path):
