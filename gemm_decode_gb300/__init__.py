@@ -17,6 +17,7 @@ import threading
 __all__ = [
     "Q4Error", "lib", "library_path", "exported_names",
     "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run", "q4gemm_run",
+    "q4gemv_run_ex", "q4gemv_fused_run_ex", "q4gemv_grouped_run_ex", "q4gemm_run_ex",
     "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
@@ -24,6 +25,7 @@ __all__ = [
     "q4gemv_bounds_violations", "q4gemv_grouped_split",
     "Q4_OK", "Q4_ERR_INVALID_ARG", "Q4_ERR_UNSUPPORTED", "Q4_ERR_MISALIGNED",
     "Q4_ERR_CUDA", "Q4_ERR_TIMEOUT", "Q4_EPILOGUE_NONE", "Q4_EPILOGUE_SWIGLU",
+    "Q4_RUN_OVERLAPPED", "Q4_RUN_EXACT_X", "Q4_RUN_WAIT_TIMEOUT",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -32,6 +34,7 @@ HEADER = os.path.join(_ROOT, "include", "q4gemv.h")
 
 Q4_OK, Q4_ERR_INVALID_ARG, Q4_ERR_UNSUPPORTED, Q4_ERR_MISALIGNED, Q4_ERR_CUDA, Q4_ERR_TIMEOUT = range(6)
 Q4_EPILOGUE_NONE, Q4_EPILOGUE_SWIGLU = 0, 1
+Q4_RUN_OVERLAPPED, Q4_RUN_EXACT_X, Q4_RUN_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 
 def library_path() -> str:
@@ -54,6 +57,10 @@ class _PackInfo(ctypes.Structure):
                 ("scales_bytes", ctypes.c_int64), ("zeros_row_bytes", ctypes.c_int64),
                 ("zeros_bytes", ctypes.c_int64), ("base_alignment", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
+
+
+class _RunOptions(ctypes.Structure):
+    _fields_ = [("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32), ("wait_timeout_ns", ctypes.c_uint64)]
 
 
 class _Segment(ctypes.Structure):
@@ -81,6 +88,12 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_fused_run.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i32, _i64, _i64,
                                            _i32, _i32, _vp]
             L.q4gemm_run.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _vp]
+            _opt = ctypes.POINTER(_RunOptions)
+            L.q4gemv_run_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _opt, _vp]
+            L.q4gemv_fused_run_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _i32, _i64, _i64,
+                                              _i32, _i32, _opt, _vp]
+            L.q4gemv_grouped_run_ex.argtypes = [ctypes.POINTER(_Segment), _i32, _i64, _i32, _opt, _vp]
+            L.q4gemm_run_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _opt, _vp]
             L.q4_0_gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_grouped_run.argtypes = [ctypes.POINTER(_Segment), _i32, _i64, _i32, _vp]
             L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
@@ -98,7 +111,8 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_grouped_split.argtypes = [ctypes.POINTER(_i64), _i32, _i64, _i32, _i32,
                                                ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run",
-                      "q4gemm_run", "f32gemv_run",
+                      "q4gemm_run", "f32gemv_run", "q4gemv_run_ex", "q4gemv_fused_run_ex", "q4gemv_grouped_run_ex",
+                      "q4gemm_run_ex",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
                       "q4gemv_device_status", "q4gemm_set_wait_timeout_ns",
                       "q4gemv_set_overlapped_launch", "q4gemv_bounds_violations", "q4gemv_grouped_split"):
@@ -204,6 +218,69 @@ def q4gemv_grouped_run(segments, K, group=32, stream=None, check=True) -> int:
     st = lib().q4gemv_grouped_run(arr, len(segments), int(K), int(group), _stream(stream))
     if check:
         _check(st, "q4gemv_grouped_run")
+    return st
+
+
+def _options(flags, wait_timeout_ns, reserved=0):
+    """Per-call options of the *_ex entry points (None: a NULL pointer, the defaults)."""
+    if flags is None and wait_timeout_ns is None and not reserved:
+        return None
+    f = int(flags or 0)
+    if wait_timeout_ns is not None:
+        f |= Q4_RUN_WAIT_TIMEOUT
+    o = _RunOptions(f, int(reserved), int(wait_timeout_ns or 0))
+    return ctypes.byref(o)
+
+
+def q4gemv_run_ex(codes, scales_f16, zeros_u4_or_null, x, y, M=None, N=None, K=None, group=32,
+                  flags=None, wait_timeout_ns=None, stream=None, check=True, _reserved=0) -> int:
+    """q4gemv_run with per-call options: flags (Q4_RUN_*), and wait_timeout_ns, which sets
+    Q4_RUN_WAIT_TIMEOUT when given."""
+    M, N, K = _mnk_q4(codes, x, M, N, K)
+    st = lib().q4gemv_run_ex(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                             _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(x, "x", 4),
+                             _addr(y, "y", 4), M, N, K, int(group), _options(flags, wait_timeout_ns, _reserved),
+                             _stream(stream))
+    if check:
+        _check(st, "q4gemv_run_ex")
+    return st
+
+
+def q4gemv_fused_run_ex(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M=None, N=None, K=None, group=32,
+                        epilogue=Q4_EPILOGUE_NONE, flags=None, wait_timeout_ns=None, stream=None, check=True) -> int:
+    M, N, K = _mnk_q4(codes, x, M, N, K)
+    st = lib().q4gemv_fused_run_ex(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                                   _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(x, "x", 4),
+                                   _addr(gamma, "gamma", 4), float(eps), _addr(y, "y", 4), M, N, K, int(group),
+                                   int(epilogue), _options(flags, wait_timeout_ns), _stream(stream))
+    if check:
+        _check(st, "q4gemv_fused_run_ex")
+    return st
+
+
+def q4gemv_grouped_run_ex(segments, K, group=32, flags=None, wait_timeout_ns=None, stream=None, check=True) -> int:
+    arr = (_Segment * max(1, len(segments)))()
+    for i, sg in enumerate(segments):
+        codes, scales, zeros, x, y = sg[:5]
+        N = int(sg[5]) if len(sg) > 5 else int(codes.shape[0])
+        arr[i] = _Segment(_addr(codes, "codes", 1), _addr(scales, "scales_f16", 2), _addr(zeros, "zeros_u4_or_null", 1),
+                          _addr(x, "x", 4), _addr(y, "y", 4), N)
+    st = lib().q4gemv_grouped_run_ex(arr, len(segments), int(K), int(group), _options(flags, wait_timeout_ns),
+                                     _stream(stream))
+    if check:
+        _check(st, "q4gemv_grouped_run_ex")
+    return st
+
+
+def q4gemm_run_ex(codes, scales_f16, zeros_u4_or_null, a_bf16, c, M=None, N=None, K=None, group=32,
+                  flags=None, wait_timeout_ns=None, stream=None, check=True) -> int:
+    M, N, K = _mnk_q4(codes, a_bf16, M, N, K)
+    st = lib().q4gemm_run_ex(_addr(codes, "codes", 1), _addr(scales_f16, "scales_f16", 2),
+                             _addr(zeros_u4_or_null, "zeros_u4_or_null", 1), _addr(a_bf16, "a_bf16", 2),
+                             _addr(c, "c", 4), M, N, K, int(group), _options(flags, wait_timeout_ns),
+                             _stream(stream))
+    if check:
+        _check(st, "q4gemm_run_ex")
     return st
 
 

@@ -14,10 +14,29 @@ namespace q4 {
 namespace {
 thread_local char g_cuda_error[256] = "";
 std::atomic<bool> g_overlapped_launch{false};
+std::atomic<unsigned long long> g_default_wait_ns{1000ull * 1000 * 1000};   // 1 s per wait
+thread_local const CallOptions *t_call_options = nullptr;
 }
 
 bool set_overlapped_launch(bool on) { return g_overlapped_launch.exchange(on); }
-bool overlapped_launch() { return g_overlapped_launch.load(std::memory_order_relaxed); }
+void set_default_wait_ns(unsigned long long ns) { g_default_wait_ns = ns; }
+
+CallOptions default_call_options() {
+    CallOptions o;
+    o.overlap = g_overlapped_launch.load(std::memory_order_relaxed);
+    o.wait_ns = g_default_wait_ns.load(std::memory_order_relaxed);
+    return o;
+}
+
+const CallOptions &call_options() {
+    if (t_call_options != nullptr) return *t_call_options;
+    thread_local CallOptions d;
+    d = default_call_options();
+    return d;
+}
+
+CallScope::CallScope(const CallOptions &o) : opts_(o), prev_(t_call_options) { t_call_options = &opts_; }
+CallScope::~CallScope() { t_call_options = prev_; }
 
 void set_cuda_error(cudaError_t e) {
     std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
@@ -50,6 +69,31 @@ const DeviceInfo &device_info() {
 }
 
 static bool valid_group(int32_t g) { return g == 32 || g == 64 || g == 128; }
+
+// Byte ranges [lo, hi) of the arrays of a call, for the check that no output overlaps
+// an input or another output (the kernels read inputs while other CTAs store results).
+struct Span {
+    uintptr_t lo, hi;
+};
+static Span span(const void *p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, p == nullptr ? a : a + static_cast<uintptr_t>(bytes)};
+}
+static bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+static bool overlaps_any(Span out, const Span *in, int n) {
+    for (int i = 0; i < n; ++i)
+        if (overlap(out, in[i])) return true;
+    return false;
+}
+// The packed-weight arrays of an N x K matrix of group g (zeros may be null).
+static int weight_spans(const void *codes, const void *scales, const void *zeros, int64_t N, int64_t K, int32_t g,
+                        Span *out) {
+    const int64_t nb = K / g;
+    out[0] = span(codes, N * (K / 2));
+    out[1] = span(scales, N * nb * 2);
+    out[2] = span(zeros, N * ((nb + 1) / 2));
+    return 3;
+}
 
 // Scalar checks shared by the packed-weight entry points.
 static int check_shape(int64_t M, int64_t N, int64_t K, int32_t group) {
@@ -135,6 +179,12 @@ int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_o
     if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
     if (x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    {
+        Span in[4];
+        weight_spans(codes, scales_f16, zeros_u4_or_null, N, K, group, in);
+        in[3] = span(x, 4 * M * K);
+        if (overlaps_any(span(y, 4 * M * N), in, 4)) return Q4_ERR_INVALID_ARG;
+    }
     return launch_q4gemv(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
                          static_cast<const uint8_t *>(zeros_u4_or_null), x, y, M, N, static_cast<int>(K), group,
                          static_cast<cudaStream_t>(stream));
@@ -153,6 +203,14 @@ int q4gemv_fused_run(const void *codes, const void *scales_f16, const void *zero
     if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
     if (x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(y, 4) || (gamma != nullptr && !aligned(gamma, 16))) return Q4_ERR_MISALIGNED;
+    {
+        Span in[5];
+        weight_spans(codes, scales_f16, zeros_u4_or_null, N, K, group, in);
+        in[3] = span(x, 4 * M * K);
+        in[4] = span(gamma, 4 * K);
+        const int64_t ycols = epilogue == Q4_EPILOGUE_SWIGLU ? N / 2 : N;
+        if (overlaps_any(span(y, 4 * M * ycols), in, 5)) return Q4_ERR_INVALID_ARG;
+    }
     if (gamma == nullptr && epilogue == Q4_EPILOGUE_NONE)
         return q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M, N, K, group, stream);
     return launch_q4gemv_fused(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
@@ -174,6 +232,22 @@ int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, i
         if ((st = check_q4_args(sg.codes, sg.scales_f16, sg.N, K, group)) != Q4_OK) return st;
         if (sg.x == nullptr || sg.y == nullptr) return Q4_ERR_INVALID_ARG;
         if (!aligned(sg.x, 16) || !aligned(sg.y, 4)) return Q4_ERR_MISALIGNED;
+    }
+    // the matrices must be independent: no output overlaps any matrix's inputs or another
+    // output (one launch serves them all, with no order among its CTAs)
+    for (int32_t i = 0; i < count; ++i) {
+        const q4gemv_segment_t &si = segs[i];
+        if (si.N == 0) continue;
+        const Span yi = span(si.y, 4 * si.N);
+        for (int32_t j = 0; j < count; ++j) {
+            const q4gemv_segment_t &sj = segs[j];
+            if (sj.N == 0) continue;
+            Span in[5];
+            weight_spans(sj.codes, sj.scales_f16, sj.zeros_u4_or_null, sj.N, K, group, in);
+            in[3] = span(sj.x, 4 * K);
+            in[4] = j != i ? span(sj.y, 4 * sj.N) : Span{0, 0};
+            if (overlaps_any(yi, in, 5)) return Q4_ERR_INVALID_ARG;
+        }
     }
     // runs of up to kStreamMaxSeg non-empty matrices: one streamed launch where it applies,
     // else one q4gemv_run per matrix
@@ -197,7 +271,7 @@ int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, i
             idx[n++] = i;
         }
         if (n == 0) break;
-        if (q4::stream_grouped_applies(run, n, static_cast<int>(K), group)) {
+        if (!call_options().exact_x && q4::stream_grouped_applies(run, n, static_cast<int>(K), group)) {
             st = q4::launch_q4gemv_stream_grouped(run, n, static_cast<int>(K), group, s);
             if (st != Q4_OK) return st;
             continue;
@@ -225,6 +299,10 @@ int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64
     if (M > 16 || N > 0x7fffffffLL || K > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
     if (blocks == nullptr || x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
     if (!aligned(blocks, 2) || !aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    {
+        const Span in[2] = {span(blocks, N * (K / 32) * 18), span(x, 4 * M * K)};
+        if (overlaps_any(span(y, 4 * M * N), in, 2)) return Q4_ERR_INVALID_ARG;
+    }
     return launch_q40gemv(static_cast<const uint8_t *>(blocks), x, y, M, N, static_cast<int>(K),
                           static_cast<cudaStream_t>(stream));
 }
@@ -237,6 +315,12 @@ int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_o
     if ((st = check_q4_args(codes, scales_f16, N, K, group)) != Q4_OK) return st;
     if (a_bf16 == nullptr || c == nullptr) return Q4_ERR_INVALID_ARG;
     if (!aligned(a_bf16, 16) || !aligned(c, 4)) return Q4_ERR_MISALIGNED;
+    {
+        Span in[4];
+        weight_spans(codes, scales_f16, zeros_u4_or_null, N, K, group, in);
+        in[3] = span(a_bf16, 2 * M * K);
+        if (overlaps_any(span(c, 4 * M * N), in, 4)) return Q4_ERR_INVALID_ARG;
+    }
     return launch_q4gemm(static_cast<const uint8_t *>(codes), static_cast<const uint16_t *>(scales_f16),
                          static_cast<const uint8_t *>(zeros_u4_or_null), static_cast<const uint16_t *>(a_bf16), c,
                          M, N, static_cast<int>(K), group, static_cast<cudaStream_t>(stream));
@@ -248,6 +332,10 @@ int f32gemv_run(const float *W, const float *x, float *y, int32_t M, int64_t N, 
     if (M > 16 || K % 4 != 0 || N > 0x7fffffffLL || K > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
     if (W == nullptr || x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
     if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    {
+        const Span in[2] = {span(W, 4 * N * K), span(x, 4 * M * K)};
+        if (overlaps_any(span(y, 4 * M * N), in, 2)) return Q4_ERR_INVALID_ARG;
+    }
     return launch_f32gemv(W, x, y, M, N, static_cast<int>(K), static_cast<cudaStream_t>(stream));
 }
 
@@ -300,7 +388,7 @@ int q4gemv_bounds_violations(void *) { return -1; }
 
 
 int q4gemm_set_wait_timeout_ns(uint64_t ns) {
-    set_gemm_wait_timeout_ns(ns);
+    set_default_wait_ns(ns);
     return Q4_OK;
 }
 
@@ -314,6 +402,58 @@ int vec4_read_probe_run(const void *buf, int64_t bytes, float *partial, int32_t 
     if (blocks_used) *blocks_used = blocks;
     return launch_read_probe(static_cast<const float4 *>(buf), bytes / 16, partial, blocks,
                              static_cast<cudaStream_t>(stream));
+}
+
+// ---- entry points with per-call options ----
+
+static int options_from(const q4_run_options_t *o, uint32_t allowed, CallOptions &out) {
+    out = CallOptions{};   // built-in defaults, whatever the process-wide settings are
+    if (o == nullptr) return Q4_OK;
+    if (o->reserved != 0 || (o->flags & ~allowed) != 0) return Q4_ERR_INVALID_ARG;
+    out.overlap = (o->flags & Q4_RUN_OVERLAPPED) != 0;
+    out.exact_x = (o->flags & Q4_RUN_EXACT_X) != 0;
+    if (o->flags & Q4_RUN_WAIT_TIMEOUT) out.wait_ns = o->wait_timeout_ns;
+    return Q4_OK;
+}
+
+constexpr uint32_t kGemvFlags = Q4_RUN_OVERLAPPED | Q4_RUN_EXACT_X | Q4_RUN_WAIT_TIMEOUT;
+
+int q4gemv_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const float *x, float *y,
+                  int32_t M, int64_t N, int64_t K, int32_t group, const q4_run_options_t *opts, void *stream) {
+    CallOptions co;
+    const int st = options_from(opts, kGemvFlags, co);
+    if (st != Q4_OK) return st;
+    CallScope scope(co);
+    return q4gemv_run(codes, scales_f16, zeros_u4_or_null, x, y, M, N, K, group, stream);
+}
+
+int q4gemv_fused_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const float *x,
+                        const float *gamma, float eps, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
+                        int32_t epilogue, const q4_run_options_t *opts, void *stream) {
+    CallOptions co;
+    const int st = options_from(opts, kGemvFlags, co);
+    if (st != Q4_OK) return st;
+    CallScope scope(co);
+    return q4gemv_fused_run(codes, scales_f16, zeros_u4_or_null, x, gamma, eps, y, M, N, K, group, epilogue, stream);
+}
+
+int q4gemv_grouped_run_ex(const q4gemv_segment_t *segs, int32_t count, int64_t K, int32_t group,
+                          const q4_run_options_t *opts, void *stream) {
+    CallOptions co;
+    const int st = options_from(opts, kGemvFlags, co);
+    if (st != Q4_OK) return st;
+    CallScope scope(co);
+    return q4gemv_grouped_run(segs, count, K, group, stream);
+}
+
+int q4gemm_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const void *a_bf16,
+                  float *c, int32_t M, int64_t N, int64_t K, int32_t group, const q4_run_options_t *opts,
+                  void *stream) {
+    CallOptions co;
+    const int st = options_from(opts, Q4_RUN_WAIT_TIMEOUT, co);
+    if (st != Q4_OK) return st;
+    CallScope scope(co);
+    return q4gemm_run(codes, scales_f16, zeros_u4_or_null, a_bf16, c, M, N, K, group, stream);
 }
 
 }  // extern "C"

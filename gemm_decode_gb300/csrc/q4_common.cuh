@@ -37,14 +37,36 @@ inline int launch_status() {
     return Q4_OK;
 }
 
-// Overlapped (programmatic dependent) launch of the GEMV kernels: process-wide flag;
-// set_overlapped_launch returns the previous value.  add_overlap_attr appends the
-// programmatic-stream-serialisation attribute to cfg when the flag is set (attrs must
-// have a free entry at cfg.numAttrs).
-bool set_overlapped_launch(bool on);
-bool overlapped_launch();
+// Options of the API call in progress on the calling thread.  The entry points without
+// an options argument take the process-wide defaults (q4gemv_set_overlapped_launch,
+// q4gemm_set_wait_timeout_ns); the *_ex entry points install the caller's own for the
+// duration of the call (CallScope), so nothing one caller chooses reaches another.
+struct CallOptions {
+    bool overlap = false;                        // programmatic dependent launch of the GEMVs
+    bool exact_x = false;                        // GEMVs on the CUDA-core float kernel only
+    unsigned long long wait_ns = 1000000000ull;  // bound on each bounded device-side wait
+};
+const CallOptions &call_options();
+CallOptions default_call_options();
+bool set_overlapped_launch(bool on);            // process default; returns the previous value
+void set_default_wait_ns(unsigned long long ns);
+class CallScope {
+public:
+    explicit CallScope(const CallOptions &o);
+    ~CallScope();
+    CallScope(const CallScope &) = delete;
+    CallScope &operator=(const CallScope &) = delete;
+
+private:
+    CallOptions opts_;
+    const CallOptions *prev_;
+};
+
+// add_overlap_attr appends the programmatic-stream-serialisation attribute to cfg when
+// the call's options ask for an overlapped launch (attrs must have a free entry at
+// cfg.numAttrs).
 inline void add_overlap_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attrs) {
-    if (!overlapped_launch()) return;
+    if (!call_options().overlap) return;
     cudaLaunchAttribute &at = attrs[cfg.numAttrs];
     at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at.val.programmaticStreamSerializationAllowed = 1;
@@ -72,7 +94,6 @@ int launch_f32gemv(const float *W, const float *x, float *y, int M, int64_t N, i
 bool tc_gemv_applies(int M, int64_t N, int K, const void *codes);
 int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x, float *y,
                      int M, int64_t N, int K, int group, cudaStream_t stream);
-void set_gemm_wait_timeout_ns(unsigned long long ns);
 int read_device_status(cudaStream_t stream);
 int launch_dequant(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
                    void *w, bool bf16, int64_t N, int K, int group, cudaStream_t stream);

@@ -316,10 +316,6 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
 
 // ------------------------------------------------------------------ host side
 
-static std::atomic<unsigned long long> g_timeout_ns{1000ull * 1000 * 1000};   // 1 s per wait
-
-unsigned long long gemm_wait_timeout_ns() { return g_timeout_ns; }
-
 // Address of the tensor-core status word, for kernels in other translation units.
 unsigned int *gemm_status_word() {
     static std::atomic<unsigned int *> addr[64];
@@ -335,11 +331,6 @@ unsigned int *gemm_status_word() {
         addr[dev] = static_cast<unsigned int *>(p);
     }
     return addr[dev];
-}
-
-void set_gemm_wait_timeout_ns(unsigned long long ns) {
-    g_timeout_ns = ns;
-    set_stream_wait_timeout_ns(ns);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -426,7 +417,7 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
     g.zrow = (g.nb + 1) / 2;
     g.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
     g.c_vec = (aligned(c, 16) && (N % 4) == 0) ? 1 : 0;
-    g.timeout_ns = g_timeout_ns;
+    g.timeout_ns = call_options().wait_ns;
     switch (nh) {
         case 4: return launch_tc<4, 2>(map, g, M, N, stream);
         case 3: return launch_tc<3, 3>(map, g, M, N, stream);

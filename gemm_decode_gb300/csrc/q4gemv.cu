@@ -85,10 +85,14 @@ static int plan_gemv(int M, int64_t N, int K, bool asym, GemvPlan &p) {
 int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
                   const float *x, float *y, int M, int64_t N, int K, int group,
                   cudaStream_t stream) {
-    if (stream_applies(M, N, K, group, codes, scales, zeros))
+    // (a call with the exact-x option takes the general kernel for every shape: its
+    // products are exact before one rounding, for any finite x)
+    const bool exact = call_options().exact_x;
+    if (!exact && stream_applies(M, N, K, group, codes, scales, zeros))
         return launch_q4gemv_stream(codes, scales, zeros, x, y, N, K, group, stream);
-    if (tc_gemv_applies(M, N, K, codes)) return launch_q4gemv_tc(codes, scales, zeros, x, y, M, N, K, group, stream);
-    {
+    if (!exact && tc_gemv_applies(M, N, K, codes))
+        return launch_q4gemv_tc(codes, scales, zeros, x, y, M, N, K, group, stream);
+    if (!exact) {
         XregPlan xp;
         XregArgs xa;
         if (plan_q4gemv_xreg(M, N, K, group, scales, zeros, xp, xa)) {
@@ -139,11 +143,12 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
 int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                         const float *gamma, float eps, int swiglu, float *y, int M, int64_t N, int K, int group,
                         cudaStream_t stream) {
-    if (stream_applies(M, N, K, group, codes, scales, zeros)) {
+    const bool exact = call_options().exact_x;   // (the general kernel only, as for launch_q4gemv)
+    if (!exact && stream_applies(M, N, K, group, codes, scales, zeros)) {
         const int st = launch_q4gemv_stream_fused(codes, scales, zeros, x, gamma, eps, swiglu, y, N, K, group, stream);
         if (st != Q4_ERR_UNSUPPORTED) return st;   // (the fused carve-up is 128 bytes larger)
     }
-    {   // M = 1 on shorter matrices: the register-resident kernel's fused instances
+    if (!exact) {   // M = 1 on shorter matrices: the register-resident kernel's fused instances
         XregPlan xp;
         XregFusedArgs xa;
         if (plan_q4gemv_xreg(M, N, K, group, scales, zeros, xp, xa, true)) {

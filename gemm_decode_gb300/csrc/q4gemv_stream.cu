@@ -93,9 +93,6 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
     return stream_geo_ok(g, asym);
 }
 
-static std::atomic<unsigned long long> g_stream_timeout_ns{1000ull * 1000 * 1000};
-void set_stream_wait_timeout_ns(unsigned long long ns) { g_stream_timeout_ns = ns; }
-
 // fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks)
 static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                              const float *gamma, float eps, int swiglu, int fuse, float *y, int64_t N, int K,
@@ -111,7 +108,7 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
     a.y = y;
     a.N = N;
     a.nblocks = 0;
-    a.timeout_ns = g_stream_timeout_ns;
+    a.timeout_ns = call_options().wait_ns;
     a.status = stream_status_word();
     a.bounds = bounds_counter();
     a.gamma = gamma;
@@ -260,7 +257,7 @@ int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int gro
     a.y = segs[0].y;
     a.N = segs[0].N;
     a.nblocks = 0;
-    a.timeout_ns = g_stream_timeout_ns;
+    a.timeout_ns = call_options().wait_ns;
     a.status = stream_status_word();
     a.bounds = bounds_counter();
     a.gamma = nullptr;

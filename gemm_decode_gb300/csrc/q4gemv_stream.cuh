@@ -153,7 +153,6 @@ int stream_assign_ctas(StreamGroupArgs &a, int grid_max);
 // cta_begin, returns the grid; Q4_ERR_UNSUPPORTED (negated) when K has no streamed geometry.
 int stream_grouped_split(const int64_t *N, int count, int K, int group, int grid_max, int *nblocks, int *cta_begin);
 int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int group, cudaStream_t stream);
-void set_stream_wait_timeout_ns(unsigned long long ns);
 int read_and_clear_stream_status(unsigned int *v);
 
 }  // namespace q4

@@ -48,7 +48,6 @@ using namespace tc;
 namespace cg = cooperative_groups;
 
 unsigned int *gemm_status_word();
-unsigned long long gemm_wait_timeout_ns();
 
 namespace {
 
@@ -615,7 +614,7 @@ int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t
     g.nb = K / group;
     g.zrow = (g.nb + 1) / 2;
     g.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
-    g.timeout_ns = gemm_wait_timeout_ns();
+    g.timeout_ns = call_options().wait_ns;
     g.status = gemm_status_word();
     if (g.status == nullptr) return Q4_ERR_CUDA;
     g.bounds = bounds_counter();

@@ -34,15 +34,14 @@ __device__ __forceinline__ void cp_wait() {
 
 // Encode one 32-element chunk of x into the plane layout, four threads per chunk
 // (the four consecutive lanes 4j..4j+3 of a warp; thread q owns elements
-// 8q..8q+7, i.e. code word q).  With 2^E > max |x| over the chunk, an even
-// element k is held as m_k = rint(x_k 2^(22-E)) and an odd one as
-// m_k = rint(x_k 2^(18-E)): the odd (high-nibble) codes are used in place, as
-// 16 q, so the odd values carry a factor 16 less and 20 rather than 24 bits.
-// For word w (elements 8w..8w+7) and plane b, word 6w+2b holds the b-th byte of
-// m for the even elements 8w, 8w+2, 8w+4, 8w+6 and word 6w+2b+1 that of the
-// odd elements; plane 2 is the signed top byte.  Words 24/25 hold the plane
-// sums of the effective values (m for even, 16 m for odd: planes 0+1 combined
-// as sum of (byte0 + 256 byte1), plane 2), word 27 the chunk scale 2^(E-22).
+// 8q..8q+7, i.e. code word q).  With 2^(E-1) <= max |x| < 2^E over the chunk,
+// every element k is held as the 24-bit integer m_k = rint(x_k 2^(22-E))
+// (|m_k| <= 2^22), i.e. to within 2^(E-23) <= 2^-22 max |x|.  For word w
+// (elements 8w..8w+7) and plane b, word 6w+2b holds the b-th byte of m for the
+// even elements 8w, 8w+2, 8w+4, 8w+6 and word 6w+2b+1 that of the odd
+// elements; plane 2 is the signed top byte.  Words 24/25 hold the plane sums
+// over the chunk (planes 0+1 combined as the sum of byte0 + 256 byte1, and
+// plane 2), word 27 the chunk scale 2^(E-22).
 // `valid` false encodes zeros; `store` false skips the stores (the shuffles
 // still run: all lanes take part).
 __device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, uint32_t *pw, int q);
@@ -114,10 +113,9 @@ __device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, 
     int E = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 126;
     if (E < -100) E = -100;
     const float up = __uint_as_float(static_cast<uint32_t>(127 + 22 - E) << 23);   // 2^(22-E)
-    const float up_odd = __uint_as_float(static_cast<uint32_t>(127 + 18 - E) << 23);   // 2^(18-E)
     int m[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * ((i & 1) ? up_odd : up));  // |m| <= 2^22
+    for (int i = 0; i < 8; ++i) m[i] = __float2int_rn(v[i] * up);  // |m| <= 2^22
     // byte b of the four even (odd) elements -> one word, via byte permutes
 #pragma unroll
     for (int par = 0; par < 2; ++par) {
@@ -129,13 +127,12 @@ __device__ __forceinline__ void encode_values8(const float (&v)[8], bool store, 
             if (store) pw[6 * q + 2 * b + par] = __byte_perm(t01, t23, 0x5410u);
         }
     }
-    // plane sums of the effective values (odd elements count 16 times)
+    // plane sums
     int s01 = 0, s2 = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int wgt = (i & 1) ? 16 : 1;
-        s01 += wgt * (m[i] & 0xFFFF);   // byte0 + 256 byte1
-        s2 += wgt * (m[i] >> 16);       // arithmetic shift: the signed top byte
+        s01 += m[i] & 0xFFFF;   // byte0 + 256 byte1
+        s2 += m[i] >> 16;       // arithmetic shift: the signed top byte
     }
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
@@ -157,16 +154,16 @@ struct Planes {
 };
 
 // Integer dot product of one 16-byte chunk with one x chunk, minus the
-// zero-point term: sum_k (q_k - z) m_eff_k (m_eff = m for even k, 16 m for odd k),
-// exact in int32 and returned as binary32 (the conversion of the planes-0/1 part,
-// |lo| < 2^30, may round once, by at most 2^-24 of it).
+// zero-point term: sum_k (q_k - z) m_k, exact in int32 and returned as binary32
+// (the conversion of the planes-0/1 part, |lo| < 2^26, may round once, by at
+// most 2^-24 of it).
 __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes &P) {
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
     int a0 = 0, a1 = 0, a2 = 0;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-        const uint32_t lo = words[w] & 0x0F0F0F0Fu;   // codes of even k, one per byte
-        const uint32_t hi = words[w] & 0xF0F0F0F0u;   // 16 x codes of odd k, in place
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu;          // codes of even k, one per byte
+        const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;   // codes of odd k, one per byte
         a0 = dp4a_uu(lo, P.p[6 * w + 0], a0);
         a0 = dp4a_uu(hi, P.p[6 * w + 1], a0);
         a1 = dp4a_uu(lo, P.p[6 * w + 2], a1);

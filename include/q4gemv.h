@@ -31,8 +31,36 @@
  *   - Sizes: 1 <= K, K % g == 0, g in {32, 64, 128}.
  *   - Alignment: codes, x, W, a_bf16 and probe buffers 16-byte aligned; scales 2-byte,
  *     y / c 4-byte; otherwise Q4_ERR_MISALIGNED.
+ *   - No output may overlap an input or another output of the same call (the kernels
+ *     read inputs while other CTAs store results): checked on the host from the byte
+ *     ranges the sizes imply, Q4_ERR_INVALID_ARG otherwise.
  *   - A launch failure reported by the CUDA runtime returns Q4_ERR_CUDA (the runtime's
  *     error string is available from q4gemv_last_cuda_error()).
+ *
+ * Accuracy of the GEMVs (y_exact: the sum in exact arithmetic; inputs finite, results
+ * finite).  The stated tolerance is |y - y_exact| <= 1e-3 * sum_k |w_nk x_mk| + 1e-6.
+ *   - CUDA-core float kernel (any call with Q4_RUN_EXACT_X; otherwise the shapes no
+ *     faster kernel takes): each product (q - z) * s * x is formed exactly and rounded
+ *     once, then summed in binary32; within the stated tolerance for every finite input.
+ *   - dp4a kernels (M <= 2: the TMA-streamed, register-resident and grouped launches):
+ *     x is held per 32-element chunk c as 24-bit integers under one power of two,
+ *     2^(E_c - 1) <= max_{k in c} |x_k| < 2^E_c (E_c >= -100), and the dot products are
+ *     exact in integers.  Per output
+ *         |y - y_exact| <= B1 + (K/32 + 10) * 2^-24 * (sum_k |w_k x_k| + B1),
+ *         B1 = (1 + 2^-7) * sum_c 2^(E_c - 23) * sum_{k in c} |w_k|
+ *              <= 1.01 * 2^-22 * sum_c (max_{k in c} |x_k|) * (sum_{k in c} |w_k|).
+ *     This is inside the stated tolerance unless a chunk of x mixes values thousands of
+ *     times apart whose large members meet small weights (B1 stays below
+ *     9e-4 * sum |w x| whenever no chunk's largest |x| exceeds about 3700 times the
+ *     |w|-weighted mean |x| of its chunk); activations of that kind should use
+ *     Q4_RUN_EXACT_X.
+ *   - tcgen05 tensor-core GEMV (3 <= M <= 16 on the shapes it takes): each weight is
+ *     rounded once to fp16 and x is carried as two fp16 parts, x = hi + lo:
+ *         |y - y_exact| <= (2^-11 + 2^-20) * sum_k |w_k x_k|
+ *                          + 2^-24 * (sum_k |w_k| + sum_k |x_k|)
+ *     plus binary32 accumulation (the last term comes from fp16 subnormals: weights or
+ *     parts of x below 2^-14); it needs |x| < 65504 and |(q - z) s| < 65504 (the fp16
+ *     range; outside it the output is not finite).
  */
 #ifndef Q4GEMV_H
 #define Q4GEMV_H
@@ -58,6 +86,29 @@ typedef enum {
     Q4_ERR_CUDA = 4,        /* the CUDA runtime refused or failed a launch */
     Q4_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (mbarrier pipelines) */
 } q4_status;
+
+/* Options of one call of the *_ex entry points.  They apply to that call alone: nothing
+ * in them outlives the call or reaches another caller (the process-wide setters below
+ * only change what the entry points without options do).  A NULL options pointer means
+ * flags 0: no overlapped launch, the fastest kernel for the shape, waits bounded at 1 s. */
+typedef struct {
+    uint32_t flags;            /* bitwise OR of the Q4_RUN_* flags                        */
+    uint32_t reserved;         /* must be 0                                               */
+    uint64_t wait_timeout_ns;  /* bound on each device-side pipeline wait, read when
+                                  flags has Q4_RUN_WAIT_TIMEOUT (0: give up at once)     */
+} q4_run_options_t;
+
+/* Overlapped (programmatic dependent) launch of the GEMV kernels: the call's kernel may
+ * start streaming its weights while the kernel before it in the stream still runs, and
+ * waits for that kernel before it reads x or writes y.  Contract: the kernel that
+ * immediately precedes the call in the stream must not write the call's weights. */
+#define Q4_RUN_OVERLAPPED 0x1u
+/* Run the GEMV on the CUDA-core float kernel, which meets the stated tolerance for every
+ * finite input (see "Accuracy" above); slower than the dp4a and tensor-core kernels on
+ * long matrices. */
+#define Q4_RUN_EXACT_X 0x2u
+/* Bound each bounded device-side wait by wait_timeout_ns instead of 1 s. */
+#define Q4_RUN_WAIT_TIMEOUT 0x4u
 
 /* Byte sizes of one packed weight matrix (all byte counts). */
 typedef struct {
@@ -88,11 +139,20 @@ Q4_API int q4gemv_pack_info(int64_t N, int64_t K, int32_t group, q4gemv_pack_inf
  * The library picks the kernel by shape: a TMA-streamed dp4a kernel for M = 1 on long
  * matrices, the tcgen05 tensor-core GEMV for 3 <= M <= 16 on large ones (K split over a
  * thread-block cluster when tiles are few), a register-resident dp4a kernel for M <= 2,
- * and a general CUDA-core kernel (split-K over a cluster for long K / few rows) otherwise.
- * Asynchronous on `stream`; allocates nothing. */
+ * and a general CUDA-core kernel (split-K over a cluster for long K / few rows) otherwise;
+ * the accuracy each gives is stated at the top of this header.  Launches are overlapped
+ * when q4gemv_set_overlapped_launch(1) is in force; waits are bounded by the process-wide
+ * q4gemm_set_wait_timeout_ns value.  Asynchronous on `stream`; allocates nothing. */
 Q4_API int q4gemv_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
                const float *x, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
                void *stream);
+
+/* q4gemv_run with per-call options (opts may be NULL; see q4_run_options_t).  Flags:
+ * Q4_RUN_OVERLAPPED, Q4_RUN_EXACT_X, Q4_RUN_WAIT_TIMEOUT; an unknown flag or a nonzero
+ * reserved field is Q4_ERR_INVALID_ARG. */
+Q4_API int q4gemv_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                  const float *x, float *y, int32_t M, int64_t N, int64_t K, int32_t group,
+                  const q4_run_options_t *opts, void *stream);
 
 /* Epilogues of q4gemv_fused_run. */
 #define Q4_EPILOGUE_NONE 0
@@ -120,6 +180,13 @@ Q4_API int q4gemv_fused_run(const void *codes, const void *scales_f16, const voi
                      const float *x, const float *gamma, float eps, float *y, int32_t M, int64_t N,
                      int64_t K, int32_t group, int32_t epilogue, void *stream);
 
+/* q4gemv_fused_run with per-call options (as q4gemv_run_ex; Q4_RUN_EXACT_X selects the
+ * general kernel's fused instances). */
+Q4_API int q4gemv_fused_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                        const float *x, const float *gamma, float eps, float *y, int32_t M, int64_t N,
+                        int64_t K, int32_t group, int32_t epilogue, const q4_run_options_t *opts,
+                        void *stream);
+
 /* One matrix of a grouped GEMV: its packed weights (as for q4gemv_run), its own input
  * x[K] (device, 16-byte aligned) and output y[N] (device, 4-byte aligned), N >= 0 rows
  * (N == 0: skipped, pointers unused). */
@@ -141,10 +208,18 @@ typedef struct {
  * 16-byte aligned; for K = 896 at least one block of 48 rows per SM over the run) are one
  * launch, in which each matrix gets its own CTAs in proportion to its rows; the matrices
  * of any other run each go through q4gemv_run.  The outputs equal those of
- * separate calls within the GEMV's tolerance.  segs: host array of count entries (read
- * during the call only).  Every entry is checked as q4gemv_run checks its arguments
- * before anything is launched.  Asynchronous; allocates nothing. */
+ * separate calls within the GEMV's tolerance.  The matrices must be independent: no
+ * matrix's y may overlap any matrix's x, codes, scales or zeros, nor another matrix's y
+ * (checked, Q4_ERR_INVALID_ARG), so a chain such as segs[1].x == segs[0].y is two calls.
+ * segs: host array of count entries (read during the call only).  Every entry is checked
+ * as q4gemv_run checks its arguments before anything is launched.  Asynchronous;
+ * allocates nothing. */
 Q4_API int q4gemv_grouped_run(const q4gemv_segment_t *segs, int32_t count, int64_t K, int32_t group, void *stream);
+
+/* q4gemv_grouped_run with per-call options (as q4gemv_run_ex; Q4_RUN_EXACT_X runs every
+ * matrix on the CUDA-core float kernel, one launch each). */
+Q4_API int q4gemv_grouped_run_ex(const q4gemv_segment_t *segs, int32_t count, int64_t K, int32_t group,
+                          const q4_run_options_t *opts, void *stream);
 
 /* GEMV over a second weight format, Q4_0 blocks (cera wgpu_gemv_bench.rs, block
  * geometry: Q4_0 holds 32 elements in 18 bytes), 1 <= M <= 16:
@@ -165,11 +240,23 @@ Q4_API int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M
  * padded and masked).
  *   a_bf16 : device bfloat16 [M][K] activations;  c : device float [M][N]
  * Each weight is dequantised exactly to f32 and rounded once to bf16 (nearest-even)
- * before the MMA.  Q4_ERR_TIMEOUT if a bounded pipeline wait expired (the kernel then
- * stops; c is unspecified). */
+ * before the MMA, so each output carries
+ *     |c - c_exact| <= (2^-9 + 2e-6) * sum_k |w_nk a_mk| + 1e-6
+ * (a bf16 weight is within 2^-9 of the exact one, then binary32 accumulation).  This is
+ * up to twice the 1e-3 relative term of the GEMVs' stated tolerance; on prefill-shaped
+ * data (K >= 2048, random signs) the errors cancel and the outputs meet it, but not for
+ * every input.  The wait bound is the process-wide q4gemm_set_wait_timeout_ns value.
+ * Q4_ERR_TIMEOUT if a bounded pipeline wait expired (the kernel then stops; c is
+ * unspecified). */
 Q4_API int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
                const void *a_bf16, float *c, int32_t M, int64_t N, int64_t K, int32_t group,
                void *stream);
+
+/* q4gemm_run with per-call options (opts may be NULL).  Only Q4_RUN_WAIT_TIMEOUT
+ * applies; any other flag or a nonzero reserved field is Q4_ERR_INVALID_ARG. */
+Q4_API int q4gemm_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
+                  const void *a_bf16, float *c, int32_t M, int64_t N, int64_t K, int32_t group,
+                  const q4_run_options_t *opts, void *stream);
 
 /* Dense f32 GEMV control (cera wgpu_gemv_bench.rs, the F32 row kept in the table as the
  * harness control): y[m][n] = sum_k W[n][k] * x[m][k], 1 <= M <= 16, K % 4 == 0.
@@ -190,11 +277,12 @@ Q4_API const char *q4gemv_last_cuda_error(void);
  * Q4_ERR_CUDA if synchronising failed.  Host-blocking. */
 Q4_API int q4gemv_device_status(void *stream);
 
-/* Upper bound, in nanoseconds, on each wait of the tensor-core pipeline and of the
- * TMA-streamed GEMV for
- * launches made after this call (default 1e9).  0 makes every wait that is not
- * already satisfied give up at once, which exercises the timeout path without a
- * fault.  Process-wide; not synchronised with launches in flight. */
+/* Process-wide default bound, in nanoseconds, on each wait of the tensor-core pipelines
+ * and of the TMA-streamed GEMV, for later launches by the entry points without options
+ * (default 1e9).  0 makes every wait that is not already satisfied give up at once,
+ * which exercises the timeout path without a fault.  Not synchronised with launches in
+ * flight; a caller that shares the process should pass Q4_RUN_WAIT_TIMEOUT to the *_ex
+ * entry points instead. */
 Q4_API int q4gemm_set_wait_timeout_ns(uint64_t ns);
 
 /* Overlapped launch of the M <= 2 GEMV kernels (programmatic dependent launch).
@@ -208,7 +296,9 @@ Q4_API int q4gemm_set_wait_timeout_ns(uint64_t ns);
  * the kernel that immediately precedes it in the stream (copies and allocations are
  * not affected).  The pages describe one launch per dispatch and have no counterpart;
  * this is a launch policy of this implementation.  Default 0.  Process-wide; it
- * applies to launches made after the call.  Returns the previous setting (0 or 1). */
+ * applies to later launches by the entry points without options (a caller that shares
+ * the process should pass Q4_RUN_OVERLAPPED to the *_ex entry points instead).
+ * Returns the previous setting (0 or 1). */
 Q4_API int q4gemv_set_overlapped_launch(int enable);
 
 /* ---- test and measurement exports (not part of the GEMV API proper) ---------------- */

@@ -60,6 +60,21 @@ int main(void)
         expect(q4gemv_grouped_run(segs, 2, 100, 32, NULL) == Q4_ERR_INVALID_ARG, "grouped: K % g != 0");
     }
 
+    {   /* per-call options: checked before the arguments; outputs may not overlap inputs */
+        q4_run_options_t bad = {0x80u, 0u, 0u}, reserved = {0u, 1u, 0u};
+        q4_run_options_t good = {Q4_RUN_OVERLAPPED | Q4_RUN_EXACT_X | Q4_RUN_WAIT_TIMEOUT, 0u, 1000u};
+        q4_run_options_t exact = {Q4_RUN_EXACT_X, 0u, 0u};
+        char *const B = (char *)(uintptr_t)0x10000000;
+        expect(q4gemv_run_ex(A, A, NULL, F, F, 1, 64, 64, 32, &bad, NULL) == Q4_ERR_INVALID_ARG, "unknown flag");
+        expect(q4gemv_run_ex(A, A, NULL, F, F, 1, 64, 64, 32, &reserved, NULL) == Q4_ERR_INVALID_ARG,
+               "reserved field");
+        expect(q4gemv_run_ex(A, A, NULL, F, F, 17, 64, 64, 32, &good, NULL) == Q4_ERR_UNSUPPORTED, "ex: M > 16");
+        expect(q4gemm_run_ex(A, A, NULL, A, F, 128, 64, 64, 32, &exact, NULL) == Q4_ERR_INVALID_ARG,
+               "gemm: exact-x flag");
+        expect(q4gemv_run_ex(B, B + 0x100000, NULL, (const float *)(B + 0x200000), (float *)(B + 0x200000), 1, 64,
+                             64, 32, NULL, NULL) == Q4_ERR_INVALID_ARG, "y on x");
+    }
+
     /* empty problems: Q4_OK, pointers unused */
     expect(q4gemv_run(NULL, NULL, NULL, NULL, NULL, 0, 64, 64, 32, NULL) == Q4_OK, "M = 0");
     expect(q4gemv_run(NULL, NULL, NULL, NULL, NULL, 3, 0, 64, 32, NULL) == Q4_OK, "N = 0");

@@ -132,6 +132,76 @@ def test_grouped_argument_checks(L):
     assert r((S * 2)(S(A, A, None, A, A, 4), S(A + 8, A, None, A, A, 4)), 2, 896, 32, None) == q4.Q4_ERR_MISALIGNED
 
 
+# disjoint aligned address ranges, 1 MiB apart, never dereferenced (every call below
+# fails a host check before the first CUDA call)
+B0, B1, B2, B3, B4, B5 = (0x10000000 + i * 0x100000 for i in range(6))
+
+
+def test_outputs_must_not_overlap_inputs(L):
+    r = L.q4gemv_run
+    M, N, K, g = 1, 64, 64, 32
+    # y on x, on the codes, on the scales, on the zero points; y ending where x starts is fine
+    # (that call would launch, so it is not made here: the overlap rules are the checks)
+    assert r(B0, B1, B2, B3, B3, M, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(B0, B1, B2, B3, B0 + 16, M, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(B0, B1, B2, B3, B1, M, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(B0, B1, B2, B3, B2, M, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    # the last byte of x (4 M K bytes from B3) overlapping the first of y
+    assert r(B0, B1, B2, B3, B3 + 4 * K - 4, M, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    f = L.q4gemv_fused_run
+    assert f(B0, B1, None, B3, B4, 1e-6, B4 + 64, 1, N, K, g, q4.Q4_EPILOGUE_NONE, None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4_0_gemv_run(B0, B3, B0 + 32, 1, N, K, None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemm_run(B0, B1, None, B3, B3 + 64, 128, N, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    assert L.f32gemv_run(B0, B3, B0 + 4 * N * K - 4, 1, N, K, None) == q4.Q4_ERR_INVALID_ARG
+
+
+def test_grouped_matrices_must_be_independent(L):
+    r = L.q4gemv_grouped_run
+    S = q4._Segment
+    K, g, N = 896, 32, 64
+    # a chain: matrix 1 reads the output of matrix 0
+    chain = (S * 2)(S(B0, B1, None, B2, B3, N), S(B4, B5, None, B3, B3 + 0x1000, N))
+    assert r(chain, 2, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    # matrix 0 writes over matrix 1's codes, or over its output
+    over_w = (S * 2)(S(B0, B1, None, B2, B4 + 64, N), S(B4, B5, None, B2, B3, N))
+    assert r(over_w, 2, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    over_y = (S * 2)(S(B0, B1, None, B2, B3, N), S(B4, B5, None, B2, B3 + 128, N))
+    assert r(over_y, 2, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    # an empty entry takes no part in the check
+    empty = (S * 2)(S(B0, B1, None, B2, B3, 0), S(B4, B5, None, B2, B3, N))
+    with_alias = (S * 2)(S(B0, B1, None, B2, B2, 0), S(B4, B5, None, B2, B2, N))
+    assert r(with_alias, 2, K, g, None) == q4.Q4_ERR_INVALID_ARG
+    del empty
+
+
+def test_per_call_options_are_checked(L):
+    O = q4._RunOptions
+    ok = (B0, B1, None, B3, B4, 1, 64, 64, 32)
+    # an unknown flag or a nonzero reserved field is rejected before anything else
+    assert L.q4gemv_run_ex(*ok, ctypes.byref(O(0x80, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemv_run_ex(*ok, ctypes.byref(O(0, 1, 0)), None) == q4.Q4_ERR_INVALID_ARG
+    # the matmul takes only the wait bound
+    gm = (B0, B1, None, B3, B4, 128, 64, 64, 32)
+    assert L.q4gemm_run_ex(*gm, ctypes.byref(O(q4.Q4_RUN_EXACT_X, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemm_run_ex(*gm, ctypes.byref(O(q4.Q4_RUN_OVERLAPPED, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
+    # valid options, then the usual argument checks
+    good = ctypes.byref(O(q4.Q4_RUN_OVERLAPPED | q4.Q4_RUN_EXACT_X | q4.Q4_RUN_WAIT_TIMEOUT, 0, 5))
+    assert L.q4gemv_run_ex(B0, B1, None, B3, B4, 17, 64, 64, 32, good, None) == q4.Q4_ERR_UNSUPPORTED
+    assert L.q4gemv_run_ex(B0, B1, None, B3, B3, 1, 64, 64, 32, None, None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemv_run_ex(None, None, None, None, None, 0, 64, 64, 32, good, None) == q4.Q4_OK
+    assert L.q4gemv_fused_run_ex(B0, B1, None, B3, None, 0.0, B4, 1, 63, 64, 32, q4.Q4_EPILOGUE_SWIGLU, good,
+                                 None) == q4.Q4_ERR_INVALID_ARG
+    S = q4._Segment
+    assert L.q4gemv_grouped_run_ex((S * 1)(S(B0, B1, None, B2, B3, 4)), 1, 96, 64, good, None) == \
+        q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemm_run_ex(B0, B1, None, B3 + 2, B4, 128, 64, 64, 32, None, None) == q4.Q4_ERR_MISALIGNED
+    # the binding's form
+    with pytest.raises(q4.Q4Error):
+        q4.q4gemv_run_ex(B0, B1, None, B3, B4, 1, 64, 64, 32, flags=0x100, stream=0)
+    assert q4.q4gemv_run_ex(B0, B1, None, B3, B4, 1, 64, 64, 32, flags=0, _reserved=3, stream=0,
+                            check=False) == q4.Q4_ERR_INVALID_ARG
+
+
 def test_q40_argument_checks(L):
     r = L.q4_0_gemv_run
     assert r(A, A, A, 1, 64, 48, None) == q4.Q4_ERR_INVALID_ARG      # K not a multiple of 32

@@ -127,13 +127,28 @@ def test_bounded_wait_reports_timeout_without_fault(torch):
     w = synth.q4_weights(4, 512, 2048, 32)
     a = synth.activations_bf16(4, 256, 2048)
     c = torch.zeros((256, 512), dtype=torch.float32, device="cuda")
+    # the bound is this call's own option: nothing process-wide changes
+    q4.q4gemm_run_ex(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c,
+                     256, 512, 2048, 32, wait_timeout_ns=0)
+    st = q4.q4gemv_device_status()
+    assert st == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK          # flag cleared
+    check_case(torch, w, a)                                # and the next call is correct
+
+
+def test_process_wide_wait_bound_still_applies_to_calls_without_options(torch):
+    # the setter keeps its meaning for q4gemm_run; a call with options ignores it
+    w = synth.q4_weights(4, 512, 2048, 32)
+    a = synth.activations_bf16(4, 256, 2048)
+    c = torch.zeros((256, 512), dtype=torch.float32, device="cuda")
+    args = (dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c, 256, 512, 2048, 32)
     try:
         q4.q4gemm_set_wait_timeout_ns(0)
-        q4.q4gemm_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c,
-                      256, 512, 2048, 32)
+        q4.q4gemm_run_ex(*args, flags=0)          # built-in 1 s bound: completes
+        assert q4.q4gemv_device_status() == q4.Q4_OK
+        q4.q4gemm_run(*args)                      # the process-wide bound of 0: gives up
         st = q4.q4gemv_device_status()
     finally:
         q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
     assert st == q4.Q4_ERR_TIMEOUT
-    assert q4.q4gemv_device_status() == q4.Q4_OK          # flag cleared
-    check_case(torch, w, a)                                # and the next call is correct
+    check_case(torch, w, a)

@@ -202,13 +202,9 @@ def test_streamed_kernel_bounded_wait_reports_timeout_without_fault(torch):
     w = synth.q4_weights(21, N, 896, 32)
     x = synth.activations_f32(21, 1, 896)
     y = torch.zeros((1, N), dtype=torch.float32, device="cuda")
-    try:
-        q4.q4gemm_set_wait_timeout_ns(0)
-        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
-                      1, N, 896, 32)
-        st = q4.q4gemv_device_status()
-    finally:
-        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    q4.q4gemv_run_ex(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                     1, N, 896, 32, wait_timeout_ns=0)
+    st = q4.q4gemv_device_status()
     assert st == q4.Q4_ERR_TIMEOUT
     assert q4.q4gemv_device_status() == q4.Q4_OK
     y2 = run_gemv(torch, w, x)

@@ -83,6 +83,10 @@ def test_other_paths(torch):
     # eight and three), and an empty entry: every matrix still right
     for K, specs in [(1024, [(4096, False), (300, False)]),
                      (896, [(5000, False), (700, True), (64, False)]),
+                     # well over one block of rows per SM at K = 896, and K = 4096 (no block
+                     # rule): only the mixed zero-point presence sends these down the fallback
+                     (896, [(6000, False), (3000, True), (4864, False)]),
+                     (4096, [(4096, True), (300, False), (1000, True)]),
                      (896, [(2000 + 97 * i, False) for i in range(11)])]:
         hw, hx, segs, bufs = make(torch, specs, K, 32, K + len(specs))
         segs.insert(1, (None, None, None, None, None, 0))
@@ -101,6 +105,20 @@ def test_grouped_deterministic(torch):
     torch.cuda.synchronize()
     for a, b in zip(first, bufs):
         np.testing.assert_array_equal(a, host(b))
+
+
+def test_dependent_matrices_rejected_without_launch(torch):
+    # a chain (the second matrix reads the first's output) is not one grouped launch: the
+    # call is refused before anything runs
+    w = synth.q4_weights(4, 4864, 896, 32)
+    a = (dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch))
+    x = torch.zeros((1, 896), dtype=torch.float32, device="cuda")
+    y0 = torch.full((4864,), 7.0, dtype=torch.float32, device="cuda")
+    y1 = torch.full((4864,), 7.0, dtype=torch.float32, device="cuda")
+    st = q4.q4gemv_grouped_run([(*a, x, y0, 4864), (*a, y0[:896], y1, 4864)], 896, 32, check=False)
+    assert st == q4.Q4_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert np.all(host(y0) == 7.0) and np.all(host(y1) == 7.0), "a rejected call launched work"
 
 
 def test_empty_and_invalid(torch):

@@ -1,8 +1,9 @@
 """Overlapped (programmatic dependent) launch of the GEMV kernels.
 
-With q4gemv_set_overlapped_launch(1) a GEMV may start streaming its weights
-while the kernel before it in the stream still runs, and must wait for that
-kernel before it reads x or writes y.  These tests run chains in which the y of
+With the Q4_RUN_OVERLAPPED option of q4gemv_run_ex (or the process-wide
+q4gemv_set_overlapped_launch(1) for q4gemv_run) a GEMV may start streaming its
+weights while the kernel before it in the stream still runs, and must wait for
+that kernel before it reads x or writes y.  These tests run chains in which the y of
 one call is the x of the next, so a read of x that does not wait sees the
 previous contents of the buffer (NaN, or the previous pass's values) and the
 stage disagrees with the oracle evaluated on the GPU's actual input.
@@ -70,9 +71,15 @@ class Chain:
     def inp(self, i):
         return self.x0 if self.src[i] < 0 else self.ys[self.src[i]]
 
-    def launch(self, stream=None):
+    def launch(self, stream=None, per_call=True):
+        """The chain; per_call: each launch overlapped by its own option, else through
+        q4gemv_run and whatever the process-wide setting is."""
         for i, ((N, K, g), (c, s, z)) in enumerate(zip(self.stages, self.dw)):
-            q4.q4gemv_run(c, s, z, self.inp(i), self.ys[i], 1, N, K, g, stream=stream)
+            if per_call:
+                q4.q4gemv_run_ex(c, s, z, self.inp(i), self.ys[i], 1, N, K, g, flags=q4.Q4_RUN_OVERLAPPED,
+                                 stream=stream)
+            else:
+                q4.q4gemv_run(c, s, z, self.inp(i), self.ys[i], 1, N, K, g, stream=stream)
 
     def check(self, seed):
         """Every stage against the oracle on the input the GPU actually held."""
@@ -98,7 +105,7 @@ def test_overlapped_launch_is_off_by_default_and_toggles(torch):
 
 @pytest.mark.parametrize("symmetric", [False, True])
 @pytest.mark.parametrize("stages", [CHAIN_05B, CHAIN_8B], ids=["0.5b", "8b"])
-def test_dependent_chain_eager(torch, overlapped, stages, symmetric):
+def test_dependent_chain_eager(torch, stages, symmetric):
     ch = Chain(torch, stages, 40 + len(stages), symmetric)
     for rep in range(2):
         # a new x0 each pass: a stage that read its input before the previous stage
@@ -109,7 +116,17 @@ def test_dependent_chain_eager(torch, overlapped, stages, symmetric):
         ch.check(500 + rep)
 
 
-def test_dependent_chain_in_cuda_graph(torch, overlapped):
+def test_dependent_chain_process_wide_setting(torch, overlapped):
+    # q4gemv_run under the process-wide setting behaves as the per-call option does
+    ch = Chain(torch, CHAIN_05B, 45, False)
+    for rep in range(2):
+        ch.x0.copy_(torch.from_numpy(synth.activations_f32(330 + rep, 1, CHAIN_05B[0][1])).cuda())
+        ch.launch(per_call=False)
+        torch.cuda.synchronize()
+        ch.check(530 + rep)
+
+
+def test_dependent_chain_in_cuda_graph(torch):
     ch = Chain(torch, CHAIN_05B, 61, False)
     s = torch.cuda.Stream()
     ch.x0.zero_()

@@ -143,13 +143,9 @@ def test_bounded_wait_reports_timeout_without_fault(torch):
     w = synth.q4_weights(21, N, K, 32, tag="tc-timeout")
     x = synth.activations_f32(22, 4, K)
     y = torch.zeros((4, N), dtype=torch.float32, device="cuda")
-    try:
-        q4.q4gemm_set_wait_timeout_ns(0)
-        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
-                      4, N, K, 32)
-        st = q4.q4gemv_device_status()
-    finally:
-        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    q4.q4gemv_run_ex(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y,
+                     4, N, K, 32, wait_timeout_ns=0)
+    st = q4.q4gemv_device_status()
     assert st == q4.Q4_ERR_TIMEOUT
     assert q4.q4gemv_device_status() == q4.Q4_OK   # the flag was cleared
     rows = [0, 1, 4095, 77777, N - 1]
@@ -187,12 +183,9 @@ def test_split_k_bounded_wait_reports_timeout_without_fault(torch):
     w = synth.q4_weights(23, N, K, 128, tag="tc-split-timeout")
     x = synth.activations_f32(24, 8, K)
     y = torch.zeros((8, N), dtype=torch.float32, device="cuda")
-    try:
-        q4.q4gemm_set_wait_timeout_ns(0)
-        q4.q4gemv_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y, 8, N, K, 128)
-        st = q4.q4gemv_device_status()
-    finally:
-        q4.q4gemm_set_wait_timeout_ns(1_000_000_000)
+    q4.q4gemv_run_ex(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(x, torch), y, 8, N, K, 128,
+                     wait_timeout_ns=0)
+    st = q4.q4gemv_device_status()
     assert st == q4.Q4_ERR_TIMEOUT
     assert q4.q4gemv_device_status() == q4.Q4_OK
     check(torch, w, x, "after timeout (split)")
