@@ -1,28 +1,33 @@
 #!/usr/bin/env python3
 """Benchmark: int4 decode GEMV achieved HBM bandwidth on one GB300 (and N replicas).
 
-One step = one pass of the decode projection set of a 0.5B-class transformer
-at M = 1, group 32 (q, k, v, gate, up, down, LM head), each projection one
-q4gemv_run call through the C ABI.  The metric is the bytes those seven GEMVs
-must move (codes + scales + zero points + x + y) divided by the step time.
+One step = one pass of the decode projection set of an 8B-class transformer at
+M = 1, group 128 (qo_proj 4096x4096, gate_up_proj 14336x4096, down_proj
+4096x14336, LM head 128256x4096), each projection one q4gemv_run call through
+the C ABI.  The metric is the bytes those four GEMVs must move (codes + scales
++ zero points + x + y) divided by the step time; the per-GEMV microseconds per
+call are reported beside it.  The 0.5B-class set (seven projections, group 32)
+is timed in the detail.
 
 Timing method (after the harness lessons of cera's wgpu_gemv_bench.rs and the
 Refractometer page):
   * the K timed steps are back-to-back launches on one stream, captured once in
     a CUDA graph and replayed, bracketed by CUDA events on that stream with a
     device synchronise (and a barrier across ranks) on both sides;
+  * that timed region of exactly K steps is repeated (at least --samples times
+    and for at least --sample-seconds); the value is the median region, with
+    p10 / p90 beside it (the Refractometer's median and p10-p90 over samples;
+    cera's "medians of several runs");
   * every step uses the next of several weight replicas whose total is several
     times the 129 MB L2, so each step streams its weights from HBM;
   * W untimed warm-up steps run first;
-  * external event nodes inside the graph bracket the LM-head launch of every
-    n-th step (--event-stride), which gives the dominant kernel's duration for
-    its roofline figure; per-projection microseconds come from separate graphs
-    of back-to-back launches;
+  * per-projection microseconds come from separate graphs of back-to-back
+    launches (median of --samples replays, with t(2n)/t(n) as the ITERS check);
   * by default the GEMVs are launched overlapped (programmatic dependent
     launch: a kernel streams its weights while the previous one finishes and
     waits for it before reading x); --overlap 0 serialises them;
   * SM clocks and throttle reasons are sampled with nvidia-smi during the
-    timed region.
+    timed regions.
 
 `--impl reference` times the CPU oracle (the plain C restatement of the
 method) on the host cores instead; there is no other reference implementation
@@ -50,16 +55,20 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
+HEADLINE = synth.DECODE_8B   # the timed step: its projections at M = 1
+
 METRIC = "int4 GEMV achieved HBM GB/s (% of GB300 peak) and µs/call at M=1, 1 GPU"
 UNIT = "GB/s"
-WORKLOAD = "decode projection set of a 0.5B-class transformer, M=1, group=32"
+WORKLOAD = ("decode projection set of an 8B-class transformer, M=1, group=128 (qo_proj 4096x4096, "
+            "gate_up_proj 14336x4096, down_proj 4096x14336, lm_head 128256x4096)")
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu capture of
 # the instance below on the LM-head shape (see profiles/); None once the kernel changes.
-DOMINANT_KERNEL = "q4gemv_stream_kernel<K=896, g=32, RG=8, U=6, ASYM> (48-row blocks, 2 ring slots, 3 CTAs per SM)"
-DOMINANT_TRAFFIC_BYTES = 78_731_776 + 1_214_720
+DOMINANT_KERNEL = ("q4gemv_stream_kernel<K=4096, g=128, RG=4, U=8, ASYM> (32-row blocks, 3 ring slots, "
+                   "1 CTA per SM)")
+DOMINANT_TRAFFIC_BYTES = 272_976_128 + 3_917_056
 
 
 def algorithmic_bytes(M, N, K, group, symmetric=False):
@@ -232,6 +241,76 @@ def make_weights(shapes, group, scale, seed=2024):
             for i, (name, N, K) in enumerate(shapes)]
 
 
+class StepSet:
+    """One decode projection set on the device: its host weights (for the oracle legs),
+    rotating device replicas whose total exceeds the L2 several times (every step streams
+    its weights from HBM), one x and one y per projection (M = 1)."""
+
+    def __init__(self, torch, spec, rotate_bytes, seed=2024):
+        self.shapes = spec["shapes"]
+        self.group = spec["group"]
+        self.ws = make_weights(self.shapes, self.group, spec["scale"], seed)
+        self.replica_bytes = sum(w.nbytes for w in self.ws)
+        self.replicas = max(2, -(-rotate_bytes // self.replica_bytes))
+        self.reps = [[(to_dev(torch, w.codes), to_dev(torch, w.scales), to_dev(torch, w.zeros)) for w in self.ws]
+                     for _ in range(self.replicas)]
+        self.xs_host = [synth.activations_f32(77 + i, 1, K) for i, (_, _, K) in enumerate(self.shapes)]
+        self.xs = [to_dev(torch, x) for x in self.xs_host]
+        self.ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in self.shapes]
+        self.bytes_per_step = step_bytes(self.shapes, 1, self.group)
+
+    def step(self, q4, r, stream):
+        for p, (name, N, K) in enumerate(self.shapes):
+            c, sc, z = self.reps[r][p]
+            q4.q4gemv_run(c, sc, z, self.xs[p], self.ys[p], 1, N, K, self.group, stream=stream)
+
+
+def to_dev(torch, a):
+    if a is None:
+        return None
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def capture_steps(torch, stream, step, n, offset, replicas):
+    """A CUDA graph of n back-to-back steps over the rotating replicas."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            step((offset + i) % replicas)
+    return g
+
+
+def quantiles(v):
+    t = sorted(v)
+    q = lambda f: t[min(len(t) - 1, max(0, int(round(f * (len(t) - 1)))))]
+    return {"median": statistics.median(t), "p10": q(0.1), "p90": q(0.9), "min": t[0], "max": t[-1],
+            "mean": statistics.fmean(t)}
+
+
+def timed_regions(torch, stream, dist, run_region, min_samples, min_seconds, max_samples=20000):
+    """Repeat the timed region (exactly K steps, issued by run_region) at least min_samples
+    times and for at least min_seconds: each sample is bracketed by a barrier and a device
+    synchronise on both sides and timed by CUDA events on the launching stream; its time
+    is the maximum over ranks.  Returns the per-sample milliseconds and the host-clock
+    window they span."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ms = []
+    t0 = time.monotonic()
+    while len(ms) < max_samples and (len(ms) < min_samples or time.monotonic() - t0 < min_seconds):
+        barrier(dist)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            run_region()
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        ms.append(reduce_over_ranks(dist, start.elapsed_time(end), "max", device="cuda"))
+    return ms, t0, time.monotonic()
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import gemm_decode_gb300 as q4
@@ -240,74 +319,36 @@ def run_gpu(args, rank, world, local_rank):
     dist = dist_init(world, "nccl")
     q4.lib()
     q4.q4gemv_set_overlapped_launch(bool(args.overlap))
-    shapes = synth.DECODE_05B["shapes"]
-    group = synth.DECODE_05B["group"]
-    ws = make_weights(shapes, group, synth.DECODE_05B["scale"])
-    per_step_weight_bytes = sum(w.nbytes for w in ws)
-    replicas = max(2, -(-args.rotate_bytes // per_step_weight_bytes))
-
-    def to_dev(a):
-        if a is None:
-            return None
-        if a.dtype == np.uint16:
-            a = a.view(np.int16)
-        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
-
-    reps = []
-    for _ in range(replicas):
-        reps.append([(to_dev(w.codes), to_dev(w.scales), to_dev(w.zeros)) for w in ws])
-    xs_host = [synth.activations_f32(77 + i, 1, K) for i, (_, _, K) in enumerate(shapes)]
-    xs = [to_dev(x) for x in xs_host]
-    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in shapes]
-
+    S = StepSet(torch, HEADLINE, args.rotate_bytes)
+    shapes, group, replicas = S.shapes, S.group, S.replicas
     stream = torch.cuda.Stream()
-    ev = GraphEvents(torch)
-
     LM = len(shapes) - 1   # the dominant launch: the LM head
 
-    def one_step(r, s, events=None, i_step=0, only=None):
-        for p, ((name, N, K), w) in enumerate(zip(shapes, ws)):
-            c, sc, z = reps[r][p]
-            timed = events is not None and (only is None or p == only)
-            if timed:
-                ev.record(events[i_step][p][0], s)
-            q4.q4gemv_run(c, sc, z, xs[p], ys[p], 1, N, K, group, stream=s)
-            if timed:
-                ev.record(events[i_step][p][1], s)
-
-    # eager pass (also sets kernel attributes before any capture)
+    # eager pass over every replica (also sets kernel attributes before any capture)
     with torch.cuda.stream(stream):
         for r in range(replicas):
-            one_step(r, stream)
+            S.step(q4, r, stream)
     torch.cuda.synchronize()
 
-    chunk = min(args.steps, max(replicas, args.graph_steps))
-    chunk = max(1, chunk)
-    reps_timed = args.steps // chunk
-    tail = args.steps - reps_timed * chunk
-    events = [[(ev.new(), ev.new()) for _ in shapes] for _ in range(chunk)]
-    # LM-head launches bracketed by event nodes: every stride-th step of the timed graph
-    # (an event node costs a bubble and breaks the launch overlap around it)
-    stride = max(1, min(args.event_stride, chunk))
-    sampled = list(range(0, chunk, stride))
+    # the timed region: exactly K steps, as replays of a graph of `chunk` steps (plus a tail)
+    chunk = max(1, min(args.steps, max(replicas, args.graph_steps)))
+    full, tail = divmod(args.steps, chunk)
+    step = lambda r: S.step(q4, r, stream)
+    g_main = capture_steps(torch, stream, step, chunk, 0, replicas)
+    g_tail = capture_steps(torch, stream, step, tail, full * chunk, replicas) if tail else None
 
-    def capture(n, with_events, offset=0, only=LM):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
-                timed = with_events and i % stride == 0
-                one_step((offset + i) % replicas, stream, events if timed else None, i, only)
-        return g
+    def region():
+        for _ in range(full):
+            g_main.replay()
+        if g_tail is not None:
+            g_tail.replay()
 
-    g_main = capture(chunk, True)
-    g_tail = capture(tail, False, offset=chunk * reps_timed) if tail else None
-
-    # warm-up: exactly W steps (a graph of min(W, chunk) steps, replayed, plus a remainder)
+    # warm-up: exactly W steps
     if args.warmup:
         wn = min(args.warmup, chunk)
-        g_warm = capture(wn, False)
+        g_warm = capture_steps(torch, stream, step, wn, 0, replicas)
         wfull, wtail = divmod(args.warmup, wn)
-        g_wtail = capture(wtail, False) if wtail else None
+        g_wtail = capture_steps(torch, stream, step, wtail, 0, replicas) if wtail else None
         with torch.cuda.stream(stream):
             for _ in range(wfull):
                 g_warm.replay()
@@ -317,93 +358,85 @@ def run_gpu(args, rank, world, local_rank):
 
     sampler = ClockSampler(smi_index(local_rank)).start()
     time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    t0 = time.monotonic()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(reps_timed):
-            g_main.replay()
-        if g_tail is not None:
-            g_tail.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
-    t1 = time.monotonic()
-    barrier(dist)
+    samples_ms, t0, t1 = timed_regions(torch, stream, dist, region, args.samples, args.sample_seconds)
     clocks = sampler.stop(t0, t1)
-    ms_total = start.elapsed_time(end)
-    ms_total_max = reduce_over_ranks(dist, ms_total, "max", device="cuda")
+    qs = quantiles(samples_ms)
+    ms_region = qs["median"]
+    total_bytes = S.bytes_per_step * args.steps * world
+    value = total_bytes / (ms_region * 1e-3) / 1e9
+    gbs_of = lambda ms: round(total_bytes / (ms * 1e-3) / 1e9, 2)
 
-    # the dominant launch's duration: event nodes around each LM-head launch of the
-    # last replay of the timed graph (the only event nodes in it)
-    lm_us = statistics.fmean(ev.elapsed_ms(events[i][LM][0], events[i][LM][1]) * 1e3 for i in sampled)
-    # per-projection microseconds per call: for each projection, one graph of back-to-back
-    # launches over the rotating replicas, timed from outside (no event nodes between
-    # launches; event nodes cost a bubble of about a microsecond or more each)
-    per_proj = []
-    n_pp = max(replicas, min(args.steps, 200))
-    for p, (name, N, K) in enumerate(shapes):
-        per_proj.append(_time_back_to_back(torch, q4, stream, [r[p] for r in reps], xs[p], ys[p], 1, N, K, group,
-                                           n_pp))
-    bytes_per_step = step_bytes(shapes, 1, group)
-    total_bytes = bytes_per_step * args.steps * world
-    value = total_bytes / (ms_total_max * 1e-3) / 1e9
-    ms_per_step = ms_total_max / args.steps
+    # per-GEMV microseconds per call: for each projection, a graph of back-to-back launches
+    # over the rotating replicas (no event nodes between launches), 25 timed replays
+    n_pp = max(replicas, min(args.steps, 200), 40)
+    per_proj = [_time_back_to_back(torch, q4, stream, [r[p] for r in S.reps], S.xs[p], S.ys[p], 1, N, K, group,
+                                   n_pp, samples=args.samples)
+                for p, (name, N, K) in enumerate(shapes)]
+
+    # the dominant launch inside the step: event nodes around every LM-head launch of a
+    # separate (untimed) graph of steps; the nodes break the launch overlap around them
+    ev = GraphEvents(torch)
+    n_ev = min(chunk, 50)
+    events = [(ev.new(), ev.new()) for _ in range(n_ev)]
+    g_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ev, stream=stream):
+        for i in range(n_ev):
+            for p, (name, N, K) in enumerate(shapes):
+                c, sc, z = S.reps[i % replicas][p]
+                if p == LM:
+                    ev.record(events[i][0], stream)
+                q4.q4gemv_run(c, sc, z, S.xs[p], S.ys[p], 1, N, K, group, stream=stream)
+                if p == LM:
+                    ev.record(events[i][1], stream)
+    with torch.cuda.stream(stream):
+        g_ev.replay()
+        g_ev.replay()
+    torch.cuda.synchronize()
+    lm_in_step_us = statistics.median(ev.elapsed_ms(a, b) * 1e3 for a, b in events)
 
     peak, peak_src = load_peaks()
     lm_bytes = algorithmic_bytes(1, shapes[LM][1], shapes[LM][2], group)
-    # the dominant kernel's launch duration: CUDA events on its launching stream around
-    # a graph of back-to-back LM-head launches (rotating replicas, cold L2, overlapped
-    # launch as in the step), timed in this run right after the timed region.  The
-    # in-step figure (event nodes around sampled LM-head launches of the timed graph)
-    # is reported beside it: those nodes break the launch overlap and add a bubble.
-    lm_b2b_us = per_proj[LM]["us"]
-    achieved = lm_bytes / (lm_b2b_us * 1e-6) / 1e9
-    in_step = lm_bytes / (lm_us * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "kernel": DOMINANT_KERNEL + " on lm_head 151936x896",
+    lm_us = per_proj[LM]["us"]
+    achieved = lm_bytes / (lm_us * 1e-6) / 1e9
+    in_step = lm_bytes / (lm_in_step_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": DOMINANT_KERNEL + f" on {shapes[LM][0]} {shapes[LM][1]}x{shapes[LM][2]}",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_src,
                 "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "traffic": args.traffic_bytes if args.traffic_bytes is not None else DOMINANT_TRAFFIC_BYTES,
                 "algorithmic_bytes_per_launch": lm_bytes,
-                "duration_us": round(lm_b2b_us, 3),
+                "duration_us": round(lm_us, 3),
+                "duration_p10_p90": [round(per_proj[LM]["p10"], 3), round(per_proj[LM]["p90"], 3)],
                 "duration_source": "CUDA events on the launching stream around a graph of back-to-back "
                                    "LM-head launches (rotating replicas, cold L2, overlapped launch), "
-                                   "median of 5 replays, right after the timed region",
-                "in_step": {"us": round(lm_us, 3), "achieved": round(in_step, 1),
+                                   f"median of {args.samples} replays, right after the timed regions",
+                "in_step": {"us": round(lm_in_step_us, 3), "achieved": round(in_step, 1),
                             "frac": round(in_step / peak, 4),
-                            "how": "event nodes around the LM-head launch of every "
-                                   f"{stride}th timed step; they break the launch overlap "
-                                   "and add a bubble, so this figure is conservative"}}
+                            "how": "event nodes around every LM-head launch of a separate graph of steps; "
+                                   "they break the launch overlap and add a bubble, so this figure is "
+                                   "conservative"}}
 
     # ---- end to end: pinned host x in, pinned host y out, through the same API ----
-    e2e = run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dist)
+    e2e = run_e2e(args, torch, q4, shapes, group, S.reps, S.xs_host, replicas, stream, dist)
 
+    us_per_call = {name: round(st["us"], 3) for (name, N, K), st in zip(shapes, per_proj)}
     detail = {"projections": [
         {"name": name, "N": N, "K": K, "us_per_call": round(st["us"], 3),
          "gbs": round(algorithmic_bytes(1, N, K, group) / (st["us"] * 1e-6) / 1e9, 1),
          "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
-         "t2n_over_tn": round(st["t2n_over_tn"], 3)}
+         "t2n_over_tn": round(st["t2n_over_tn"], 3), "launches_per_sample": st["n"]}
         for (name, N, K), st in zip(shapes, per_proj)],
-        "weight_replicas": replicas, "replica_bytes": per_step_weight_bytes,
-        "graph_steps": chunk, "event_mode": ev.mode,
-        "lm_head_us_in_timed_region": round(lm_us, 3),
-        "lm_head_event_samples": f"{len(sampled)} per {chunk}-step graph (every {stride}th step)",
-        "us_per_call_note": "per projection: a graph of back-to-back launches over the rotating replicas, "
-                            "5 timed replays (median; p10, p90, min) and t(2n)/t(n) from two replays; "
-                            "the LM head's in-step time carries the event-node bubble"}
+        "weight_replicas": replicas, "replica_bytes": S.replica_bytes, "graph_steps": chunk,
+        "event_mode": ev.mode,
+        "us_per_call_note": f"per projection: a graph of back-to-back launches over the rotating replicas, "
+                            f"{args.samples} timed replays (median; p10, p90, min) and t(2n)/t(n) from two "
+                            f"replays"}
     if args.controls and rank == 0:
+        detail["decode_05b"] = run_decode_05b(args, torch, q4, stream)
         detail["controls"] = run_controls(args, torch, q4)
         detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
         detail["decode_8b"] = run_decode_8b(args, torch, q4)
-        detail["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas,
-                                                          stream)
         detail["q4_0_format"] = run_q40(args, torch, q4)
-        try:   # a detail figure: its failure is recorded, the measured step stands
-            detail["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream)
-        except Exception as e:   # noqa: BLE001
-            detail["grouped_step"] = {"error": f"{type(e).__name__}: {e}"}
 
     probe = detail.get("controls", {}).get("vec4_read_probe_1GiB", {}).get("gbs")
     if probe:   # the same kernel's rate against this GPU's own streaming read (the vec4 probe)
@@ -411,26 +444,65 @@ def run_gpu(args, rank, world, local_rank):
         roofline["read_probe_gbs"] = probe
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_region / args.steps, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4 weights (fp16 scales, u4 zeros), f32 x/accumulate/y",
-        "data": "synthetic (seeded; codes/zeros uniform 0..15, scales fp16 U[0.005,0.02], x N(0,1))",
+        "data": "synthetic (seeded; codes/zeros uniform 0..15, scales fp16 U[0.001,0.01], x N(0,1))",
         "config": {"workload": WORKLOAD, "M": 1, "group": group,
                    "shapes": [[n, N, K] for n, N, K in shapes],
-                   "bytes_per_step": bytes_per_step,
+                   "bytes_per_step": S.bytes_per_step,
                    "l2_policy": f"inputs larger than L2: {replicas} rotating weight replicas "
-                                f"({replicas * per_step_weight_bytes / 1e6:.0f} MB > 129 MB L2)",
+                                f"({replicas * S.replica_bytes / 1e6:.0f} MB > 129 MB L2)",
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "launch": ("overlapped: programmatic dependent launch, each GEMV waits for the "
                               "previous kernel before reading x" if args.overlap else "serialised")},
+        "timing": {"samples": len(samples_ms), "statistic": "median over timed regions of exactly K steps",
+                   "ms_per_region": {k: round(v, 6) for k, v in qs.items()},
+                   "value_p10_p90": [gbs_of(qs["p90"]), gbs_of(qs["p10"])],
+                   "seconds_sampled": round(t1 - t0, 3)},
+        "us_per_call": us_per_call,
         "clocks": clocks, "e2e": e2e, "gpu_launches": len(shapes) * args.steps,
+        "gpu_launches_note": "per timed region (each sample is one region of K steps)",
         "roofline": roofline, "pct_of_8TBs_nominal": round(value / NOMINAL_HBM_GBS, 4),
         "detail": detail,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args, ws, xs_host, shapes, group,
-                                              gpu_outputs=[y.cpu().numpy() for y in ys])
+        result["cpu_baseline"] = cpu_baseline(args, S.ws, S.xs_host, shapes, group,
+                                              gpu_outputs=[y.cpu().numpy() for y in S.ys])
     return result, dist
+
+
+def run_decode_05b(args, torch, q4, stream):
+    """The decode projection set of a 0.5B-class model at M = 1, group 32 (seven GEMVs per
+    step): the step as a graph of back-to-back launches, each projection's microseconds per
+    call, the step with stacked q|k|v and gate|up and with the RMSNorm / SwiGLU fusions, and
+    the step as two grouped calls."""
+    S = StepSet(torch, synth.DECODE_05B, args.rotate_bytes)
+    shapes, group, replicas = S.shapes, S.group, S.replicas
+    n = max(replicas, min(args.steps, 400), 100)
+    st = _time_launches(torch, stream, lambda i: S.step(q4, i % replicas, stream), n, samples=args.samples)
+    per_proj = [_time_back_to_back(torch, q4, stream, [r[p] for r in S.reps], S.xs[p], S.ys[p], 1, N, K, group,
+                                   max(replicas, 200), samples=args.samples)
+                for p, (name, N, K) in enumerate(shapes)]
+    out = {"workload": "decode projection set of a 0.5B-class transformer, M=1, group=32",
+           "shapes": [[nm, N, K] for nm, N, K in shapes], "bytes_per_step": S.bytes_per_step,
+           "us_per_step": round(st["us"], 3), "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3),
+                                                                 round(st["min"], 3)],
+           "gbs": round(S.bytes_per_step / st["us"] / 1e3, 1), "t2n_over_tn": round(st["t2n_over_tn"], 3),
+           "steps_per_sample": n, "samples": args.samples,
+           "projections": [{"name": name, "N": N, "K": K, "us_per_call": round(p["us"], 3),
+                            "gbs": round(algorithmic_bytes(1, N, K, group) / (p["us"] * 1e-6) / 1e9, 1),
+                            "us_p10_p90_min": [round(p["p10"], 3), round(p["p90"], 3), round(p["min"], 3)],
+                            "t2n_over_tn": round(p["t2n_over_tn"], 3)}
+                           for (name, N, K), p in zip(shapes, per_proj)]}
+    out["fused_projections_step"] = run_fused_step(args, torch, q4, shapes, group, S.reps, S.xs, replicas, stream)
+    try:   # a detail figure: its failure is recorded, the measured step stands
+        out["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, S.reps, S.xs, replicas, stream)
+    except Exception as e:   # noqa: BLE001
+        out["grouped_step"] = {"error": f"{type(e).__name__}: {e}"}
+    del S
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dist):
@@ -501,18 +573,15 @@ def run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dis
             with torch.cuda.graph(gt, stream=stream):
                 for i in range(tail):
                     step((full * chunk + i) % replicas)
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            start.record(stream)
+        def region():
             for _ in range(full):
                 g.replay()
             if gt is not None:
                 gt.replay()
-            end.record(stream)
-        torch.cuda.synchronize()
-        return reduce_over_ranks(dist, start.elapsed_time(end), "max", device="cuda")
+
+        # the median of several timed regions of exactly K steps (max over ranks each)
+        ms, _, _ = timed_regions(torch, stream, dist, region, max(5, args.samples // 5), 0.0)
+        return statistics.median(ms)
 
     world = dist.get_world_size() if dist is not None else 1
     ms_copy = timed(step_copy)
@@ -539,10 +608,11 @@ def run_e2e(args, torch, q4, shapes, group, reps, xs_host, replicas, stream, dis
     def gbs(ms):
         return round(bytes_step * n * world / (ms * 1e-3) / 1e9, 2)
 
-    hows = {"copy": "CUDA graph of K steps: pinned-host x -> device copy, 7 x q4gemv_run, y -> pinned host copy",
-            "mapped": "CUDA graph of K steps; 7 x q4gemv_run reading x from and writing y to pinned host memory "
+    nl = len(shapes)
+    hows = {"copy": f"CUDA graph of K steps: pinned-host x -> device copy, {nl} x q4gemv_run, y -> pinned host copy",
+            "mapped": f"CUDA graph of K steps; {nl} x q4gemv_run reading x from and writing y to pinned host memory "
                       "(NVLink-C2C, no copy nodes)",
-            "x_copy_y_mapped": "CUDA graph of K steps: pinned-host x -> device copy, 7 x q4gemv_run writing y "
+            "x_copy_y_mapped": f"CUDA graph of K steps: pinned-host x -> device copy, {nl} x q4gemv_run writing y "
                                "straight to pinned host memory (NVLink-C2C)"}
     times = {"copy": ms_copy, "mapped": ms_mapped, "x_copy_y_mapped": ms_ymap}
     best = min(times, key=times.get) if same else "copy"
@@ -681,10 +751,12 @@ def oracle_step(ws, xs_host, shapes, group, threads, row_fraction=1.0):
 
 
 def cpu_baseline(args, ws, xs_host, shapes, group, gpu_outputs=None):
+    """The oracle timed on the host cores: full steps over all cores (row slices), then a
+    bounded sample on one core (the first rows of every projection); the all-core run's
+    outputs gate the GPU run's parity on every row."""
     threads = os.cpu_count() or 1
     t0 = time.perf_counter()
     outs, nbytes = oracle_step(ws, xs_host, shapes, group, threads)
-    dt = time.perf_counter() - t0
     steps = 1
     while time.perf_counter() - t0 < args.cpu_seconds:
         oracle_step(ws, xs_host, shapes, group, threads)
@@ -694,12 +766,24 @@ def cpu_baseline(args, ws, xs_host, shapes, group, gpu_outputs=None):
            "kind": "oracle",
            "sample": f"{steps} full step(s) of the projection set (all rows), "
                      f"{threads} threads over row slices, {dt:.1f} s wall"}
+    # one core: the first rows of every projection, sized to about --cpu-seconds
+    t0 = time.perf_counter()
+    _, b_probe = oracle_step(ws, xs_host, shapes, group, 1, 0.002)
+    est = (time.perf_counter() - t0) / 0.002
+    frac = min(1.0, max(0.002, args.cpu_seconds / max(est, 1e-9)))
+    t0 = time.perf_counter()
+    _, b1 = oracle_step(ws, xs_host, shapes, group, 1, frac)
+    dt1 = time.perf_counter() - t0
+    res["one_core"] = {"value": round(b1 / dt1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                       "sample": f"the first {frac * 100:.2f}% of the rows of every projection on one thread, "
+                                 f"{dt1:.1f} s wall"}
     if gpu_outputs is not None:
         worst = 0.0
         for (y_ref, bound), y in zip(outs, gpu_outputs):
             err = np.abs(y.astype(np.float64) - y_ref.astype(np.float64))
             worst = max(worst, float(np.max(err / (1e-3 * bound + 1e-6))))
-        res["parity_gate"] = {"max_err_over_bound": round(worst, 6), "ok": worst <= 1.0}
+        res["parity_gate"] = {"max_err_over_bound": round(worst, 6), "ok": worst <= 1.0,
+                              "rows": "every row of every projection of the step"}
     return res
 
 
@@ -712,9 +796,9 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     from concurrent.futures import ThreadPoolExecutor
-    shapes = synth.DECODE_05B["shapes"]
-    group = synth.DECODE_05B["group"]
-    ws = make_weights(shapes, group, synth.DECODE_05B["scale"])
+    shapes = HEADLINE["shapes"]
+    group = HEADLINE["group"]
+    ws = make_weights(shapes, group, HEADLINE["scale"])
     xs_host = [synth.activations_f32(77 + i, 1, K) for i, (_, _, K) in enumerate(shapes)]
     threads = os.cpu_count() or 1
     across = args.steps >= 4 * threads
@@ -765,8 +849,12 @@ def run_reference(args, rank, world):
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--samples", type=int, default=25,
+                   help="timed regions of K steps (at least), and replays per microsecond figure")
+    p.add_argument("--sample-seconds", type=float, default=2.0,
+                   help="keep repeating the timed region for at least this long (clock samples)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--graph-steps", type=int, default=400,
                    help="steps per captured CUDA graph (replayed to reach --steps)")
@@ -938,26 +1026,14 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
             c, sc, z = freps[r][p]
             q4.q4gemv_run(c, sc, z, fxs[p], fys[p], 1, N, K, group, stream=stream)
 
-    n = max(replicas, min(args.steps, 2000))
-    with torch.cuda.stream(stream):
-        for r in range(replicas):
-            step(r)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(n):
-            step(i % replicas)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
+    n = max(replicas, min(args.steps, 400), 100)
+    st = _time_launches(torch, stream, lambda i: step(i % replicas), n, samples=args.samples)
+    us = st["us"]
     byts = step_bytes(fshapes, 1, group)
     out = {"launches_per_step": len(fshapes), "shapes": [[nm, N, K] for nm, N, K in fshapes],
-           "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
+           "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts,
+           "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+           "t2n_over_tn": round(st["t2n_over_tn"], 3), "samples": st["samples"], "steps_per_sample": n}
 
     # the same four launches with the RMSNorm prologue fused into q|k|v, gate|up and the
     # LM head, and the SwiGLU combine into gate|up (its rows read as interleaved gate / up
@@ -981,21 +1057,8 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
         c, sc, z = freps[r][3]
         q4.q4gemv_fused_run(c, sc, z, fxs[3], gammas[2], 1e-6, fys[3], 1, Nl, Kl, group, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for r in range(replicas):
-            step_fused(r)
-    torch.cuda.synchronize()
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=stream):
-        for i in range(n):
-            step_fused(i % replicas)
-    with torch.cuda.stream(stream):
-        g2.replay()
-        e0.record(stream)
-        g2.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us2 = e0.elapsed_time(e1) * 1e3 / n
+    st2 = _time_launches(torch, stream, lambda i: step_fused(i % replicas), n, samples=args.samples)
+    us2 = st2["us"]
     byts2 = byts - 4 * (N_gu // 2) + 3 * 4 * K0   # gate|up writes N/2 outputs; three gamma vectors
     # each launch of the fused step alone, back to back over the replicas
     (nq, Nq, Kq), (ng, Ng, Kg), (nd, Nd, Kd), (nl, Nl, Kl) = fshapes
@@ -1039,26 +1102,14 @@ def run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream)
         for K, ps in byK.items():
             q4.q4gemv_grouped_run([(*reps[r][p], xs[p], ys[p], shapes[p][1]) for p in ps], K, group, stream=stream)
 
-    n = max(replicas, min(args.steps, 2000))
-    with torch.cuda.stream(stream):
-        for r in range(replicas):
-            step(r)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(n):
-            step(i % replicas)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / n
+    n = max(replicas, min(args.steps, 400), 100)
+    st = _time_launches(torch, stream, lambda i: step(i % replicas), n, samples=args.samples)
+    us = st["us"]
     byts = step_bytes(shapes, 1, group)
     return {"calls_per_step": len(byK), "groups": {str(K): [shapes[p][0] for p in ps] for K, ps in byK.items()},
-            "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts}
+            "us_per_step": round(us, 3), "gbs": round(byts / us / 1e3, 1), "bytes_per_step": byts,
+            "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
+            "t2n_over_tn": round(st["t2n_over_tn"], 3), "samples": st["samples"], "steps_per_sample": n}
 
 
 def run_q40(args, torch, q4):
