@@ -347,6 +347,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// The split launch (q4gemm_split.cu) for shapes whose 128 x 128 tiles leave most SMs idle.
+bool gemm_split_plan(int M, int64_t N, int K, int64_t regular, int &bn, int &split);
+int launch_q4gemm_split(const CUtensorMap &map_a, const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
+                        float *c, int M, int64_t N, int K, int group, int bn, int split, cudaStream_t stream);
+
 // Halves of A per CTA for M rows: the fewest padded rows plus dequantisation, counting
 // one dequantised weight tile as much work as 256 rows of MMA (the dequantiser warps,
 // not the tensor core, set the pace at the prefill shapes).
@@ -405,6 +410,12 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return Q4_ERR_UNSUPPORTED;
+    {   // few tiles (e.g. 128 tokens x 512 weight rows): narrower tiles with K split over a cluster
+        const int64_t regular = ((N + BN - 1) / BN) * ((M + nh * BM - 1) / (nh * BM));
+        int bn = 0, split = 1;
+        if (gemm_split_plan(M, N, K, regular, bn, split))
+            return launch_q4gemm_split(map, codes, scales, zeros, c, M, N, K, group, bn, split, stream);
+    }
     GemmArgs g;
     g.codes = codes;
     g.scales = scales;

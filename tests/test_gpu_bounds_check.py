@@ -132,3 +132,17 @@ def test_grouped_streamed_kernel(torch, K, g):
     for w, x, y in zip(ws, xs, ys):
         y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, g)
         assert_within_bound(host(y), y_ref, bound, f"grouped K={K} N={w.N}")
+
+
+@pytest.mark.parametrize("M,N,K,g", [(100, 200, 2080, 32), (300, 96, 1024, 64), (256, 1000, 4096, 128)])
+def test_split_matmul_kernel(torch, M, N, K, g):
+    # the matmul's split kernel: ragged tiles of A and of weight rows, a half-empty last
+    # K-block, 32- and 64-row tiles, 4- and 8-CTA clusters
+    w = synth.q4_weights(M + N + K, N, K, g, tag="bounds-split")
+    a = synth.activations_bf16(M + 1, M, K)
+    c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q4gemm_run(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c, M, N, K, g)
+    assert q4.q4gemv_bounds_violations() == 0, f"split matmul M={M} N={N} K={K}: out-of-range accesses counted"
+    c_ref, bound = oracle.q4_gemm(w.codes, w.scales, w.zeros, a, g)
+    err = np.abs(host(c).astype(np.float64) - c_ref.astype(np.float64))
+    assert np.all(err <= (2.0 ** -9 + 2e-6) * bound + 1e-6)
