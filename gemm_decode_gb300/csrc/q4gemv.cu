@@ -90,6 +90,8 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
     const bool exact = call_options().exact_x;
     if (!exact && stream_applies(M, N, K, group, codes, scales, zeros))
         return launch_q4gemv_stream(codes, scales, zeros, x, y, N, K, group, stream);
+    if (!exact && stream2_applies(M, N, K, group, codes, scales, zeros))
+        return launch_q4gemv_stream2(codes, scales, zeros, x, y, N, K, group, stream);
     if (!exact && tc_gemv_applies(M, N, K, codes))
         return launch_q4gemv_tc(codes, scales, zeros, x, y, M, N, K, group, stream);
     if (!exact) {

@@ -93,7 +93,21 @@ bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const
     return stream_geo_ok(g, asym);
 }
 
-// fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks)
+bool stream2_applies(int M, int64_t N, int K, int group, const void *codes, const void *scales, const void *zeros) {
+    if (M != 2 || N < 4096 || K < 2048 || K % 32 != 0) return false;
+    if (group != 32 && group != 64 && group != 128) return false;
+    if (!aligned(codes, 16) || !aligned(scales, 16) || (zeros && !aligned(zeros, 16))) return false;
+    const int rg = stream_rg(K);
+    if (rg == 0) return false;
+    const bool asym = zeros != nullptr;
+    const int u = stream_u(K);
+    const StreamGeo g = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, false, 2), asym, false,
+                                        false, 2);
+    return stream_geo_ok(g, asym);
+}
+
+// fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks),
+// 16 two rows of x
 static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                              const float *gamma, float eps, int swiglu, int fuse, float *y, int64_t N, int K,
                              int group, cudaStream_t stream) {
@@ -117,8 +131,9 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
     if (a.status == nullptr) return Q4_ERR_CUDA;
     const int u = stream_u(K);
     const bool q40 = fuse == 4;
-    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, q40), asym, fuse == 1 || fuse == 3,
-                            q40);
+    const int mx = fuse == 16 ? 2 : 1;
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, q40, mx), asym, fuse == 1 || fuse == 3,
+                            q40, mx);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
     switch (K) {
@@ -129,6 +144,8 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
         case 16384: return launch_stream_k16384(a, group, asym, fuse, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
             if (fuse == 4) return launch_stream<0, 0, 0, 8, false, 4>(a, stream);
+            if (fuse == 16)
+                return asym ? launch_stream<0, 0, 0, 8, true, 16>(a, stream) : launch_stream<0, 0, 0, 8, false, 16>(a, stream);
             if (fuse == 3)
                 return asym ? launch_stream<0, 0, 0, 8, true, 3>(a, stream) : launch_stream<0, 0, 0, 8, false, 3>(a, stream);
             if (fuse == 1)
@@ -140,6 +157,11 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
 int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                          float *y, int64_t N, int K, int group, cudaStream_t stream) {
     return launch_stream_any(codes, scales, zeros, x, nullptr, 0.0f, 0, 0, y, N, K, group, stream);
+}
+
+int launch_q4gemv_stream2(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                          float *y, int64_t N, int K, int group, cudaStream_t stream) {
+    return launch_stream_any(codes, scales, zeros, x, nullptr, 0.0f, 0, 16, y, N, K, group, stream);
 }
 
 int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,

@@ -43,9 +43,10 @@ __host__ __device__ constexpr int stream_u(int K) { return K == 896 ? 6 : 8; }
 // fused: the fused-variant kernels also keep their RMSNorm sums (one float per consumer
 // warp) in 128 bytes after the abort flag.  q40: the weights are Q4_0 blocks (32 codes and
 // their binary16 scale in 18 bytes), so a block of rows is one stretch of ROWS * C * 18
-// bytes (group 32, no zero points).
+// bytes (group 32, no zero points).  mx: rows of x (1, or 2 for the two-row instances),
+// each with its own x planes and partial sums.
 __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym,
-                                                        bool fused = false, bool q40 = false) {
+                                                        bool fused = false, bool q40 = false, int mx = 1) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
@@ -65,11 +66,11 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
     g.WRED = g.C % 32 == 0 ? 1 : 0;
     g.PARTS = g.WRED ? g.C / 32 : g.C;
     g.RED_LD = g.PARTS + 1;
-    g.RED_B = g.ROWS * g.RED_LD * 4;
+    g.RED_B = g.ROWS * g.RED_LD * 4 * mx;   // [mx][ROWS][RED_LD]
     g.D = D;
     // shared memory: x planes | partial sums [kStreamNRed] | ring [D] | barriers | abort flag
     // | (fused) RMSNorm sums
-    g.OFF_RED = stream_round128(g.C * 28 * 4);
+    g.OFF_RED = stream_round128(g.C * 28 * 4 * mx);
     g.OFF_RING = stream_round128(g.OFF_RED + kStreamNRed * g.RED_B);
     g.OFF_BAR = g.OFF_RING + D * g.SLOT_B;
     g.OFF_FLAG = g.OFF_BAR + 8 * (2 * D + 2 * kStreamNRed);
@@ -81,9 +82,9 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
 // Ring slots: three (one more block in flight) when they fit the shared-memory
 // budget without lowering the CTAs an SM holds, else two.
 __host__ __device__ constexpr int stream_ctas_per_sm(int smem) { return kStreamSmemPerSM / (smem + 1024); }
-__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym, bool q40 = false) {
-    const int s2 = make_stream_geo(K, G, RG, U, 2, asym, false, q40).SMEM;
-    const int s3 = make_stream_geo(K, G, RG, U, 3, asym, false, q40).SMEM;
+__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym, bool q40 = false, int mx = 1) {
+    const int s2 = make_stream_geo(K, G, RG, U, 2, asym, false, q40, mx).SMEM;
+    const int s3 = make_stream_geo(K, G, RG, U, 3, asym, false, q40, mx).SMEM;
     return (s3 <= kStreamSmemBudget && stream_ctas_per_sm(s3) >= stream_ctas_per_sm(s2)) ? 3 : 2;
 }
 
@@ -133,6 +134,11 @@ using StreamArgsOf = std::conditional_t<(FUSE & 8) != 0, StreamGroupArgs, Stream
 // geometry whose blocks are whole warps and 16-byte multiples, 16-byte aligned
 // arrays, and a carve-up that fits the shared memory of one CTA).
 bool stream_applies(int M, int64_t N, int K, int group, const void *codes, const void *scales, const void *zeros);
+// Two rows of x (M = 2): the two-row instances, for K >= 2048 (one CTA per SM, so the second
+// set of x planes has the registers it needs).
+bool stream2_applies(int M, int64_t N, int K, int group, const void *codes, const void *scales, const void *zeros);
+int launch_q4gemv_stream2(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
+                          float *y, int64_t N, int K, int group, cudaStream_t stream);
 int launch_q4gemv_stream(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                          float *y, int64_t N, int K, int group, cudaStream_t stream);
 // The fused variant (q4gemv_fused_run): gamma may be null (no RMSNorm), swiglu 0 or 1.

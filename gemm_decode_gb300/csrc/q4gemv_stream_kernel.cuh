@@ -16,11 +16,11 @@ namespace {
 
 // The geometry an instance works with: compile-time when the instance fixes K, g
 // and RG (the tuned decode shapes), else the launcher's.
-template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED, bool Q40 = false>
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED, bool Q40 = false, int MXC = 1>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
-        constexpr StreamGeo g =
-            make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM, Q40), ASYM, FUSED, Q40);
+        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM, Q40, MXC), ASYM,
+                                                FUSED, Q40, MXC);
         return g;
     } else {
         return rt;
@@ -37,15 +37,18 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 // set -- the gate / up row pairs leave silu(gate) * up.  FUSE = 4: the weights are Q4_0
 // blocks (a.codes; 18 bytes per 32 codes: binary16 scale, then the codes; zero point 8).
 // FUSE = 8: a grouped launch (a.seg: several matrices, each served by its own CTAs).
+// FUSE = 16: two rows of x (M = 2): x[2][K], y[2][N], every block of codes serving both.
 template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
     constexpr int U = UC, NRED = kStreamNRed;
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
     constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0, Q40 = (FUSE & 4) != 0, GROUPED = (FUSE & 8) != 0;
+    constexpr int MX = (FUSE & 16) != 0 ? 2 : 1;   // rows of x
     static_assert(!Q40 || (!ASYM && (KC == 0 || GC == 32) && FUSE == 4), "Q4_0: group 32, symmetric, not fused");
     static_assert(!GROUPED || FUSE == 8, "grouped launches are plain");
-    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40>(a.geo);
+    static_assert(MX == 1 || FUSE == 16, "two rows of x: plain launches only");
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40, MX>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -230,18 +233,22 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
             }
         }
     } else {
-        for (int base = 0; base < C; base += G.TC / 4) {
-            const int i = base + (tid >> 2);
-            const bool in_range = i < C;
-            const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
-            encode_chunk4(w_x + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
-                          planes + (in_range ? i : 0) * kPlaneWords, tid & 3);
+#pragma unroll
+        for (int m = 0; m < MX; ++m) {   // row m of x: planes [m][C]
+            for (int base = 0; base < C; base += G.TC / 4) {
+                const int i = base + (tid >> 2);
+                const bool in_range = i < C;
+                const bool x_ok = ib(!in_range || (i + 1) * 32 <= C * 32);
+                encode_chunk4(w_x + m * C * 32 + (in_range ? i : 0) * 32, in_range && x_ok, in_range,
+                              planes + (m * C + (in_range ? i : 0)) * kPlaneWords, tid & 3);
+            }
         }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(G.TC) : "memory");
-    Planes P;
-    {
-        const uint32_t pa = s_planes + c * kPlaneWords * 4;
+    Planes P[MX];
+#pragma unroll
+    for (int m = 0; m < MX; ++m) {
+        const uint32_t pa = s_planes + (m * C + c) * kPlaneWords * 4;
         uint32_t w[28];
 #pragma unroll
         for (int i = 0; i < 7; ++i) {
@@ -252,10 +259,10 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
             w[4 * i + 3] = v.w;
         }
 #pragma unroll
-        for (int i = 0; i < 24; ++i) P.p[i] = w[i];
-        P.s_lo = static_cast<int>(w[24]);
-        P.s_hi = static_cast<int>(w[25]);
-        P.f = __uint_as_float(w[27]);
+        for (int i = 0; i < 24; ++i) P[m].p[i] = w[i];
+        P[m].s_lo = static_cast<int>(w[24]);
+        P[m].s_hi = static_cast<int>(w[25]);
+        P[m].f = __uint_as_float(w[27]);
     }
     const int grp = c >> G.GSHIFT;
     // byte offsets of this thread's data inside a slot for sub-row u = 0, and the
@@ -271,13 +278,17 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
     const int red_u = G.WRED ? (lane >> NSH) : 0;
     const uint32_t red_off = G.WRED ? ((red_u * G.RG + r) * G.RED_LD + (c >> 5)) * 4 : (r * G.RED_LD + c) * 4;
     const uint32_t str_red = G.RG * G.RED_LD * 4;
+    const uint32_t red_m = G.ROWS * G.RED_LD * 4;   // bytes of one row of x's partials in a buffer
 
     // Sum the partials of rows [lo, hi) of a block and store them: ql lanes per row
     // (a power of two), each adding every ql-th partial, combined by shuffles.
     // ql = 1 is a lane per row, partials in order.
     auto reduce_rows = [&](int buf, int64_t row0, int lo, int hi, int ql) {
-        const uint32_t src = s_red + buf * G.RED_B;
-        const int q = lane & (ql - 1);
+      const int q = lane & (ql - 1);
+#pragma unroll
+      for (int mr = 0; mr < MX; ++mr) {   // each row of x: its partials, its row of y
+        const uint32_t src = s_red + buf * G.RED_B + mr * red_m;
+        float *yrow = w_y + mr * w_N;
         for (int base = lo; base < hi; base += 32 / ql) {   // warp-uniform trip count
             const int rho = base + lane / ql;
             const bool mine = rho < hi;
@@ -297,8 +308,9 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
                     continue;
                 }
             }
-            if (mine && q == 0 && row0 + rho < w_N) w_y[row0 + rho] = acc;
+            if (mine && q == 0 && row0 + rho < w_N) yrow[row0 + rho] = acc;
         }
+      }
     };
 
     int s = 0, ph = 0;       // ring slot of block i and its wrap parity
@@ -317,7 +329,7 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
         }
         const uint32_t sl = s_ring + s * G.SLOT_B;
         const uint32_t rd = s_red + rb * G.RED_B;
-        float v[U];
+        float v[MX][U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             uint4 cw;
@@ -347,22 +359,36 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
             const bool z_ok = !ASYM || ib(off_z + u * str_z + 1 <= static_cast<uint32_t>(G.CODE_B + G.SC_B + G.Z_B));
             const int z = ASYM ? (z_ok ? static_cast<int>((lds_u8(sl + off_z + u * str_z) >> zsh) & 0xFu) : 8) : 8;
             const float sc = __half2float(__ushort_as_half(static_cast<unsigned short>(sh)));
-            v[u] = (sc * P.f) * chunk_dot(cw, z, P);
+            if constexpr (MX == 1) {
+                v[0][u] = (sc * P[0].f) * chunk_dot(cw, z, P[0]);
+            } else {
+                float d0, d1;
+                chunk_dot2(cw, z, P[0], P[1], d0, d1);
+                v[0][u] = (sc * P[0].f) * d0;
+                v[1][u] = (sc * P[1].f) * d1;
+            }
         }
         bool summed = false;
         if constexpr (U_POW2) {
             if (G.WRED) {   // (the host pairs whole-warp rows with a power-of-two U only)
-                const float t = warp_sum_many<U>(v, lane);
-                if (red_writer && ib(rb * G.RED_B + red_off + 4 <= static_cast<uint32_t>(kStreamNRed * G.RED_B)))
-                sts_f32(rd + red_off, t);
+#pragma unroll
+                for (int m = 0; m < MX; ++m) {
+                    const float t = warp_sum_many<U>(v[m], lane);
+                    if (red_writer &&
+                        ib(rb * G.RED_B + m * red_m + red_off + 4 <= static_cast<uint32_t>(kStreamNRed * G.RED_B)))
+                        sts_f32(rd + m * red_m + red_off, t);
+                }
                 summed = true;
             }
         }
         if (!summed) {
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (ib(rb * G.RED_B + red_off + u * str_red + 4 <= static_cast<uint32_t>(kStreamNRed * G.RED_B)))
-                    sts_f32(rd + red_off + u * str_red, v[u]);
+            for (int m = 0; m < MX; ++m)
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (ib(rb * G.RED_B + m * red_m + red_off + u * str_red + 4 <=
+                           static_cast<uint32_t>(kStreamNRed * G.RED_B)))
+                        sts_f32(rd + m * red_m + red_off + u * str_red, v[m][u]);
         }
         __syncwarp();
         if (lane == 0) {
@@ -518,6 +544,11 @@ int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
         if constexpr (GV == 32) return asym ? Q4_ERR_UNSUPPORTED : launch_stream<KV, 32, RGV, UV, false, 4>(a, s);
         return Q4_ERR_UNSUPPORTED;
     }
+    if (fuse == 16) {   // two rows of x: the one-CTA-per-SM geometries (K >= 2048)
+        if constexpr (KV >= 2048)
+            return asym ? launch_stream<KV, GV, RGV, UV, true, 16>(a, s) : launch_stream<KV, GV, RGV, UV, false, 16>(a, s);
+        return Q4_ERR_UNSUPPORTED;
+    }
     switch (fuse) {
         case 0: return asym ? launch_stream<KV, GV, RGV, UV, true, 0>(a, s) : launch_stream<KV, GV, RGV, UV, false, 0>(a, s);
         case 1: return asym ? launch_stream<KV, GV, RGV, UV, true, 1>(a, s) : launch_stream<KV, GV, RGV, UV, false, 1>(a, s);
@@ -527,7 +558,7 @@ int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
 }
 
 // One translation unit per K instantiates the compile-time geometries of that K (plain,
-// RMSNorm, RMSNorm + SwiGLU, Q4_0, grouped).
+// RMSNorm, RMSNorm + SwiGLU, Q4_0, grouped, and for K >= 2048 two rows of x).
 #define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
     int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s) {    \
         switch (group) {                                                                              \

@@ -176,6 +176,32 @@ __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes 
     return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
 }
 
+// The same for two rows of x at once: the codes are unpacked once and serve both rows'
+// planes (d0: row 0, d1: row 1).
+__device__ __forceinline__ void chunk_dot2(const uint4 &cw, int z, const Planes &P0, const Planes &P1, float &d0,
+                                           float &d1) {
+    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    int a0 = 0, a1 = 0, a2 = 0, b0 = 0, b1 = 0, b2 = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = words[w] & 0x0F0F0F0Fu;          // codes of even k, one per byte
+        const uint32_t hi = (words[w] >> 4) & 0x0F0F0F0Fu;   // codes of odd k, one per byte
+        a0 = dp4a_uu(lo, P0.p[6 * w + 0], a0);
+        a0 = dp4a_uu(hi, P0.p[6 * w + 1], a0);
+        a1 = dp4a_uu(lo, P0.p[6 * w + 2], a1);
+        a1 = dp4a_uu(hi, P0.p[6 * w + 3], a1);
+        a2 = dp4a_us(lo, P0.p[6 * w + 4], a2);
+        a2 = dp4a_us(hi, P0.p[6 * w + 5], a2);
+        b0 = dp4a_uu(lo, P1.p[6 * w + 0], b0);
+        b0 = dp4a_uu(hi, P1.p[6 * w + 1], b0);
+        b1 = dp4a_uu(lo, P1.p[6 * w + 2], b1);
+        b1 = dp4a_uu(hi, P1.p[6 * w + 3], b1);
+        b2 = dp4a_us(lo, P1.p[6 * w + 4], b2);
+        b2 = dp4a_us(hi, P1.p[6 * w + 5], b2);
+    }
+    d0 = fmaf(static_cast<float>(a2 - z * P0.s_hi), 65536.0f, static_cast<float>(a1 * 256 + a0 - z * P0.s_lo));
+    d1 = fmaf(static_cast<float>(b2 - z * P1.s_hi), 65536.0f, static_cast<float>(b1 * 256 + b0 - z * P1.s_lo));
+}
 
 // ---- mbarrier primitives with bounded waits ----
 __device__ __forceinline__ unsigned long long global_ns() {

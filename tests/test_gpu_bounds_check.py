@@ -57,6 +57,14 @@ def test_streamed_kernel(torch, N, K, g, symmetric):
     run_checked(torch, w, x, f"streamed N={N} K={K} g={g}")
 
 
+@pytest.mark.parametrize("N,K,g", [(4899, 4096, 128), (4101, 14336, 128), (9777, 2048, 32)])
+def test_streamed_kernel_two_rows(torch, N, K, g):
+    # M = 2: the two-row instances (and the runtime geometry at K = 14336), partial last block
+    w = synth.q4_weights(N + K + 2, N, K, g, tag="bounds-two-rows")
+    x = synth.activations_f32(N + 3, 2, K)
+    run_checked(torch, w, x, f"streamed two rows N={N} K={K} g={g}")
+
+
 @pytest.mark.parametrize("M,N,K,g", [(16, 8323, 4128, 32), (5, 8196, 2048, 64), (9, 4100, 896, 128),
                                      (8, 4100, 4128, 32), (3, 900, 4864, 64)])
 def test_tensor_core_kernel(torch, M, N, K, g):

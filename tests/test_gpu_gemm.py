@@ -1,5 +1,10 @@
 """GPU parity of the tensor-core int4 matmul (q4gemm_run) against the CPU oracle.
 
+Shapes whose 128 x 128 tiles would leave most SMs idle (few weight rows and tokens)
+run on the split kernel: 128 x 32 or 128 x 64 tiles with the K-blocks split over a
+cluster of up to 8 CTAs and the partials added in rank order; the other shapes on the
+128 x 128-tile kernel.  Both are covered below.
+
 The tensor-core path feeds the MMA bf16 weights, each the exact binary32
 (q - z) * s rounded once to bfloat16, so a single term can be off by up to
 2^-9 of |w a|.  Checks:
@@ -10,6 +15,8 @@ The tensor-core path feeds the MMA bf16 weights, each the exact binary32
   * the prefill workloads (K >= 2048): against the exact oracle within the
     stated tolerance |c - c_ref| <= 1e-3 * sum_k |w_nk a_mk| + 1e-6.
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -88,6 +95,51 @@ def test_small_shapes(torch, g, symmetric):
         check_case(torch, w, a)
 
 
+@pytest.mark.parametrize("M,N,K,g,symmetric", [
+    (128, 512, 2048, 64, True),      # the 128-token prefill shape: 32-row tiles, 8-CTA clusters
+    (128, 512, 2048, 128, False),
+    (100, 200, 2080, 32, False),     # ragged M and N tiles, a half-empty last K-block, 8-CTA clusters
+    (300, 96, 1024, 32, True),       # three 128-row tiles of A, the last 44 rows
+    (256, 1000, 4096, 128, False),   # 64-row tiles, 4-CTA clusters, two tiles of A
+    (512, 300, 8192, 64, False),     # 64-row tiles, four tiles of A, 32 K-blocks per CTA
+    (1, 512, 2048, 32, False),       # one token
+    (128, 512, 96, 32, False),       # two K-blocks: no split, 32-row tiles
+])
+def test_split_kernel_whole_output(torch, M, N, K, g, symmetric):
+    w = synth.q4_weights(M * 7 + N + K, N, K, g, symmetric=symmetric, tag="split")
+    a = synth.activations_bf16(M + 3 * K, M, K)
+    check_case(torch, w, a, stated_tolerance=K >= 2048)
+
+
+@pytest.mark.parametrize("M,N,K,g", [(130, 10240, 256, 32), (300, 10368, 512, 64), (513, 10240, 384, 128)])
+def test_regular_tiles_kernel(torch, M, N, K, g):
+    # enough 128 x 128 tiles (at least half the SMs) for the regular kernel: 2, 3 and 4
+    # halves of A per CTA, partial last tiles
+    w = synth.q4_weights(M + N + K, N, K, g, tag="regular")
+    a = synth.activations_bf16(M + K + 1, M, K)
+    check_case(torch, w, a)
+
+
+def test_split_kernel_deterministic(torch):
+    # the partials of a cluster are added in rank order: repeated calls agree bit for bit
+    w = synth.q4_weights(19, 512, 2048, 32, tag="split-det")
+    a = synth.activations_bf16(19, 128, 2048)
+    np.testing.assert_array_equal(run_gemm(torch, w, a), run_gemm(torch, w, a))
+
+
+def test_split_kernel_bounded_wait_reports_timeout_without_fault(torch):
+    # every wait that is not already satisfied gives up at once; the CTAs still meet both
+    # cluster barriers, release tensor memory and raise the status word
+    w = synth.q4_weights(23, 512, 2048, 32, tag="split-timeout")
+    a = synth.activations_bf16(23, 128, 2048)
+    c = torch.zeros((128, 512), dtype=torch.float32, device="cuda")
+    q4.q4gemm_run_ex(dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch), dev(a, torch), c,
+                     128, 512, 2048, 32, wait_timeout_ns=0)
+    assert q4.q4gemv_device_status() == q4.Q4_ERR_TIMEOUT
+    assert q4.q4gemv_device_status() == q4.Q4_OK
+    check_case(torch, w, a, stated_tolerance=True)
+
+
 def test_k_tail_half_block(torch):
     # K = 96: the last 64-wide K-block is half empty
     w = synth.q4_weights(3, 256, 96, 32)
@@ -112,6 +164,22 @@ def test_prefill_ffn_2048_tokens_sampled(torch):
     ns = sorted(set(r.choice(N, 24, replace=False).tolist()) | {0, N - 1})
     c_ref, bound = oracle.q4_gemm_rows(w.codes, w.scales, w.zeros, a, 32, ms, ns)
     assert_within_bound(c[np.ix_(ms, ns)], c_ref, bound, "2048x14336x4096 sampled")
+    # a whole strip: 128 tokens (one tile of A, rows 1024..1151) against all 14336 weight
+    # rows, the oracle run over the host cores in slices of weight rows
+    from concurrent.futures import ThreadPoolExecutor
+    m0 = 1024
+    strip = np.ascontiguousarray(a[m0:m0 + 128])
+    cuts = np.linspace(0, N, (os.cpu_count() or 1) + 1).astype(int)
+
+    def part(i):
+        n0, n1 = cuts[i], cuts[i + 1]
+        return oracle.q4_gemm(w.codes[n0:n1], w.scales[n0:n1], w.zeros[n0:n1], strip, 32)
+
+    with ThreadPoolExecutor(max_workers=len(cuts) - 1) as ex:
+        parts = list(ex.map(part, range(len(cuts) - 1)))
+    c_ref = np.concatenate([p[0] for p in parts], axis=1)
+    bound = np.concatenate([p[1] for p in parts], axis=1)
+    assert_within_bound(c[m0:m0 + 128], c_ref, bound, "2048x14336x4096, a 128-token strip, every column")
 
 
 def test_deterministic(torch):

@@ -2,6 +2,7 @@
 against the CPU oracle.  Marked gpu: needs an sm_103a device and the built
 library; every call goes through the C ABI.
 """
+import os
 import zlib
 
 import numpy as np
@@ -161,10 +162,19 @@ def _full_size_check(torch, w, M, seed, count=96):
     return assert_within_bound(y[:, rows], y_ref, bound, f"N={w.N} K={w.K} M={M}")
 
 
+def _all_rows_check(torch, w, M, seed):
+    """Every output against the oracle, run over the host cores in row slices."""
+    x = synth.activations_f32(seed, M, w.K)
+    y = run_gemv(torch, w, x)
+    y_ref, bound = oracle.q4_gemv_threaded(w.codes, w.scales, w.zeros, x, w.group, os.cpu_count() or 1)
+    return assert_within_bound(y, y_ref, bound, f"all rows N={w.N} K={w.K} M={M}")
+
+
 @pytest.mark.parametrize("name,N,K", synth.DECODE_05B["shapes"])
 def test_decode_05b_projection_set(torch, name, N, K):
+    # every row of every projection, the LM head included
     w = synth.q4_weights(zlib.crc32(name.encode()) & 0xFFFF, N, K, 32, scale_range=synth.SCALE_05B, tag=name)
-    _full_size_check(torch, w, 1, 17)
+    _all_rows_check(torch, w, 1, 17)
 
 
 def test_single_896(torch):
@@ -177,20 +187,26 @@ def test_single_896(torch):
 
 @pytest.mark.parametrize("name,N,K", synth.DECODE_8B["shapes"])
 def test_decode_8b_shapes(torch, name, N, K):
+    # every row at every M (the LM head's 128256 rows included)
     w = synth.q4_weights(len(name) * 31, N, K, 128, scale_range=synth.SCALE_8B, tag=name)
     for M in synth.DECODE_8B["Ms"]:
-        _full_size_check(torch, w, M, 100 + M, count=48)
+        _all_rows_check(torch, w, M, 100 + M)
 
 
 @pytest.mark.parametrize("K", synth.SWEEP["Ks"])
 @pytest.mark.parametrize("g", synth.SWEEP["groups"])
 def test_sweep_cells(torch, K, g):
-    # every (N, symmetric, M) of the sweep at this (K, g); sampled rows at full size
+    # every (N, symmetric, M) of the sweep at this (K, g): every row of the M = 1 cells
+    # with at least 64 MB of packed weights (the bandwidth bar's cells), sampled rows of
+    # the others
     for N in synth.SWEEP["Ns"]:
         for sym in synth.SWEEP["symmetric"]:
             w = synth.q4_weights(K + N + g, N, K, g, symmetric=sym, tag="sweep")
             for M in synth.SWEEP["Ms"]:
-                _full_size_check(torch, w, M, K + M, count=16)
+                if M == 1 and w.nbytes >= 64e6:
+                    _all_rows_check(torch, w, M, K + M)
+                else:
+                    _full_size_check(torch, w, M, K + M, count=16)
 
 
 def test_streamed_kernel_bounded_wait_reports_timeout_without_fault(torch):
@@ -211,6 +227,22 @@ def test_streamed_kernel_bounded_wait_reports_timeout_without_fault(torch):
     rows = _sample_rows(N, 64, 3)
     y_ref, bound = oracle.q4_gemv_rows(w.codes, w.scales, w.zeros, x, 32, rows)
     assert_within_bound(y2[:, rows], y_ref, bound, "after timeout")
+
+
+@pytest.mark.parametrize("K,g,N", [(2048, 64, 9777), (4096, 128, 4899), (8192, 32, 4103), (16384, 128, 4099),
+                                   (14336, 128, 4101), (4096, 32, 32771)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_streamed_kernel_two_rows(torch, K, g, N, symmetric):
+    # M = 2 on long matrices: the streamed kernel's two-row instances (both rows of x held
+    # as planes, every block of codes serving both), partial last blocks; K = 14336 takes
+    # the runtime-geometry instance.  Every row against the oracle.
+    w = synth.q4_weights(N + 2 * K + g, N, K, g, symmetric=symmetric, tag="two-rows")
+    x = synth.activations_f32(N + g + 2, 2, K)
+    y = run_gemv(torch, w, x)
+    y_ref, bound = oracle.q4_gemv_threaded(w.codes, w.scales, w.zeros, x, g, os.cpu_count() or 1)
+    assert_within_bound(y, y_ref, bound, f"two rows N={N} K={K} g={g}")
+    # and the call is deterministic
+    np.testing.assert_array_equal(y, run_gemv(torch, w, x))
 
 
 @pytest.mark.parametrize("K,g,N", [(896, 32, 9765), (896, 128, 9765), (2048, 64, 9777), (4096, 128, 4899),

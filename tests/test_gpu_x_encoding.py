@@ -1,6 +1,6 @@
 """The x encoding of the dp4a GEMV kernels as a stated, tested contract.
 
-The streamed (M = 1, long matrices), register-resident (M <= 2) and grouped
+The streamed (M = 1 and 2, long matrices), register-resident (M <= 2) and grouped
 GEMV kernels hold each 32-element chunk c of a row of x as 24-bit integers
 under one shared power of two 2^E_c, 2^(E_c-1) <= max_{k in c} |x_k| < 2^E_c
 (E_c >= -100).  The library header states what that guarantees per output:
@@ -127,9 +127,10 @@ def gemv(torch, w, x, ex_flags=None):
     return host(y)
 
 
-# (N, K, g, symmetric, M): the streamed kernel (M = 1, long matrices), the register-
+# (N, K, g, symmetric, M): the streamed kernel (M = 1 and 2, long matrices), the register-
 # resident kernel (M <= 2, short matrices and small K)
-STREAMED = [(8192, 4096, 128, False, 1), (7680, 896, 32, False, 1), (4096, 2048, 64, True, 1)]
+STREAMED = [(8192, 4096, 128, False, 1), (7680, 896, 32, False, 1), (4096, 2048, 64, True, 1),
+            (8192, 4096, 128, False, 2), (4101, 14336, 32, True, 2)]
 REGISTER_RESIDENT = [(1000, 896, 32, False, 1), (1000, 896, 32, False, 2), (300, 64, 32, False, 2),
                      (64, 4096, 128, True, 1), (777, 128, 64, False, 2)]
 
