@@ -56,6 +56,7 @@ struct GemmArgs {
     int M, N, K, nb, zrow, gshift;
     int c_vec;   // C is 16-byte aligned and N % 4 == 0: float4 stores
     unsigned long long timeout_ns;
+    unsigned int *bounds;   // out-of-range access counter (bounds-checking builds)
 };
 
 // Instruction descriptor: D f32, A/B bf16, both K-major, N = BN, M = BM.
@@ -122,6 +123,7 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const unsigned long long limit = g.timeout_ns;
+    auto ib = [&](bool ok) { return q4_in_bounds(ok, g.bounds); };   // bounds-checking builds
 
     auto fail = [&]() {
         *abort_flag = 1;
@@ -199,9 +201,9 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
             const int k = kb * BK + half * 32;
             if (kb < kblocks && k < g.K) {
                 const int grp = k >> (5 + g.gshift);
-                f.cw = ldg_stream(crow + k / 2);
-                f.sc = ldg_u16(srow + grp);
-                f.zb = zrow ? ldg_u8(zrow + (grp >> 1)) : 0u;
+                if (ib(k / 2 + 16 <= g.K / 2)) f.cw = ldg_stream(crow + k / 2);
+                if (ib(grp < g.nb)) f.sc = ldg_u16(srow + grp);
+                f.zb = (zrow && ib((grp >> 1) < g.zrow)) ? ldg_u8(zrow + (grp >> 1)) : 0u;
             }
         };
         static_assert(PF == 3, "the fetch ring below rotates three registers sets");
@@ -251,8 +253,10 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
             unsigned char *tb = tiles_b + s * kTileBytes;
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                *reinterpret_cast<uint4 *>(tb + sw128_offset(row, half * 4 + w)) =
-                    make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
+                const uint32_t off = sw128_offset(row, half * 4 + w);
+                if (ib(off + 16 <= static_cast<uint32_t>(kTileBytes)))
+                    *reinterpret_cast<uint4 *>(tb + off) =
+                        make_uint4(out[4 * w], out[4 * w + 1], out[4 * w + 2], out[4 * w + 3]);
             }
             fence_proxy_async();      // generic-proxy stores -> visible to the tensor core
             mbar_arrive(full_b(s));
@@ -429,6 +433,7 @@ int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
     g.gshift = group == 32 ? 0 : (group == 64 ? 1 : 2);
     g.c_vec = (aligned(c, 16) && (N % 4) == 0) ? 1 : 0;
     g.timeout_ns = call_options().wait_ns;
+    g.bounds = bounds_counter();
     switch (nh) {
         case 4: return launch_tc<4, 2>(map, g, M, N, stream);
         case 3: return launch_tc<3, 3>(map, g, M, N, stream);

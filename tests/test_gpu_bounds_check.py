@@ -142,10 +142,12 @@ def test_grouped_streamed_kernel(torch, K, g):
         assert_within_bound(host(y), y_ref, bound, f"grouped K={K} N={w.N}")
 
 
-@pytest.mark.parametrize("M,N,K,g", [(100, 200, 2080, 32), (300, 96, 1024, 64), (256, 1000, 4096, 128)])
+@pytest.mark.parametrize("M,N,K,g", [(100, 200, 2080, 32), (300, 96, 1024, 64), (256, 1000, 4096, 128),
+                                     (1030, 4100, 160, 32)])
 def test_split_matmul_kernel(torch, M, N, K, g):
     # the matmul's split kernel: ragged tiles of A and of weight rows, a half-empty last
-    # K-block, 32- and 64-row tiles, 4- and 8-CTA clusters
+    # K-block, 32- and 64-row tiles, 4- and 8-CTA clusters; and (the last case) the
+    # 128 x 128-tile kernel with a 6-row last tile of A, a 4-row last tile of weights, a K tail
     w = synth.q4_weights(M + N + K, N, K, g, tag="bounds-split")
     a = synth.activations_bf16(M + 1, M, K)
     c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")

@@ -120,6 +120,16 @@ def test_regular_tiles_kernel(torch, M, N, K, g):
     check_case(torch, w, a)
 
 
+@pytest.mark.parametrize("M,N,K,g", [(1030, 4100, 256, 32), (2048, 2560, 160, 32), (1536, 3840, 512, 128)])
+def test_large_tiles_kernel(torch, M, N, K, g):
+    # larger problems on the 128 x 128-tile kernel with several halves of A per CTA: a last
+    # tile of A a few rows deep, a last tile of weights with 4 rows, a half-empty last
+    # K-block (K = 160)
+    w = synth.q4_weights(M + N + K + 1, N, K, g, tag="wide")
+    a = synth.activations_bf16(M + K + 2, M, K)
+    check_case(torch, w, a)
+
+
 def test_split_kernel_deterministic(torch):
     # the partials of a cluster are added in rank order: repeated calls agree bit for bit
     w = synth.q4_weights(19, 512, 2048, 32, tag="split-det")
