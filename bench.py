@@ -432,11 +432,19 @@ def run_gpu(args, rank, world, local_rank):
                             f"{args.samples} timed replays (median; p10, p90, min) and t(2n)/t(n) from two "
                             f"replays"}
     if args.controls and rank == 0:
+        try:   # a detail figure: its failure is recorded, the measured step stands
+            detail["grouped_step"] = run_grouped_step(args, torch, q4, shapes, group, S.reps, S.xs, replicas, stream)
+        except Exception as e:   # noqa: BLE001
+            detail["grouped_step"] = {"error": f"{type(e).__name__}: {e}"}
         detail["decode_05b"] = run_decode_05b(args, torch, q4, stream)
         detail["controls"] = run_controls(args, torch, q4)
         detail["prefill_tensor_core"] = run_prefill(args, torch, q4)
         detail["decode_8b"] = run_decode_8b(args, torch, q4)
         detail["q4_0_format"] = run_q40(args, torch, q4)
+        try:   # a detail figure: its failure is recorded, the measured step stands
+            detail["q8_0_format"] = run_q80(args, torch, q4)
+        except Exception as e:   # noqa: BLE001
+            detail["q8_0_format"] = {"error": f"{type(e).__name__}: {e}"}
 
     probe = detail.get("controls", {}).get("vec4_read_probe_1GiB", {}).get("gbs")
     if probe:   # the same kernel's rate against this GPU's own streaming read (the vec4 probe)
@@ -1086,9 +1094,10 @@ def run_fused_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
 
 
 def run_grouped_step(args, torch, q4, shapes, group, reps, xs, replicas, stream):
-    """The same seven projections, each with its own x and y as in the timed step, issued
-    through q4gemv_grouped_run: the six K = 896 matrices (q, k, v, gate, up, LM head) as
-    one streamed launch in which each has CTAs of its own, down (K = 4864) as a second.
+    """The projections of a step, each with its own x and y as in the timed step, issued
+    through q4gemv_grouped_run, one call per K: the matrices of one K as one streamed
+    launch in which each has CTAs of its own (0.5B set: q, k, v, gate, up and the LM head
+    at K = 896, down alone; 8B set: qo, gate_up and the LM head at K = 4096, down alone).
     A CUDA graph of back-to-back steps over the replicas; the outputs are checked against
     the separate calls' within the GEMV tolerance by the tests, not here."""
     ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for _, N, _ in shapes]
@@ -1141,6 +1150,39 @@ def run_q40(args, torch, q4):
     return {"kernel": "streamed kernel's Q4_0 instances (M = 1, long matrices: whole 18-byte blocks by bulk copy, "
                       "codes read as five 32-bit words shifted to the 2-byte offset), else the general kernel's "
                       "(nine 16-bit loads per block)", "cells": out}
+
+
+def run_q80(args, torch, q4):
+    """The third format (Q8_0 blocks, 34 bytes per 32 weights: 1.0625 B per weight):
+    microseconds per q8_0_gemv_run call and GB/s from back-to-back launches over rotating
+    replicas (cold)."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(80)
+    stream = torch.cuda.Stream()
+    out = []
+    for name, N, K, M in [("lm_head", 151936, 896, 1), ("qo_proj", 4096, 4096, 1), ("lm_head_8b", 128256, 4096, 1),
+                          ("down_proj", 896, 4864, 1), ("lm_head", 151936, 896, 4)]:
+        nblk = K // 32
+        wbytes = N * nblk * 34
+        nrep = int(min(64, max(2, -(-6 * L2_BYTES // wbytes))))
+        reps = []
+        for _ in range(nrep):
+            b = torch.randint(0, 256, (N, nblk, 34), dtype=torch.uint8, device="cuda", generator=gen)
+            d = torch.empty((N, nblk), dtype=torch.float16, device="cuda").uniform_(*synth.SCALE_Q80, generator=gen)
+            b[:, :, 0:2] = d.view(torch.uint8).view(N, nblk, 2)
+            reps.append(b)
+        x = torch.randn((M, K), dtype=torch.float32, device="cuda", generator=gen)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        st = _time_launches(torch, stream, lambda i: q4.q8_0_gemv_run(reps[i % nrep], x, y, M, N, K, stream=stream),
+                            max(nrep, 100))
+        byts = wbytes + 4 * M * K + 4 * M * N
+        out.append({"name": name, "M": M, "N": N, "K": K, "us_per_call": round(st["us"], 3),
+                    "gbs": round(byts / st["us"] / 1e3, 1), "t2n_over_tn": round(st["t2n_over_tn"], 3)})
+        del reps
+        torch.cuda.empty_cache()
+    return {"kernel": "streamed kernel's Q8_0 instances (M = 1, long matrices: whole 34-byte blocks by bulk copy, "
+                      "codes read as nine 32-bit words shifted to the 2-byte offset, dp4a on the byte planes of x), "
+                      "else a CUDA-core kernel (a warp per row, codes widened exactly)", "cells": out}
 
 
 def run_decode_8b(args, torch, q4):

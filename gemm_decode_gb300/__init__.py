@@ -16,8 +16,8 @@ import threading
 
 __all__ = [
     "Q4Error", "lib", "library_path", "exported_names",
-    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run", "q4gemm_run",
-    "q4gemv_run_ex", "q4gemv_fused_run_ex", "q4gemv_grouped_run_ex", "q4gemm_run_ex",
+    "q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run", "q8_0_gemv_run",
+    "q4gemm_run", "q4gemv_run_ex", "q4gemv_fused_run_ex", "q4gemv_grouped_run_ex", "q4gemm_run_ex",
     "f32gemv_run",
     "q4gemv_status_string", "q4gemv_last_cuda_error",
     "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
@@ -95,6 +95,7 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_grouped_run_ex.argtypes = [ctypes.POINTER(_Segment), _i32, _i64, _i32, _opt, _vp]
             L.q4gemm_run_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _i64, _i64, _i32, _opt, _vp]
             L.q4_0_gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
+            L.q8_0_gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_grouped_run.argtypes = [ctypes.POINTER(_Segment), _i32, _i64, _i32, _vp]
             L.f32gemv_run.argtypes = [_vp, _vp, _vp, _i32, _i64, _i64, _vp]
             L.q4gemv_status_string.argtypes = [ctypes.c_int]
@@ -111,6 +112,7 @@ def lib() -> ctypes.CDLL:
             L.q4gemv_grouped_split.argtypes = [ctypes.POINTER(_i64), _i32, _i64, _i32, _i32,
                                                ctypes.POINTER(_i32), ctypes.POINTER(_i32)]
             for f in ("q4gemv_pack_info", "q4gemv_run", "q4gemv_fused_run", "q4gemv_grouped_run", "q4_0_gemv_run",
+                      "q8_0_gemv_run",
                       "q4gemm_run", "f32gemv_run", "q4gemv_run_ex", "q4gemv_fused_run_ex", "q4gemv_grouped_run_ex",
                       "q4gemm_run_ex",
                       "q4_dequant_f32_run", "q4_dequant_bf16_run", "vec4_read_probe_run",
@@ -292,6 +294,17 @@ def q4_0_gemv_run(blocks, x, y, M=None, N=None, K=None, stream=None, check=True)
                              _stream(stream))
     if check:
         _check(st, "q4_0_gemv_run")
+    return st
+
+
+def q8_0_gemv_run(blocks, x, y, M=None, N=None, K=None, stream=None, check=True) -> int:
+    M = int(x.shape[0] if M is None else M)
+    K = int(x.shape[1] if K is None else K)
+    N = int(blocks.shape[0] if N is None else N)
+    st = lib().q8_0_gemv_run(_addr(blocks, "blocks", 1), _addr(x, "x", 4), _addr(y, "y", 4), M, N, K,
+                             _stream(stream))
+    if check:
+        _check(st, "q8_0_gemv_run")
     return st
 
 

@@ -307,6 +307,20 @@ int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64
                           static_cast<cudaStream_t>(stream));
 }
 
+int q8_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K, void *stream) {
+    if (M < 0 || N < 0 || K < 32 || K % 32 != 0) return Q4_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return Q4_OK;
+    if (M > 16 || N > 0x7fffffffLL || K > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
+    if (blocks == nullptr || x == nullptr || y == nullptr) return Q4_ERR_INVALID_ARG;
+    if (!aligned(blocks, 2) || !aligned(x, 16) || !aligned(y, 4)) return Q4_ERR_MISALIGNED;
+    {
+        const Span in[2] = {span(blocks, N * (K / 32) * 34), span(x, 4 * M * K)};
+        if (overlaps_any(span(y, 4 * M * N), in, 2)) return Q4_ERR_INVALID_ARG;
+    }
+    return launch_q80gemv(static_cast<const uint8_t *>(blocks), x, y, M, N, static_cast<int>(K),
+                          static_cast<cudaStream_t>(stream));
+}
+
 int q4gemm_run(const void *codes, const void *scales_f16, const void *zeros_u4_or_null, const void *a_bf16,
                float *c, int32_t M, int64_t N, int64_t K, int32_t group, void *stream) {
     int st = check_shape(M, N, K, group);

@@ -85,6 +85,7 @@ int launch_q4gemv_fused(const uint8_t *codes, const uint16_t *scales, const uint
                         const float *gamma, float eps, int swiglu, float *y, int M, int64_t N, int K, int group,
                         cudaStream_t stream);
 int launch_q40gemv(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream);
+int launch_q80gemv(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream);
 int launch_q4gemm(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros,
                   const uint16_t *a, float *c, int M, int64_t N, int K, int group,
                   cudaStream_t stream);

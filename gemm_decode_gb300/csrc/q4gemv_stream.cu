@@ -107,7 +107,7 @@ bool stream2_applies(int M, int64_t N, int K, int group, const void *codes, cons
 }
 
 // fuse: 0 plain, 1 RMSNorm, 3 RMSNorm and/or SwiGLU, 4 Q4_0 blocks (codes = the blocks),
-// 16 two rows of x
+// 16 two rows of x, 32 Q8_0 blocks (codes = the blocks)
 static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const uint8_t *zeros, const float *x,
                              const float *gamma, float eps, int swiglu, int fuse, float *y, int64_t N, int K,
                              int group, cudaStream_t stream) {
@@ -129,11 +129,11 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
     a.eps = eps;
     a.swiglu = swiglu;
     if (a.status == nullptr) return Q4_ERR_CUDA;
-    const int u = stream_u(K);
-    const bool q40 = fuse == 4;
+    const bool q40 = fuse == 4, q80 = fuse == 32;
+    const int u = q80 ? stream_q80_u(K) : stream_u(K);
     const int mx = fuse == 16 ? 2 : 1;
-    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, q40, mx), asym, fuse == 1 || fuse == 3,
-                            q40, mx);
+    a.geo = make_stream_geo(K, group, rg, u, stream_slots(K, group, rg, u, asym, q40, mx, q80), asym,
+                            fuse == 1 || fuse == 3, q40, mx, q80);
     if (!stream_geo_ok(a.geo, asym)) return Q4_ERR_UNSUPPORTED;
     // compile-time row geometry for the K of the decode and sweep shapes
     switch (K) {
@@ -144,6 +144,7 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
         case 16384: return launch_stream_k16384(a, group, asym, fuse, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
             if (fuse == 4) return launch_stream<0, 0, 0, 8, false, 4>(a, stream);
+            if (fuse == 32) return launch_stream<0, 0, 0, stream_q80_u(0), false, 32>(a, stream);
             if (fuse == 16)
                 return asym ? launch_stream<0, 0, 0, 8, true, 16>(a, stream) : launch_stream<0, 0, 0, 8, false, 16>(a, stream);
             if (fuse == 3)
@@ -184,6 +185,22 @@ bool stream_q40_applies(int M, int64_t N, int K, const void *blocks) {
 
 int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream) {
     return launch_stream_any(blocks, nullptr, nullptr, x, nullptr, 0.0f, 0, 4, y, N, K, 32, stream);
+}
+
+bool stream_q80_applies(int M, int64_t N, int K, const void *blocks) {
+    if (M != 1 || N < 4096 || K % 32 != 0 || !aligned(blocks, 16)) return false;
+    const int rg = stream_rg(K);
+    if (rg == 0) return false;
+    const int u = stream_q80_u(K);
+    const StreamGeo g =
+        make_stream_geo(K, 32, rg, u, stream_slots(K, 32, rg, u, false, false, 1, true), false, false, false, 1, true);
+    if ((g.ROWS * g.C * 34) % 16 != 0) return false;   // every block of rows starts 16-byte aligned
+    if (K < 2048 && (N + g.ROWS - 1) / g.ROWS < device_info().sms) return false;
+    return stream_geo_ok(g, false);
+}
+
+int launch_q4gemv_stream_q80(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream) {
+    return launch_stream_any(blocks, nullptr, nullptr, x, nullptr, 0.0f, 0, 32, y, N, K, 32, stream);
 }
 
 // ---- grouped launches (several matrices of the same K, one launch) ----

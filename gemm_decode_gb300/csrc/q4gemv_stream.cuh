@@ -39,14 +39,19 @@ __host__ __device__ constexpr int stream_round128(int v) { return (v + 127) / 12
 // Rows per consumer thread and block: 6 for K = 896 (48-row blocks: three CTAs fit an
 // SM), 8 otherwise.  Rows that span whole warps (K % 1024 == 0) need a power of two.
 __host__ __device__ constexpr int stream_u(int K) { return K == 896 ? 6 : 8; }
+// Q8_0 blocks carry 34 bytes per 32 codes: 4 rows per thread from K = 2048 on keep two
+// ring slots inside the shared memory.
+__host__ __device__ constexpr int stream_q80_u(int K) { return K == 896 ? 6 : 4; }
 
 // fused: the fused-variant kernels also keep their RMSNorm sums (one float per consumer
 // warp) in 128 bytes after the abort flag.  q40: the weights are Q4_0 blocks (32 codes and
 // their binary16 scale in 18 bytes), so a block of rows is one stretch of ROWS * C * 18
 // bytes (group 32, no zero points).  mx: rows of x (1, or 2 for the two-row instances),
-// each with its own x planes and partial sums.
+// each with its own x planes and partial sums.  q80: Q8_0 blocks (32 int8 codes and their
+// binary16 scale in 34 bytes), a block of rows one stretch of ROWS * C * 34 bytes.
 __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, int U, int D, bool asym,
-                                                        bool fused = false, bool q40 = false, int mx = 1) {
+                                                        bool fused = false, bool q40 = false, int mx = 1,
+                                                        bool q80 = false) {
     StreamGeo g{};
     g.C = K / 32;
     g.RG = RG;
@@ -57,12 +62,13 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
     g.ROWS = U * RG;
     g.TC = g.C * RG;
     g.NWC = g.TC / 32;
-    g.CODE_B = g.ROWS * g.C * (q40 ? 18 : 16);
-    g.SC_B = q40 ? 0 : g.ROWS * g.NB * 2;
-    g.Z_B = asym && !q40 ? g.ROWS * g.ZROW : 0;
-    // (Q4_0: 16 bytes of slack, as the 2-byte-aligned code reads fetch up to 2 bytes past
-    // a slot's last block)
-    g.SLOT_B = stream_round128(g.CODE_B + g.SC_B + g.Z_B + (q40 ? 16 : 0));
+    const bool blocks = q40 || q80;   // scale and codes interleaved per 32-element block
+    g.CODE_B = g.ROWS * g.C * (q40 ? 18 : (q80 ? 34 : 16));
+    g.SC_B = blocks ? 0 : g.ROWS * g.NB * 2;
+    g.Z_B = asym && !blocks ? g.ROWS * g.ZROW : 0;
+    // (Q4_0 / Q8_0: 16 bytes of slack, as the 2-byte-aligned code reads fetch up to 2 or 4
+    // bytes past a slot's last block)
+    g.SLOT_B = stream_round128(g.CODE_B + g.SC_B + g.Z_B + (blocks ? 16 : 0));
     g.WRED = g.C % 32 == 0 ? 1 : 0;
     g.PARTS = g.WRED ? g.C / 32 : g.C;
     g.RED_LD = g.PARTS + 1;
@@ -82,9 +88,10 @@ __host__ __device__ constexpr StreamGeo make_stream_geo(int K, int G, int RG, in
 // Ring slots: three (one more block in flight) when they fit the shared-memory
 // budget without lowering the CTAs an SM holds, else two.
 __host__ __device__ constexpr int stream_ctas_per_sm(int smem) { return kStreamSmemPerSM / (smem + 1024); }
-__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym, bool q40 = false, int mx = 1) {
-    const int s2 = make_stream_geo(K, G, RG, U, 2, asym, false, q40, mx).SMEM;
-    const int s3 = make_stream_geo(K, G, RG, U, 3, asym, false, q40, mx).SMEM;
+__host__ __device__ constexpr int stream_slots(int K, int G, int RG, int U, bool asym, bool q40 = false, int mx = 1,
+                                               bool q80 = false) {
+    const int s2 = make_stream_geo(K, G, RG, U, 2, asym, false, q40, mx, q80).SMEM;
+    const int s3 = make_stream_geo(K, G, RG, U, 3, asym, false, q40, mx, q80).SMEM;
     return (s3 <= kStreamSmemBudget && stream_ctas_per_sm(s3) >= stream_ctas_per_sm(s2)) ? 3 : 2;
 }
 
@@ -148,6 +155,9 @@ int launch_q4gemv_stream_fused(const uint8_t *codes, const uint16_t *scales, con
 // Q4_0 blocks (q4_0_gemv_run): whether the streamed kernel serves the problem, and the launch.
 bool stream_q40_applies(int M, int64_t N, int K, const void *blocks);
 int launch_q4gemv_stream_q40(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream);
+// Q8_0 blocks (q8_0_gemv_run): whether the streamed kernel serves the problem, and the launch.
+bool stream_q80_applies(int M, int64_t N, int K, const void *blocks);
+int launch_q4gemv_stream_q80(const uint8_t *blocks, const float *x, float *y, int64_t N, int K, cudaStream_t stream);
 // Grouped: whether one streamed launch serves these matrices (same K and group, all with or
 // all without zero points, every one streamable on its own alignment), and the launch.
 bool stream_grouped_applies(const StreamSeg *segs, int nseg, int K, int group);

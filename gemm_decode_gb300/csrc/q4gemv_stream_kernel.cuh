@@ -16,11 +16,11 @@ namespace {
 
 // The geometry an instance works with: compile-time when the instance fixes K, g
 // and RG (the tuned decode shapes), else the launcher's.
-template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED, bool Q40 = false, int MXC = 1>
+template <int KC, int GC, int RGC, int UC, bool ASYM, bool FUSED, bool Q40 = false, int MXC = 1, bool Q80 = false>
 __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
     if constexpr (KC != 0) {
-        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM, Q40, MXC), ASYM,
-                                                FUSED, Q40, MXC);
+        constexpr StreamGeo g = make_stream_geo(KC, GC, RGC, UC, stream_slots(KC, GC, RGC, UC, ASYM, Q40, MXC, Q80),
+                                                ASYM, FUSED, Q40, MXC, Q80);
         return g;
     } else {
         return rt;
@@ -38,6 +38,8 @@ __device__ __forceinline__ StreamGeo geo_of(const StreamGeo &rt) {
 // blocks (a.codes; 18 bytes per 32 codes: binary16 scale, then the codes; zero point 8).
 // FUSE = 8: a grouped launch (a.seg: several matrices, each served by its own CTAs).
 // FUSE = 16: two rows of x (M = 2): x[2][K], y[2][N], every block of codes serving both.
+// FUSE = 32: the weights are Q8_0 blocks (a.codes; 34 bytes per 32 codes: binary16 scale,
+// then 32 two's-complement 8-bit codes; no zero point).
 template <int KC, int GC, int RGC, int UC, bool ASYM, int FUSE>
 __global__ void __launch_bounds__(KC ? KC / 32 * RGC + 32 : kStreamMaxTC + 32, 1)
 q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
@@ -45,10 +47,12 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
     constexpr bool U_POW2 = (U & (U - 1)) == 0;
     constexpr bool NORM = (FUSE & 1) != 0, SWIG = (FUSE & 2) != 0, Q40 = (FUSE & 4) != 0, GROUPED = (FUSE & 8) != 0;
     constexpr int MX = (FUSE & 16) != 0 ? 2 : 1;   // rows of x
+    constexpr bool Q80 = (FUSE & 32) != 0;
+    static_assert(!Q80 || (!ASYM && (KC == 0 || GC == 32) && FUSE == 32), "Q8_0: group 32, no zero points, plain");
     static_assert(!Q40 || (!ASYM && (KC == 0 || GC == 32) && FUSE == 4), "Q4_0: group 32, symmetric, not fused");
     static_assert(!GROUPED || FUSE == 8, "grouped launches are plain");
     static_assert(MX == 1 || FUSE == 16, "two rows of x: plain launches only");
-    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40, MX>(a.geo);
+    const StreamGeo G = geo_of<KC, GC, RGC, UC, ASYM, (FUSE & 3) != 0, Q40, MX, Q80>(a.geo);
     const int D = G.D;
     const int C = G.C;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -140,12 +144,13 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
                 const unsigned char *src_z = ASYM ? w_zeros + row0 * G.ZROW : nullptr;
                 if (!ib(row0 >= 0 && rows >= 1 && row0 + rows <= w_N && s < D)) {
                     mbar_arrive(full(s));   // (checking builds) keep the ring moving, copy nothing
-                } else if constexpr (Q40) {
-                    // Q4_0: one stretch of rows * C * 18 bytes (a 16-byte multiple for a whole
-                    // block of rows); its largest 16-byte multiple by bulk copy, the at most
-                    // 15 bytes left by plain copies, published by the arrive below
-                    const unsigned char *src = w_codes + row0 * (C * 18);
-                    const int cb = rows * C * 18, cb16 = cb & ~15;
+                } else if constexpr (Q40 || Q80) {
+                    // Q4_0 / Q8_0: one stretch of rows * C * 18 (34) bytes (a 16-byte multiple
+                    // for a whole block of rows); its largest 16-byte multiple by bulk copy, the
+                    // at most 15 bytes left by plain copies, published by the arrive below
+                    constexpr int QB = Q40 ? 18 : 34;
+                    const unsigned char *src = w_codes + row0 * (C * QB);
+                    const int cb = rows * C * QB, cb16 = cb & ~15;
                     unsigned char *sl = smem + G.OFF_RING + s * G.SLOT_B;
                     for (int j = cb16; j < cb; ++j) sl[j] = src[j];
                     mbar_expect_tx(full(s), cb16);
@@ -334,6 +339,25 @@ q4gemv_stream_kernel(const StreamArgsOf<FUSE> a) {
         for (int u = 0; u < U; ++u) {
             uint4 cw;
             uint32_t sh;
+            if constexpr (Q80) {
+                // block (r + RG u) * C + c: its scale at 34 * block, its 32 code bytes from
+                // 34 * block + 2 (2-byte aligned): nine words from the 4-byte boundary below,
+                // shifted by 0 or 16 bits (the ninth may reach 4 bytes past the block, inside
+                // the slot's 16 bytes of slack after its last block)
+                const uint32_t boff = static_cast<uint32_t>((r * C + c) * 34) + u * static_cast<uint32_t>(G.RG * C * 34);
+                const bool b_ok = ib(boff + 34 <= static_cast<uint32_t>(G.CODE_B));
+                const uint32_t cstart = boff + 2, base = cstart & ~3u, shift = (cstart & 3u) * 8u;
+                uint32_t w[9];
+#pragma unroll
+                for (int i = 0; i < 9; ++i) w[i] = b_ok ? lds_u32(sl + base + 4 * i) : 0u;
+                uint32_t c8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) c8[i] = __funnelshift_r(w[i], w[i + 1], shift);
+                const uint32_t dh = b_ok ? lds_u16(sl + boff) : 0u;
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(dh)));
+                v[0][u] = (d * P[0].f) * chunk_dot_q8(c8, P[0]);
+                continue;
+            }
             if constexpr (Q40) {
                 // block (r + RG u) * C + c: its scale at 18 * block, its 16 code bytes from
                 // 18 * block + 2 (2-byte aligned): five words from the 4-byte boundary below,
@@ -544,6 +568,11 @@ int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
         if constexpr (GV == 32) return asym ? Q4_ERR_UNSUPPORTED : launch_stream<KV, 32, RGV, UV, false, 4>(a, s);
         return Q4_ERR_UNSUPPORTED;
     }
+    if (fuse == 32) {   // Q8_0 blocks: group 32, no zero points
+        constexpr int UQ = stream_q80_u(KV);
+        if constexpr (GV == 32) return asym ? Q4_ERR_UNSUPPORTED : launch_stream<KV, 32, RGV, UQ, false, 32>(a, s);
+        return Q4_ERR_UNSUPPORTED;
+    }
     if (fuse == 16) {   // two rows of x: the one-CTA-per-SM geometries (K >= 2048)
         if constexpr (KV >= 2048)
             return asym ? launch_stream<KV, GV, RGV, UV, true, 16>(a, s) : launch_stream<KV, GV, RGV, UV, false, 16>(a, s);
@@ -558,7 +587,7 @@ int launch_stream_kg(const StreamArgs &a, bool asym, int fuse, cudaStream_t s) {
 }
 
 // One translation unit per K instantiates the compile-time geometries of that K (plain,
-// RMSNorm, RMSNorm + SwiGLU, Q4_0, grouped, and for K >= 2048 two rows of x).
+// RMSNorm, RMSNorm + SwiGLU, Q4_0, Q8_0, grouped, and for K >= 2048 two rows of x).
 #define Q4_STREAM_K_LAUNCHER(KV, RGV)                                                                    \
     int launch_stream_k##KV(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s) {    \
         switch (group) {                                                                              \

@@ -20,6 +20,16 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
     asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
 }
@@ -174,6 +184,26 @@ __device__ __forceinline__ float chunk_dot(const uint4 &cw, int z, const Planes 
     const int lo = a1 * 256 + a0 - z * P.s_lo;   // planes 0 and 1
     const int hi = a2 - z * P.s_hi;               // plane 2
     return fmaf(static_cast<float>(hi), 65536.0f, static_cast<float>(lo));
+}
+
+// Integer dot product of one Q8_0 block's 32 signed 8-bit codes (cw[j]: elements 4j ..
+// 4j + 3, one per byte) with one x chunk: sum_k q_k m_k, exact in int32 (|lo| < 2^30),
+// returned as binary32.  Two byte permutes per 8 codes regroup them into the even and
+// odd elements the planes hold; no zero point.
+__device__ __forceinline__ float chunk_dot_q8(const uint32_t (&cw)[8], const Planes &P) {
+    int a0 = 0, a1 = 0, a2 = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t ev = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x6420u);   // elements 8w, 8w+2, 8w+4, 8w+6
+        const uint32_t od = __byte_perm(cw[2 * w], cw[2 * w + 1], 0x7531u);   // elements 8w+1, 8w+3, 8w+5, 8w+7
+        a0 = dp4a_su(ev, P.p[6 * w + 0], a0);
+        a0 = dp4a_su(od, P.p[6 * w + 1], a0);
+        a1 = dp4a_su(ev, P.p[6 * w + 2], a1);
+        a1 = dp4a_su(od, P.p[6 * w + 3], a1);
+        a2 = dp4a_ss(ev, P.p[6 * w + 4], a2);
+        a2 = dp4a_ss(od, P.p[6 * w + 5], a2);
+    }
+    return fmaf(static_cast<float>(a2), 65536.0f, static_cast<float>(a1 * 256 + a0));
 }
 
 // The same for two rows of x at once: the codes are unpacked once and serve both rows'

@@ -235,6 +235,21 @@ Q4_API int q4gemv_grouped_run_ex(const q4gemv_segment_t *segs, int32_t count, in
 Q4_API int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K,
                   void *stream);
 
+/* GEMV over a third weight format, Q8_0 blocks (cera wgpu_gemv_bench.rs, block geometry:
+ * Q8_0 holds 32 elements in 34 bytes), 1 <= M <= 16:
+ * y[m][n] = sum_k q[n][k] * d[n][k/32] * x[m][k].
+ *   blocks : device, [N][K/32][34] bytes, 2-byte aligned: per block the binary16 scale d
+ *            (little-endian), then 32 codes, two's-complement int8, element j at byte 2 + j
+ *            (no zero point)
+ *   x : device float [M][K], 16-byte aligned;  y : device float [M][N]
+ * K a multiple of 32.  M = 1 with N >= 4096 and blocks 16-byte aligned runs the
+ * TMA-streamed kernel's Q8_0 instances (dp4a on the byte planes of x: the dp4a kernels'
+ * accuracy, with sum |w| = sum |q d|); every other shape a CUDA-core kernel in which each
+ * code is widened exactly and each block's 32 products are summed with fused multiply-adds
+ * and scaled once by d.  Asynchronous; allocates nothing. */
+Q4_API int q8_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K,
+                  void *stream);
+
 /* Prefill-shaped int4 matmul on the tensor cores (tcgen05, bf16 operands, f32
  * accumulate in tensor memory), any M >= 1 (tiles of 128 rows; a partial tile is
  * padded and masked).

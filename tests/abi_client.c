@@ -48,6 +48,8 @@ int main(void)
     expect(q4gemv_fused_run(A, A, NULL, F, NULL, 0.0f, F, 1, 63, 64, 32, Q4_EPILOGUE_SWIGLU, NULL) ==
                Q4_ERR_INVALID_ARG, "odd N with SwiGLU");
     expect(q4_0_gemv_run(A, F, F, 1, 64, 48, NULL) == Q4_ERR_INVALID_ARG, "Q4_0 K % 32 != 0");
+    expect(q8_0_gemv_run(A, F, F, 1, 64, 48, NULL) == Q4_ERR_INVALID_ARG, "Q8_0 K % 32 != 0");
+    expect(q8_0_gemv_run(A, F, F, 17, 64, 64, NULL) == Q4_ERR_UNSUPPORTED, "Q8_0 M > 16");
     expect(q4gemm_run(A, A, NULL, A, F, 1, 64, 100, 32, NULL) == Q4_ERR_INVALID_ARG, "gemm K % g != 0");
     expect(f32gemv_run(F, F, F, 17, 64, 64, NULL) == Q4_ERR_UNSUPPORTED, "f32 M > 16");
 

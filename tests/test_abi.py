@@ -213,6 +213,18 @@ def test_q40_argument_checks(L):
     assert r(A + 2, A + 4, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED  # x: 16-byte aligned
 
 
+def test_q80_argument_checks(L):
+    r = L.q8_0_gemv_run
+    assert r(A, A, A, 1, 64, 48, None) == q4.Q4_ERR_INVALID_ARG      # K not a multiple of 32
+    assert r(A, A, A, -1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A, A, A, 17, 64, 64, None) == q4.Q4_ERR_UNSUPPORTED
+    assert r(None, None, None, 0, 64, 64, None) == q4.Q4_OK
+    assert r(None, A, A, 1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG
+    assert r(A + 1, A, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED    # blocks: 2-byte aligned
+    assert r(A + 2, A + 4, A, 1, 64, 64, None) == q4.Q4_ERR_MISALIGNED  # x: 16-byte aligned
+    assert r(B0, B3, B0 + 64, 1, 64, 64, None) == q4.Q4_ERR_INVALID_ARG  # y inside the blocks
+
+
 def test_gemm_and_control_argument_checks(L):
     g = L.q4gemm_run
     assert g(A, A, None, A, A, 1, 64, 100, 32, None) == q4.Q4_ERR_INVALID_ARG

@@ -156,3 +156,15 @@ def test_split_matmul_kernel(torch, M, N, K, g):
     c_ref, bound = oracle.q4_gemm(w.codes, w.scales, w.zeros, a, g)
     err = np.abs(host(c).astype(np.float64) - c_ref.astype(np.float64))
     assert np.all(err <= (2.0 ** -9 + 2e-6) * bound + 1e-6)
+
+
+@pytest.mark.parametrize("N,K", [(9765, 896), (4101, 14336), (4901, 4096)])
+def test_q80_streamed_kernel(torch, N, K):
+    blocks = synth.q80_blocks(N + 9, N, K)
+    x = synth.activations_f32(N + 10, 1, K)
+    y = torch.full((1, N), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q8_0_gemv_run(dev(blocks, torch), dev(x, torch), y, 1, N, K)
+    assert q4.q4gemv_bounds_violations() == 0, f"Q8_0 N={N} K={K}: out-of-range accesses counted"
+    rows = sorted(set(np.random.default_rng(3).choice(N, 64, replace=False).tolist()) | {0, N - 1})
+    y_ref, bound = oracle.q80_gemv_rows(blocks, x, rows)
+    assert_within_bound(host(y)[:, rows], y_ref, bound, f"Q8_0 bounds N={N} K={K}")
