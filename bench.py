@@ -871,7 +871,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--controls", type=int, default=1)
     p.add_argument("--profile", choices=["none", "lm_head", "lm_head_fused", "lm_head_8b", "down_8b", "tc_m16",
-                                         "tc_lm05_m8", "tc_down8b_m8", "f32_lm_head", "gemm_ffn", "gemm_gate"],
+                                         "tc_lm05_m8", "tc_down8b_m8", "f32_lm_head", "gemm_ffn", "gemm_gate",
+                                         "q80_lm_head_m4", "q80_lm_head_8b"],
                    default="none",
                    help="launch one kernel a few times on a small case and exit (for ncu)")
     p.add_argument("--sweep", action="store_true",
@@ -920,6 +921,16 @@ def run_profile_case(args):
             q4.q4gemm_run(cw, sw, zw, a, c, M, N, K, 32)
         torch.cuda.synchronize()
         print(json.dumps({"profile": args.profile, "launches": 4}))
+        return
+    if args.profile.startswith("q80_"):
+        N, K, M = (151936, 896, 4) if args.profile == "q80_lm_head_m4" else (128256, 4096, 1)
+        reps = [dev(synth.q80_blocks(5 + i, N, K)) for i in range(2)]
+        x = dev(synth.activations_f32(5, M, K))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        for i in range(7):
+            q4.q8_0_gemv_run(reps[i % 2], x, y, M, N, K)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": args.profile, "launches": 7}))
         return
     if args.profile == "f32_lm_head":
         N, K = 151936, 896

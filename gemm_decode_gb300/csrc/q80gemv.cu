@@ -7,11 +7,14 @@
 //
 // M = 1 on long matrices runs the TMA-streamed kernel's Q8_0 instances (a block of rows
 // is one stretch of 34-byte blocks, dp4a on the byte planes of x; q4gemv_stream.cu).
-// Every other shape runs the kernel below on CUDA cores: one warp per weight row, its
-// lanes striding over the row's blocks; each code is widened exactly to binary32, the 32
-// products of a block summed with fused multiply-adds and scaled once by d, the blocks
-// summed over the lanes by shuffles.  Blocks are only 2-byte aligned, so a block is read
-// as 17 16-bit loads; x is read through the read-only cache as 16-byte vectors.
+// Every other shape runs the kernel below on CUDA cores.  A warp takes two blocks of a
+// row at a time, lanes 0-15 the first and 16-31 the second, each lane two neighbouring
+// elements (one 16-bit load of codes: blocks are only 2-byte aligned), so that a warp's
+// read of a row of x is 256 contiguous bytes.  Each weight q * d is formed exactly in
+// binary32 (an 8-bit integer times an 11-bit significand) and accumulated with fused
+// multiply-adds.  A warp carries R rows of weights, so that each load of x serves R rows;
+// when the rows alone would give too few CTAs, the warps of a CTA split the blocks of
+// their rows and add their partial sums in shared memory in warp order.
 #include "q4_common.cuh"
 #include "q4gemv_stream.cuh"
 
@@ -20,62 +23,106 @@ namespace q4 {
 namespace {
 
 constexpr int kQ80Threads = 256;
-constexpr int kQ80RowsPerCta = kQ80Threads / 32;
+constexpr int kQ80Warps = kQ80Threads / 32;
 
-template <int MT>
-__global__ void __launch_bounds__(kQ80Threads)
-q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x, float *__restrict__ y, int M,
-                int64_t N, int K) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n = static_cast<int64_t>(blockIdx.x) * kQ80RowsPerCta + warp;
-    if (n >= N) return;   // (warp-uniform)
-    wait_prior_grid();    // x may belong to the kernel before this one in the stream
-    const int nblk = K / 32;
-    const uint16_t *row = reinterpret_cast<const uint16_t *>(blocks + n * static_cast<int64_t>(nblk) * 34);
-    float acc[MT];
+// Sums each of v[0 .. V-1] over the 32 lanes of the warp (V a power of two, <= 32):
+// halving exchanges leave lane l holding, in v[0], the whole sum of entry l / (32 / V).
+template <int V>
+__device__ __forceinline__ void warp_sum_scatter(float (&v)[V], int lane) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] = 0.0f;
-    for (int b = lane; b < nblk; b += 32) {
-        const uint16_t *h = row + b * 17;           // block b: 17 half-words
-        const float d = half_bits_to_float(ldg_u16(h));
-        uint32_t w[8];
+    for (int s = 0; s < 5; ++s) {
+        const int o = 16 >> s;
+        const int c = V >> s;   // entries still held by each lane
+        if (c >= 2) {
+            const bool upper = (lane & o) != 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w[i] = ldg_u16(h + 1 + 2 * i) | (ldg_u16(h + 2 + 2 * i) << 16);
-        float s[MT];
-#pragma unroll
-        for (int m = 0; m < MT; ++m) s[m] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // codes 4i .. 4i + 3 of the block, sign-extended and widened exactly
-            float q[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) q[e] = static_cast<float>(static_cast<int32_t>(w[i] << (24 - 8 * e)) >> 24);
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                if (m < M) {
-                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + static_cast<int64_t>(m) * K + b * 32) + i);
-                    s[m] = fmaf(q[0], xv.x, s[m]);
-                    s[m] = fmaf(q[1], xv.y, s[m]);
-                    s[m] = fmaf(q[2], xv.z, s[m]);
-                    s[m] = fmaf(q[3], xv.w, s[m]);
-                }
+            for (int i = 0; i < c / 2; ++i) {
+                const float send = upper ? v[i] : v[i + c / 2];
+                const float keep = upper ? v[i + c / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
         }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] = fmaf(d, s[m], acc[m]);
-    }
-    allow_next_grid();
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-        if (lane == m && m < M) y[static_cast<int64_t>(m) * N + n] = acc[m];
     }
 }
 
-template <int MT>
-int launch_q80_mt(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
-    const int64_t grid = (N + kQ80RowsPerCta - 1) / kQ80RowsPerCta;
+// MT rows of x at most (M <= MT at run time), R weight rows per warp, ksplit warps per
+// group of rows (a divisor of 8).  Entry e = m * R + r of a lane's sums is y[m][n0 + r].
+template <int MT, int R>
+__global__ void __launch_bounds__(kQ80Threads)
+q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x, float *__restrict__ y, int M,
+                int64_t N, int K, int ksplit) {
+    constexpr int V = MT * R;
+    static_assert(V <= 32 && (V & (V - 1)) == 0, "entries per lane");
+    __shared__ float part[kQ80Warps][V];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = warp / ksplit, kw = warp - group * ksplit;
+    const int64_t n0 = (static_cast<int64_t>(blockIdx.x) * (kQ80Warps / ksplit) + group) * R;
+    const int nblk = K >> 5, npair = (nblk + 1) >> 1;
+    const int half = lane >> 4, j = lane & 15;
+    // rows past N read row N - 1; their sums are not stored
+    const uint16_t *row[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t n = n0 + r < N ? n0 + r : N - 1;
+        row[r] = reinterpret_cast<const uint16_t *>(blocks) + n * nblk * 17;
+    }
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.0f;
+    wait_prior_grid();   // x may belong to the kernel before this one in the stream
+#pragma unroll 2
+    for (int p = kw; p < npair; p += ksplit) {
+        const int bl = 2 * p + half;
+        const bool live = bl < nblk;           // false only for lanes 16-31 past an odd last block
+        const int b = live ? bl : nblk - 1;
+        float t0[R], t1[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t c = ldg_u16(row[r] + b * 17 + 1 + j);   // elements 2j (low byte), 2j + 1
+            const float d = live ? half_bits_to_float(ldg_u16(row[r] + b * 17)) : 0.0f;
+            t0[r] = static_cast<float>(static_cast<int32_t>(c << 24) >> 24) * d;
+            t1[r] = static_cast<float>(static_cast<int32_t>(c << 16) >> 24) * d;
+        }
+        const float *xb = x + b * 32 + 2 * j;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const float2 xv = __ldg(reinterpret_cast<const float2 *>(xb + static_cast<int64_t>(m) * K));
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    acc[m * R + r] = fmaf(t0[r], xv.x, acc[m * R + r]);
+                    acc[m * R + r] = fmaf(t1[r], xv.y, acc[m * R + r]);
+                }
+            }
+        }
+    }
+    allow_next_grid();
+    warp_sum_scatter<V>(acc, lane);
+    constexpr int kCopies = 32 / V;   // lanes holding the same entry
+    const int e = lane / kCopies;
+    const bool writer = (lane % kCopies) == 0;
+    if (ksplit == 1) {
+        const int m = e / R, r = e - (e / R) * R;
+        if (writer && m < M && n0 + r < N) y[static_cast<int64_t>(m) * N + n0 + r] = acc[0];
+        return;
+    }
+    if (writer) part[warp][e] = acc[0];
+    __syncthreads();
+    if (kw == 0 && lane < V) {
+        float s = part[warp][lane];
+        for (int w = 1; w < ksplit; ++w) s += part[warp + w][lane];
+        const int m = lane / R, r = lane - (lane / R) * R;
+        if (m < M && n0 + r < N) y[static_cast<int64_t>(m) * N + n0 + r] = s;
+    }
+}
+
+template <int MT, int R>
+int launch_q80(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, int ksplit,
+               cudaStream_t stream) {
+    const int64_t rows_per_cta = static_cast<int64_t>(kQ80Warps / ksplit) * R;
+    const int64_t grid = (N + rows_per_cta - 1) / rows_per_cta;
     if (grid > 0x7fffffffLL) return Q4_ERR_UNSUPPORTED;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -84,7 +131,7 @@ int launch_q80_mt(const uint8_t *blocks, const float *x, float *y, int M, int64_
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     add_overlap_attr(cfg, attr);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, q80_gemv_kernel<MT>, blocks, x, y, M, N, K);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, q80_gemv_kernel<MT, R>, blocks, x, y, M, N, K, ksplit);
     if (e != cudaSuccess) {
         set_cuda_error(e);
         return Q4_ERR_CUDA;
@@ -92,16 +139,40 @@ int launch_q80_mt(const uint8_t *blocks, const float *x, float *y, int M, int64_
     return launch_status();
 }
 
+// The smallest split of the blocks over the warps of a CTA (1, 2, 4 or 8, at most the
+// pairs of blocks in a row) that gives at least `want` CTAs, or the largest allowed.
+int q80_split(int64_t N, int R, int npair, int64_t want) {
+    int ks = 1;
+    while (ks < kQ80Warps && 2 * ks <= npair) {
+        const int64_t rows = static_cast<int64_t>(kQ80Warps / ks) * R;
+        if ((N + rows - 1) / rows >= want) break;
+        ks *= 2;
+    }
+    return ks;
+}
+
+// R = RW (2 to 4 weight rows per warp) where that still gives `want` CTAs, else one row
+// per warp.
+template <int MT, int RW>
+int launch_q80_m(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
+    const int npair = (K / 32 + 1) / 2;
+    const int64_t want = 4LL * device_info().sms;
+    const int ks = q80_split(N, RW, npair, want);
+    const int64_t rows = static_cast<int64_t>(kQ80Warps / ks) * RW;
+    if ((N + rows - 1) / rows >= want) return launch_q80<MT, RW>(blocks, x, y, M, N, K, ks, stream);
+    return launch_q80<MT, 1>(blocks, x, y, M, N, K, q80_split(N, 1, npair, want), stream);
+}
+
 }  // namespace
 
 int launch_q80gemv(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
     if (!call_options().exact_x && stream_q80_applies(M, N, K, blocks))
         return launch_q4gemv_stream_q80(blocks, x, y, N, K, stream);
-    if (M <= 1) return launch_q80_mt<1>(blocks, x, y, M, N, K, stream);
-    if (M <= 2) return launch_q80_mt<2>(blocks, x, y, M, N, K, stream);
-    if (M <= 4) return launch_q80_mt<4>(blocks, x, y, M, N, K, stream);
-    if (M <= 8) return launch_q80_mt<8>(blocks, x, y, M, N, K, stream);
-    return launch_q80_mt<16>(blocks, x, y, M, N, K, stream);
+    if (M <= 1) return launch_q80_m<1, 4>(blocks, x, y, M, N, K, stream);
+    if (M <= 2) return launch_q80_m<2, 4>(blocks, x, y, M, N, K, stream);
+    if (M <= 4) return launch_q80_m<4, 4>(blocks, x, y, M, N, K, stream);
+    if (M <= 8) return launch_q80_m<8, 4>(blocks, x, y, M, N, K, stream);
+    return launch_q80_m<16, 2>(blocks, x, y, M, N, K, stream);
 }
 
 }  // namespace q4

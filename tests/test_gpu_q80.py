@@ -37,8 +37,15 @@ def run(torch, blocks, x):
     return b[guard:guard + M * N].reshape(M, N)
 
 
+# On 152 SMs these reach every plan of the CUDA-core kernel: 4 weight rows per warp with
+# the blocks unsplit (40003 x 896, 20001 x 608 with an odd 19 blocks per row) or split over
+# 4 or 8 warps (4864 x 896, 4096 x 4096, 3001 x 608), 2 rows per warp at M = 16 (9001 x 864,
+# 27 blocks), one row per warp split over 4 or 8 warps (2051 x 4096, 896 x 896), ragged
+# last CTAs, a single block per row (K = 32: lanes 16-31 idle) and single rows.
 @pytest.mark.parametrize("M,N,K", [(1, 896, 896), (2, 4864, 896), (1, 896, 4864), (3, 1000, 2048), (4, 4096, 4096),
-                                   (8, 300, 16384), (16, 512, 2048), (5, 77, 32), (1, 1, 64), (2, 33, 4864)])
+                                   (8, 300, 16384), (16, 512, 2048), (5, 77, 32), (1, 1, 64), (2, 33, 4864),
+                                   (4, 40003, 896), (3, 20001, 608), (16, 9001, 864), (2, 2051, 4096),
+                                   (1, 3001, 608), (7, 4099, 1056)])
 def test_cuda_core_kernel_against_oracle(torch, M, N, K):
     blocks = synth.q80_blocks(M + N + K, N, K)
     x = synth.activations_f32(M * N + K, M, K)
