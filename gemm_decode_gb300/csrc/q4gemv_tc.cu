@@ -80,6 +80,8 @@ struct TcArgs {
     int64_t N;
     int M, K, nb, zrow, gshift;
     int S;                  // K split: CTAs per cluster (grid y), 1 = no cluster
+    int side_vec;           // nb % 4 == 0, scales 8-byte and zeros 2-byte aligned: a chunk of
+                            // four groups' side data is one 8-byte and one 2-byte load
     unsigned long long timeout_ns;
     unsigned int *status;
     unsigned int *bounds;   // out-of-range access counter (bounds-checking builds)
@@ -259,23 +261,56 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         const int xm = t / TPR;                    // x row (< MP)
         const int xk = (t - xm * TPR) * VPT;       // first slot of the share within the block
 
-        // scales of this thread's halves of K-block kb (the same group unless g = 32), the
-        // zero-point byte that holds their nibbles (with two halves and g = 32 the first
-        // half's group is even), and this thread's share of x for the block
+        // 256-row tiles (a whole 64-code row segment per thread and block): scales and zero
+        // points come in chunks of four groups of this thread's row: the four binary16 scales
+        // in two words and the four zero nibbles in 16 bits (8 each when symmetric), one
+        // 8-byte and one 2-byte load per chunk where the layout allows (side_vec), else one
+        // load per value.  The chunk in use and the next one (in flight) are held in
+        // registers: a chunk spans 2 (g = 32) to 8 (g = 128) K-blocks, and the K-blocks'
+        // groups never skip a chunk (at most two groups per block).  (Measured against one
+        // 2-byte load per scale and one 1-byte load per zero-point pair and block, prefetched
+        // four blocks ahead: 3-8 % faster with 256-row tiles, 2-13 % slower with 128-row
+        // tiles, whose threads convert half a block each; those keep the per-block loads.)
+        // (volatile: issued where written, a chunk ahead of its use)
+        auto load_chunk = [&](int c, uint2 &sv, uint32_t &zv) {
+            const int g0 = 4 * c;
+            if (g.side_vec) {
+                if (ib(g0 + 4 <= g.nb)) {
+                    asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(sv.x), "=r"(sv.y) : "l"(srow + g0));
+                }
+                zv = 0x8888u;
+                if (zrow && ib((g0 >> 1) + 2 <= g.zrow)) {
+                    unsigned short h;
+                    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(h) : "l"(zrow + (g0 >> 1)));
+                    zv = h;
+                }
+            } else {
+                uint32_t v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) v[i] = g0 + i < g.nb ? ldg_u16(srow + g0 + i) : 0u;
+                sv = make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+                zv = 0x8888u;
+                if (zrow) {
+                    const uint32_t z0 = ldg_u8(zrow + (g0 >> 1));
+                    const uint32_t z1 = (g0 >> 1) + 1 < g.zrow ? ldg_u8(zrow + (g0 >> 1) + 1) : 0u;
+                    zv = z0 | (z1 << 8);
+                }
+            }
+        };
+        // 128-row tiles: the scale of this thread's half of K-block kb and the zero-point byte
+        // that holds its nibble; both tile heights: this thread's share of x for the block
         struct Side {
-            uint32_t sc[NH], zb;
+            uint32_t sc, zb;
             float xv[VPT];
         };
         auto fetch_w = [&](Side &f, int kb) {
-            const int k = kb * TK + h0 * 32;
-            if (kb < kb_end && k < g.K) {
-                const int grp0 = k >> (5 + g.gshift);
-                if (ib(grp0 < g.nb)) f.sc[0] = ldg_u16(srow + grp0);
-                if constexpr (NH == 2) {
-                    const int grp1 = (k + 32) >> (5 + g.gshift);
-                    if (k + 32 < g.K && ib(grp1 < g.nb)) f.sc[1] = grp1 == grp0 ? f.sc[0] : ldg_u16(srow + grp1);
+            if constexpr (NH == 1) {
+                const int k = kb * TK + h0 * 32;
+                if (kb < kb_end && k < g.K) {
+                    const int grp0 = k >> (5 + g.gshift);
+                    if (ib(grp0 < g.nb)) f.sc = ldg_u16(srow + grp0);
+                    if (zrow && ib((grp0 >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp0 >> 1));
                 }
-                if (zrow && ib((grp0 >> 1) < g.zrow)) f.zb = ldg_u8(zrow + (grp0 >> 1));
             }
         };
         // slots xk .. xk + VPT - 1 of a block hold x at k = 8 * (slot / 8) + slot_k(slot % 8):
@@ -298,6 +333,16 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
         };
         static_assert(PF == 4, "the K loop below is unrolled over four register sets");
         Side f0{}, f1{}, f2{}, f3{};
+        // the chunk of the first K-block's groups, and the next one
+        int cur_c = ((kb_begin * TK + h0 * 32) >> (5 + g.gshift)) >> 2;
+        uint2 sc_cur = make_uint2(0u, 0u), sc_next = make_uint2(0u, 0u);
+        uint32_t z_cur = 0x8888u, z_next = 0x8888u;
+        if constexpr (NH == 2) {
+            if (nkb > 0 && kb_begin * TK < g.K) {
+                load_chunk(cur_c, sc_cur, z_cur);
+                if (4 * (cur_c + 1) < g.nb) load_chunk(cur_c + 1, sc_next, z_next);
+            }
+        }
         fetch_w(f0, kb_begin);
         fetch_w(f1, kb_begin + 1);
         fetch_w(f2, kb_begin + 2);
@@ -338,6 +383,15 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
             }
             if (j >= WST && !mbar_wait(wempty(ws), ((j / WST) - 1) & 1, limit)) return false;
             const uint32_t wrow_addr = smem_addr(wtiles + ws * kWTile) + w_row;
+            // (256-row tiles) move to the next chunk of side data when this block's groups start it
+            if constexpr (NH == 2) {
+                if (kb * TK < g.K && (((kb * TK) >> (5 + g.gshift)) >> 2) != cur_c) {
+                    sc_cur = sc_next;
+                    z_cur = z_next;
+                    ++cur_c;
+                    if (4 * (cur_c + 1) < g.nb) load_chunk(cur_c + 1, sc_next, z_next);
+                }
+            }
             // this thread's 32-code halves of the row's block, one after the other
 #pragma unroll
             for (int i = 0; i < NH; ++i) {
@@ -345,16 +399,23 @@ q4gemv_tc_kernel(const __grid_constant__ CUtensorMap tmap_codes, const TcArgs g)
                 const int k = kb * TK + h * 32;    // first code of this half
                 uint32_t out[16];
                 if (k < g.K) {
-                    const int grp = k >> (5 + g.gshift);
-                    uint32_t z = 8u;
-                    if (zrow) z = (grp & 1) ? (f.zb >> 4) : (f.zb & 0xFu);
+                    uint32_t z = 8u, ss;
+                    if constexpr (NH == 2) {
+                        const int gi = (k >> (5 + g.gshift)) & 3;   // the group's place in the chunk
+                        z = (z_cur >> (4 * gi)) & 0xFu;
+                        // the group's binary16 scale in both halves
+                        ss = __byte_perm(gi & 2 ? sc_cur.y : sc_cur.x, 0u, gi & 1 ? 0x3232u : 0x1010u);
+                    } else {
+                        const int grp = k >> (5 + g.gshift);
+                        if (zrow) z = (grp & 1) ? (f.zb >> 4) : (f.zb & 0xFu);
+                        ss = f.sc * 0x00010001u;
+                    }
                     // fp16 1024 + q from a nibble OR-ed into the fraction of 1024 (0x6400); the
                     // half2 subtraction of 1024 + z is exact, and one half2 multiply by s rounds the
                     // exact product (q - z) * s once -- the same value as rounding the binary32
                     // product.  Each word gives the nibble pairs (0,4), (1,5), (2,6), (3,7), stored
                     // in that order; x is stored with the same permutation of k.
                     const uint32_t zz = (0x6400u | z) * 0x00010001u;
-                    const uint32_t ss = f.sc[i] * 0x00010001u;
                     const uint32_t words[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
 #pragma unroll
                     for (int w = 0; w < 4; ++w) {
@@ -619,6 +680,7 @@ int launch_q4gemv_tc(const uint8_t *codes, const uint16_t *scales, const uint8_t
     if (g.status == nullptr) return Q4_ERR_CUDA;
     g.bounds = bounds_counter();
     g.S = tc_gemv_split(N, K, tm);
+    g.side_vec = (g.nb % 4 == 0 && aligned(scales, 8) && (zeros == nullptr || aligned(zeros, 2))) ? 1 : 0;
     return tm == 256 ? launch_tc_rows<256>(map, g, stream) : launch_tc_rows<128>(map, g, stream);
 }
 

@@ -71,6 +71,41 @@ def test_shapes_against_oracle(torch, N, K, g, symmetric):
         check(torch, w, x, f"M={M} N={N} K={K} g={g} sym={symmetric}")
 
 
+def _offset_copy(torch, a, offset_bytes):
+    """A device copy of uint8/uint16 array `a` whose data starts `offset_bytes` past a
+    256-byte boundary (a view into a larger buffer)."""
+    raw = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+    buf = torch.zeros(raw.size + 256, dtype=torch.uint8, device="cuda")
+    buf[offset_bytes:offset_bytes + raw.size] = torch.from_numpy(raw).cuda()
+    return buf[offset_bytes:offset_bytes + raw.size]
+
+
+@pytest.mark.parametrize("K,g,scale_off,zero_off", [
+    (896, 32, 2, 1),      # 28 groups: four-group loads possible, but scales 2 bytes past 8 and zeros odd
+    (2048, 64, 6, 0),     # scales 6 bytes past an 8-byte boundary
+    (896, 64, 0, 0),      # 14 groups per row: rows of scales only 4-byte aligned
+    (896, 128, 0, 0),     # 7 groups per row (a partial last chunk, 4 zero-point bytes per row)
+    (4128, 32, 0, 1),     # 129 groups, the last K-block half empty
+])
+def test_side_data_loaded_one_value_at_a_time(torch, K, g, scale_off, zero_off):
+    # Scales and zero points come in chunks of four groups per row: one 8-byte and one
+    # 2-byte load where the groups per row are a multiple of 4 and the arrays 8- and
+    # 2-byte aligned, else one load per value.  These cases take the second form.
+    N = 8192
+    w = synth.q4_weights(K + g + scale_off, N, K, g, tag="tc-side")
+    sc = _offset_copy(torch, w.scales, scale_off)
+    zr = _offset_copy(torch, w.zeros, zero_off)
+    for M in (5, 16):
+        x = synth.activations_f32(M + K, M, K)
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        q4.q4gemv_run(dev(w.codes, torch), sc.data_ptr(), zr.data_ptr(), dev(x, torch), y, M, N, K, g)
+        torch.cuda.synchronize()
+        y_ref, bound = oracle.q4_gemv(w.codes, w.scales, w.zeros, x, g)
+        assert_within_bound(host(y), y_ref, bound, f"side data one value at a time K={K} g={g} M={M}")
+        err = np.abs(host(y).astype(np.float64) - y_ref.astype(np.float64))
+        assert np.all(err <= FP16_REL * bound + 1e-6)
+
+
 def test_few_rows_of_x_on_a_tall_matrix(torch):
     # M = 3 and 4 take the tensor cores only for N >= 65536
     N, K = 65600, 896
