@@ -48,54 +48,88 @@ __device__ __forceinline__ void warp_sum_scatter(float (&v)[V], int lane) {
 }
 
 // MT rows of x at most (M <= MT at run time), R weight rows per warp, ksplit warps per
-// group of rows (a divisor of 8).  Entry e = m * R + r of a lane's sums is y[m][n0 + r].
+// group of rows (a divisor of 8).  Lane l takes codes 8p .. 8p + 7 (p = l % 4) of block
+// b0 + l / 4, so a warp covers 8 blocks of each of its rows per step: three aligned loads
+// (32, 32 and 16 bits) hold the 8 codes, which start 2 bytes into the block, after a shift
+// by 0 or 16 bits; the block's scale is one 16-bit load.  Each code is widened exactly, the
+// 8 products of a row of x are summed with fused multiply-adds and that sum is scaled by d
+// once.  Rows of x are taken four at a time (their 8 x values each in registers).  Entry
+// e = m * R + r of a lane's sums is y[m][n0 + r].
 template <int MT, int R>
 __global__ void __launch_bounds__(kQ80Threads)
 q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x, float *__restrict__ y, int M,
                 int64_t N, int K, int ksplit) {
     constexpr int V = MT * R;
+    constexpr int MG = MT < 4 ? MT : 4;   // rows of x per pass
     static_assert(V <= 32 && (V & (V - 1)) == 0, "entries per lane");
     __shared__ float part[kQ80Warps][V];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int group = warp / ksplit, kw = warp - group * ksplit;
     const int64_t n0 = (static_cast<int64_t>(blockIdx.x) * (kQ80Warps / ksplit) + group) * R;
-    const int nblk = K >> 5, npair = (nblk + 1) >> 1;
-    const int half = lane >> 4, j = lane & 15;
+    const int nblk = K >> 5, nstep = (nblk + 7) >> 3;
+    const int bs = lane >> 2, p = lane & 3;
     // rows past N read row N - 1; their sums are not stored
-    const uint16_t *row[R];
+    const uint8_t *row[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const int64_t n = n0 + r < N ? n0 + r : N - 1;
-        row[r] = reinterpret_cast<const uint16_t *>(blocks) + n * nblk * 17;
+        row[r] = blocks + n * nblk * 34;
     }
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.0f;
     wait_prior_grid();   // x may belong to the kernel before this one in the stream
-#pragma unroll 2
-    for (int p = kw; p < npair; p += ksplit) {
-        const int bl = 2 * p + half;
-        const bool live = bl < nblk;           // false only for lanes 16-31 past an odd last block
+    for (int st = kw; st < nstep; st += ksplit) {
+        const int bl = 8 * st + bs;
+        const bool live = bl < nblk;   // false only for lanes past an incomplete last step
         const int b = live ? bl : nblk - 1;
-        float t0[R], t1[R];
+        // codes 8p .. 8p + 7 start at byte 34 b + 2 + 8p of the row, an address that is only
+        // 2-byte aligned (rows and blocks start on even bytes): two 32-bit words from the
+        // 4-byte boundary at or below it, shifted by 0 or 16 bits, and after a shift a 16-bit
+        // load for the last two codes (so every load ends on the block's last code byte)
+        const uint32_t off = static_cast<uint32_t>(b) * 34u + 2u + 8u * p;
+        float q[R][8], d[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const uint32_t c = ldg_u16(row[r] + b * 17 + 1 + j);   // elements 2j (low byte), 2j + 1
-            const float d = live ? half_bits_to_float(ldg_u16(row[r] + b * 17)) : 0.0f;
-            t0[r] = static_cast<float>(static_cast<int32_t>(c << 24) >> 24) * d;
-            t1[r] = static_cast<float>(static_cast<int32_t>(c << 16) >> 24) * d;
+            const uint8_t *cp = row[r] + off;
+            const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(cp) & 2u) * 8u;   // 0 or 16
+            const uint32_t *wp = reinterpret_cast<const uint32_t *>(cp - (shift >> 3));
+            const uint32_t a0 = __ldg(wp), a1 = __ldg(wp + 1);
+            const uint32_t a2 = shift ? ldg_u16(reinterpret_cast<const uint16_t *>(cp + 6)) : 0u;
+            const uint32_t w0 = __funnelshift_r(a0, a1, shift), w1 = __funnelshift_r(a1, a2, shift);
+            d[r] = live ? half_bits_to_float(ldg_u16(reinterpret_cast<const uint16_t *>(row[r] + 34u * b))) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                q[r][i] = static_cast<float>(static_cast<int32_t>(w0 << (24 - 8 * i)) >> 24);
+                q[r][4 + i] = static_cast<float>(static_cast<int32_t>(w1 << (24 - 8 * i)) >> 24);
+            }
         }
-        const float *xb = x + b * 32 + 2 * j;
+        const float *xb = x + 32 * b + 8 * p;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < M) {
-                const float2 xv = __ldg(reinterpret_cast<const float2 *>(xb + static_cast<int64_t>(m) * K));
+        for (int m0 = 0; m0 < MT; m0 += MG) {
+            float xv[MG][8];
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    acc[m * R + r] = fmaf(t0[r], xv.x, acc[m * R + r]);
-                    acc[m * R + r] = fmaf(t1[r], xv.y, acc[m * R + r]);
+            for (int mm = 0; mm < MG; ++mm) {
+                const int m = m0 + mm;
+                if (m < M) {
+                    const float4 lo = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<int64_t>(m) * K));
+                    const float4 hi = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<int64_t>(m) * K) + 1);
+                    xv[mm][0] = lo.x; xv[mm][1] = lo.y; xv[mm][2] = lo.z; xv[mm][3] = lo.w;
+                    xv[mm][4] = hi.x; xv[mm][5] = hi.y; xv[mm][6] = hi.z; xv[mm][7] = hi.w;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) xv[mm][i] = 0.0f;
                 }
             }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int mm = 0; mm < MG; ++mm) {
+                    float sum = q[r][0] * xv[mm][0];
+#pragma unroll
+                    for (int i = 1; i < 8; ++i) sum = fmaf(q[r][i], xv[mm][i], sum);
+                    acc[(m0 + mm) * R + r] = fmaf(d[r], sum, acc[(m0 + mm) * R + r]);
+                }
         }
     }
     allow_next_grid();
@@ -140,10 +174,10 @@ int launch_q80(const uint8_t *blocks, const float *x, float *y, int M, int64_t N
 }
 
 // The smallest split of the blocks over the warps of a CTA (1, 2, 4 or 8, at most the
-// pairs of blocks in a row) that gives at least `want` CTAs, or the largest allowed.
-int q80_split(int64_t N, int R, int npair, int64_t want) {
+// steps of 8 blocks in a row) that gives at least `want` CTAs, or the largest allowed.
+int q80_split(int64_t N, int R, int nstep, int64_t want) {
     int ks = 1;
-    while (ks < kQ80Warps && 2 * ks <= npair) {
+    while (ks < kQ80Warps && 2 * ks <= nstep) {
         const int64_t rows = static_cast<int64_t>(kQ80Warps / ks) * R;
         if ((N + rows - 1) / rows >= want) break;
         ks *= 2;
@@ -155,12 +189,12 @@ int q80_split(int64_t N, int R, int npair, int64_t want) {
 // per warp.
 template <int MT, int RW>
 int launch_q80_m(const uint8_t *blocks, const float *x, float *y, int M, int64_t N, int K, cudaStream_t stream) {
-    const int npair = (K / 32 + 1) / 2;
+    const int nstep = (K / 32 + 7) / 8;
     const int64_t want = 4LL * device_info().sms;
-    const int ks = q80_split(N, RW, npair, want);
+    const int ks = q80_split(N, RW, nstep, want);
     const int64_t rows = static_cast<int64_t>(kQ80Warps / ks) * RW;
     if ((N + rows - 1) / rows >= want) return launch_q80<MT, RW>(blocks, x, y, M, N, K, ks, stream);
-    return launch_q80<MT, 1>(blocks, x, y, M, N, K, q80_split(N, 1, npair, want), stream);
+    return launch_q80<MT, 1>(blocks, x, y, M, N, K, q80_split(N, 1, nstep, want), stream);
 }
 
 }  // namespace
@@ -171,7 +205,7 @@ int launch_q80gemv(const uint8_t *blocks, const float *x, float *y, int M, int64
     if (M <= 1) return launch_q80_m<1, 4>(blocks, x, y, M, N, K, stream);
     if (M <= 2) return launch_q80_m<2, 4>(blocks, x, y, M, N, K, stream);
     if (M <= 4) return launch_q80_m<4, 4>(blocks, x, y, M, N, K, stream);
-    if (M <= 8) return launch_q80_m<8, 4>(blocks, x, y, M, N, K, stream);
+    if (M <= 8) return launch_q80_m<8, 2>(blocks, x, y, M, N, K, stream);
     return launch_q80_m<16, 2>(blocks, x, y, M, N, K, stream);
 }
 

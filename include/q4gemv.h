@@ -245,9 +245,9 @@ Q4_API int q4_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M
  * K a multiple of 32.  M = 1 with N >= 4096 and blocks 16-byte aligned runs the
  * TMA-streamed kernel's Q8_0 instances (dp4a on the byte planes of x: the dp4a kernels'
  * accuracy, with sum |w| = sum |q d|); every other shape a CUDA-core kernel in which each
- * weight q d is formed exactly in binary32 and the products are accumulated with fused
- * multiply-adds (the stated tolerance for every finite x).  Asynchronous; allocates
- * nothing. */
+ * code is widened exactly to binary32, the products of 8 codes of a block with x are summed
+ * with fused multiply-adds and each such sum is scaled by d once (the stated tolerance for
+ * every finite x).  Asynchronous; allocates nothing. */
 Q4_API int q8_0_gemv_run(const void *blocks, const float *x, float *y, int32_t M, int64_t N, int64_t K,
                   void *stream);
 

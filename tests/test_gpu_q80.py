@@ -37,11 +37,13 @@ def run(torch, blocks, x):
     return b[guard:guard + M * N].reshape(M, N)
 
 
-# On 152 SMs these reach every plan of the CUDA-core kernel: 4 weight rows per warp with
-# the blocks unsplit (40003 x 896, 20001 x 608 with an odd 19 blocks per row) or split over
-# 4 or 8 warps (4864 x 896, 4096 x 4096, 3001 x 608), 2 rows per warp at M = 16 (9001 x 864,
-# 27 blocks), one row per warp split over 4 or 8 warps (2051 x 4096, 896 x 896), ragged
-# last CTAs, a single block per row (K = 32: lanes 16-31 idle) and single rows.
+# On 152 SMs these reach every plan of the CUDA-core kernel (a warp takes 8 blocks of each
+# of its rows per step): 4 weight rows per warp with the blocks unsplit (40003 x 896;
+# 20001 x 608, whose 19 blocks leave a partial last step) or split over 4 or 8 warps
+# (4864 x 896, 4096 x 4096), 2 rows per warp at M = 5..8 split over 4 warps (4099 x 1056,
+# 33 blocks), one row per warp unsplit at M = 16 (9001 x 864) or split over 2, 4 or 8 warps
+# (3001 x 608, 2051 x 4096, 896 x 4864), ragged last CTAs, a single block per row (K = 32:
+# the lanes past it idle) and single rows.
 @pytest.mark.parametrize("M,N,K", [(1, 896, 896), (2, 4864, 896), (1, 896, 4864), (3, 1000, 2048), (4, 4096, 4096),
                                    (8, 300, 16384), (16, 512, 2048), (5, 77, 32), (1, 1, 64), (2, 33, 4864),
                                    (4, 40003, 896), (3, 20001, 608), (16, 9001, 864), (2, 2051, 4096),
@@ -85,6 +87,20 @@ def test_lm_head(torch):
     y_ref, bound = _rows_threaded(blocks, x)
     r = assert_within_bound(y, y_ref, bound, "Q8_0 LM head")
     assert r < 0.05, r   # N(0, 1) activations: far inside the tolerance
+
+
+@pytest.mark.parametrize("M,N,K", [(4, 128256, 4096), (2, 128256, 4096), (16, 151936, 896), (8, 14336, 4096)])
+def test_cuda_core_kernel_full_size_sampled(torch, M, N, K):
+    # the decode shapes at M > 1 (the CUDA-core kernel): every output finite, 257 rows
+    # (both ends, random ones in between) against the oracle
+    blocks = synth.q80_blocks(M + 31, N, K)
+    x = synth.activations_f32(M + 37, M, K)
+    y = run(torch, blocks, x)
+    assert np.all(np.isfinite(y)), f"{int(np.sum(~np.isfinite(y)))} outputs not finite"
+    rows = np.unique(np.concatenate([[0, 1, N - 2, N - 1],
+                                     np.random.default_rng(N + M).choice(N, size=253, replace=False)]))
+    y_ref, bound = oracle.q80_gemv(np.ascontiguousarray(blocks[rows]), x)
+    assert_within_bound(y[:, rows], y_ref, bound, f"Q8_0 full size M={M} N={N} K={K}")
 
 
 def test_matches_q4_0_on_the_int4_range(torch):
