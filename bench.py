@@ -1193,7 +1193,7 @@ def run_q80(args, torch, q4):
         torch.cuda.empty_cache()
     return {"kernel": "streamed kernel's Q8_0 instances (M = 1, long matrices: whole 34-byte blocks by bulk copy, "
                       "codes read as nine 32-bit words shifted to the 2-byte offset, dp4a on the byte planes of x), "
-                      "else a CUDA-core kernel (lanes over elements, 4 weight rows per warp sharing each x load, q*d exact in f32)", "cells": out}
+                      "else a CUDA-core kernel (8 codes per lane, 2-4 weight rows per warp sharing each x load, one scale multiply per 8 codes)", "cells": out}
 
 
 def run_decode_8b(args, torch, q4):

@@ -58,7 +58,7 @@ __device__ __forceinline__ void warp_sum_scatter(float (&v)[V], int lane) {
 template <int MT, int R>
 __global__ void __launch_bounds__(kQ80Threads)
 q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x, float *__restrict__ y, int M,
-                int64_t N, int K, int ksplit) {
+                int64_t N, int K, int ksplit, unsigned int *bounds) {
     constexpr int V = MT * R;
     constexpr int MG = MT < 4 ? MT : 4;   // rows of x per pass
     static_assert(V <= 32 && (V & (V - 1)) == 0, "entries per lane");
@@ -75,6 +75,14 @@ q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x,
         const int64_t n = n0 + r < N ? n0 + r : N - 1;
         row[r] = blocks + n * nblk * 34;
     }
+    // (bounds-checking builds) a load of sz bytes at p lies inside the blocks and is
+    // naturally aligned
+    const uint8_t *const blocks_end = blocks + N * nblk * 34;
+    auto ok_w = [&](const void *p, int sz) {
+        const uint8_t *b = static_cast<const uint8_t *>(p);
+        return q4_in_bounds(b >= blocks && b + sz <= blocks_end && (reinterpret_cast<uintptr_t>(b) % sz) == 0,
+                            bounds);
+    };
     float acc[V];
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.0f;
@@ -94,10 +102,13 @@ q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x,
             const uint8_t *cp = row[r] + off;
             const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(cp) & 2u) * 8u;   // 0 or 16
             const uint32_t *wp = reinterpret_cast<const uint32_t *>(cp - (shift >> 3));
-            const uint32_t a0 = __ldg(wp), a1 = __ldg(wp + 1);
-            const uint32_t a2 = shift ? ldg_u16(reinterpret_cast<const uint16_t *>(cp + 6)) : 0u;
+            const uint32_t a0 = ok_w(wp, 4) ? __ldg(wp) : 0u, a1 = ok_w(wp + 1, 4) ? __ldg(wp + 1) : 0u;
+            const uint32_t a2 =
+                shift && ok_w(cp + 6, 2) ? ldg_u16(reinterpret_cast<const uint16_t *>(cp + 6)) : 0u;
             const uint32_t w0 = __funnelshift_r(a0, a1, shift), w1 = __funnelshift_r(a1, a2, shift);
-            d[r] = live ? half_bits_to_float(ldg_u16(reinterpret_cast<const uint16_t *>(row[r] + 34u * b))) : 0.0f;
+            d[r] = live && ok_w(row[r] + 34u * b, 2)
+                       ? half_bits_to_float(ldg_u16(reinterpret_cast<const uint16_t *>(row[r] + 34u * b)))
+                       : 0.0f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 q[r][i] = static_cast<float>(static_cast<int32_t>(w0 << (24 - 8 * i)) >> 24);
@@ -111,7 +122,10 @@ q80_gemv_kernel(const uint8_t *__restrict__ blocks, const float *__restrict__ x,
 #pragma unroll
             for (int mm = 0; mm < MG; ++mm) {
                 const int m = m0 + mm;
-                if (m < M) {
+                const float *xp = xb + static_cast<int64_t>(m) * K;
+                if (m < M && q4_in_bounds(xp >= x && xp + 8 <= x + static_cast<int64_t>(M) * K &&
+                                              (reinterpret_cast<uintptr_t>(xp) & 15u) == 0,
+                                          bounds)) {
                     const float4 lo = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<int64_t>(m) * K));
                     const float4 hi = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<int64_t>(m) * K) + 1);
                     xv[mm][0] = lo.x; xv[mm][1] = lo.y; xv[mm][2] = lo.z; xv[mm][3] = lo.w;
@@ -165,7 +179,7 @@ int launch_q80(const uint8_t *blocks, const float *x, float *y, int M, int64_t N
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     add_overlap_attr(cfg, attr);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, q80_gemv_kernel<MT, R>, blocks, x, y, M, N, K, ksplit);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, q80_gemv_kernel<MT, R>, blocks, x, y, M, N, K, ksplit, bounds_counter());
     if (e != cudaSuccess) {
         set_cuda_error(e);
         return Q4_ERR_CUDA;

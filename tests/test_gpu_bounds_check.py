@@ -1,6 +1,7 @@
 """The bounds-checking build (libq4gemv_check.so, -DQ4_BOUNDS_CHECK): every checked
 shared- and global-memory index of the streamed, tensor-core and register-resident GEMV
-kernels is compared with its buffer; one out of range is counted on a device counter
+kernels, the split matmul and the Q8_0 CUDA-core GEMV (whose loads are also checked for
+alignment) is compared with its buffer; one out of range is counted on a device counter
 and skipped.  With a memory checker unavailable, these tests run the shapes with the
 most index arithmetic (ragged last blocks and tiles, K tails, runtime geometry) through
 that build and require zero counted violations and results within tolerance.  Marked gpu.
@@ -168,3 +169,23 @@ def test_q80_streamed_kernel(torch, N, K):
     rows = sorted(set(np.random.default_rng(3).choice(N, 64, replace=False).tolist()) | {0, N - 1})
     y_ref, bound = oracle.q80_gemv_rows(blocks, x, rows)
     assert_within_bound(host(y)[:, rows], y_ref, bound, f"Q8_0 bounds N={N} K={K}")
+
+
+@pytest.mark.parametrize("offset", [0, 2])
+@pytest.mark.parametrize("M,N,K", [(5, 77, 32), (3, 2001, 608), (7, 999, 1056), (4, 4099, 896), (16, 301, 864),
+                                   (1, 896, 4864), (2, 33, 4864)])
+def test_q80_cuda_core_kernel(torch, M, N, K, offset):
+    # the CUDA-core Q8_0 kernel: 32- and 16-bit code loads at addresses that are only 2-byte
+    # aligned; rows of an odd number of blocks alternate between the two alignments, and a
+    # blocks array 2 bytes past a 4-byte boundary swaps them; every load is checked for range
+    # and alignment
+    blocks = synth.q80_blocks(N + K + offset, N, K)
+    raw = torch.zeros(blocks.size + 16, dtype=torch.uint8, device="cuda")
+    raw[offset:offset + blocks.size] = torch.from_numpy(blocks.reshape(-1)).cuda()
+    x = synth.activations_f32(N + M, M, K)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    q4.q8_0_gemv_run(raw.data_ptr() + offset, dev(x, torch), y, M, N, K)
+    assert q4.q4gemv_bounds_violations() == 0, f"Q8_0 CUDA-core M={M} N={N} K={K}: out-of-range accesses counted"
+    y_ref, bound = oracle.q80_gemv(blocks, x)
+    assert_within_bound(host(y), y_ref, bound, f"Q8_0 CUDA-core bounds M={M} N={N} K={K} offset={offset}")
+
