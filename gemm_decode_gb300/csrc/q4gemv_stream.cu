@@ -48,11 +48,13 @@ int launch_stream_k896(const StreamArgs &a, int group, bool asym, int fuse, cuda
 int launch_stream_k2048(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_k4096(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_k8192(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
+int launch_stream_k14336(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_k16384(const StreamArgs &a, int group, bool asym, int fuse, cudaStream_t s);
 int launch_stream_grouped_k896(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 int launch_stream_grouped_k2048(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 int launch_stream_grouped_k4096(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 int launch_stream_grouped_k8192(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
+int launch_stream_grouped_k14336(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 int launch_stream_grouped_k16384(StreamGroupArgs &a, int group, bool asym, cudaStream_t s);
 
 // ------------------------------------------------------------------ host side
@@ -141,6 +143,7 @@ static int launch_stream_any(const uint8_t *codes, const uint16_t *scales, const
         case 2048: return launch_stream_k2048(a, group, asym, fuse, stream);
         case 4096: return launch_stream_k4096(a, group, asym, fuse, stream);
         case 8192: return launch_stream_k8192(a, group, asym, fuse, stream);
+        case 14336: return launch_stream_k14336(a, group, asym, fuse, stream);
         case 16384: return launch_stream_k16384(a, group, asym, fuse, stream);
         default:   // runtime geometry; stream_u(K) is 8 for every K without an instance
             if (fuse == 4) return launch_stream<0, 0, 0, 8, false, 4>(a, stream);
@@ -208,7 +211,7 @@ int launch_q4gemv_stream_q80(const uint8_t *blocks, const float *x, float *y, in
 bool stream_grouped_applies(const StreamSeg *segs, int nseg, int K, int group) {
     if (nseg < 1 || nseg > kStreamMaxSeg) return false;
     if (group != 32 && group != 64 && group != 128) return false;
-    if (K != 896 && K != 2048 && K != 4096 && K != 8192 && K != 16384) return false;   // compile-time geometries
+    if (K != 896 && K != 2048 && K != 4096 && K != 8192 && K != 14336 && K != 16384) return false;   // compile-time geometries
     const bool asym = segs[0].zeros != nullptr;
     const int rg = stream_rg(K);
     if (rg == 0) return false;
@@ -312,6 +315,7 @@ int launch_q4gemv_stream_grouped(const StreamSeg *segs, int nseg, int K, int gro
         case 2048: return launch_stream_grouped_k2048(a, group, asym, stream);
         case 4096: return launch_stream_grouped_k4096(a, group, asym, stream);
         case 8192: return launch_stream_grouped_k8192(a, group, asym, stream);
+        case 14336: return launch_stream_grouped_k14336(a, group, asym, stream);
         case 16384: return launch_stream_grouped_k16384(a, group, asym, stream);
         default: return Q4_ERR_UNSUPPORTED;
     }
