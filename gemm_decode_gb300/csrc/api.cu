@@ -464,7 +464,7 @@ int q4gemm_run_ex(const void *codes, const void *scales_f16, const void *zeros_u
                   float *c, int32_t M, int64_t N, int64_t K, int32_t group, const q4_run_options_t *opts,
                   void *stream) {
     CallOptions co;
-    const int st = options_from(opts, Q4_RUN_WAIT_TIMEOUT, co);
+    const int st = options_from(opts, Q4_RUN_OVERLAPPED | Q4_RUN_WAIT_TIMEOUT, co);
     if (st != Q4_OK) return st;
     CallScope scope(co);
     return q4gemm_run(codes, scales_f16, zeros_u4_or_null, a_bf16, c, M, N, K, group, stream);

@@ -122,6 +122,7 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    allow_next_grid();   // (overlapped launch) the next kernel may be scheduled
     const unsigned long long limit = g.timeout_ns;
     auto ib = [&](bool ok) { return q4_in_bounds(ok, g.bounds); };   // bounds-checking builds
 
@@ -133,6 +134,9 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (A)
         if (lane == 0) {
+            // (overlapped launch) A may be written by the kernel before this one in the
+            // stream; the weights are read without waiting
+            wait_prior_grid();
             int issued = 0;
             for (int kb = 0; kb < kblocks && !*abort_flag; ++kb) {
                 const int s = kb % STAGES;
@@ -268,6 +272,7 @@ q4gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const GemmArgs g) {
             const int r = quad * 32 + lane;        // accumulator row = TMEM lane
             const bool ok = mbar_wait(done_bar, 0, limit);
             if (!ok) fail();
+            wait_prior_grid();   // (overlapped launch) c may be in use by the kernel before this one
             if (ok && !*abort_flag) {
                 tc_fence_after();
                 const int m = m0 + eh * BM + r;
@@ -394,7 +399,18 @@ static int launch_tc(const CUtensorMap &map, const GemmArgs &g, int M, int64_t N
     }
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + NH * BM - 1) / (NH * BM)));
     if (grid.y > 65535) return Q4_ERR_UNSUPPORTED;
-    q4gemm_tc_kernel<NH, STAGES><<<grid, kThreads, smem, stream>>>(map, g);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    add_overlap_attr(cfg, attr);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, q4gemm_tc_kernel<NH, STAGES>, map, g);
+    if (e != cudaSuccess) {
+        set_cuda_error(e);
+        return Q4_ERR_CUDA;
+    }
     return launch_status();
 }
 

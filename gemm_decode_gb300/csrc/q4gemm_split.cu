@@ -146,6 +146,7 @@ q4gemm_split_kernel(const __grid_constant__ CUtensorMap tmap_a, const SplitArgs 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    allow_next_grid();   // (overlapped launch) the next kernel may be scheduled
     if (split > 1) cluster_arrive_relaxed();   // phase 1: this CTA has started (waited on before any push)
 
     auto fail = [&]() {
@@ -156,6 +157,9 @@ q4gemm_split_kernel(const __grid_constant__ CUtensorMap tmap_a, const SplitArgs 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (A)
         if (lane == 0) {
+            // (overlapped launch) A may be written by the kernel before this one in the
+            // stream; the weights are read without waiting
+            wait_prior_grid();
             int issued = 0;
             for (int j = 0; j < nkb && !*abort_flag; ++j) {
                 const int s = j % kSplitStages;
@@ -287,6 +291,7 @@ q4gemm_split_kernel(const __grid_constant__ CUtensorMap tmap_a, const SplitArgs 
         const int r = quad * 32 + lane;              // accumulator row = TMEM lane = row of A
         const bool ok = mbar_wait(done_bar, 0, limit);
         if (!ok) fail();
+        wait_prior_grid();   // (overlapped launch) c may be in use by the kernel before this one
         __syncwarp();
         if (split > 1) cluster_wait();   // every peer has started: its shared memory may be written
         if (ok && !*abort_flag) {
@@ -415,13 +420,14 @@ static int launch_split(const CUtensorMap &map, const SplitArgs &g, cudaStream_t
     cfg.blockDim = dim3(kSplitThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(g.S);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    add_overlap_attr(cfg, attr);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, g);
     if (e != cudaSuccess) {
         set_cuda_error(e);

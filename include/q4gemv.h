@@ -268,8 +268,12 @@ Q4_API int q4gemm_run(const void *codes, const void *scales_f16, const void *zer
                const void *a_bf16, float *c, int32_t M, int64_t N, int64_t K, int32_t group,
                void *stream);
 
-/* q4gemm_run with per-call options (opts may be NULL).  Only Q4_RUN_WAIT_TIMEOUT
- * applies; any other flag or a nonzero reserved field is Q4_ERR_INVALID_ARG. */
+/* q4gemm_run with per-call options (opts may be NULL).  Q4_RUN_OVERLAPPED and
+ * Q4_RUN_WAIT_TIMEOUT apply; any other flag or a nonzero reserved field is
+ * Q4_ERR_INVALID_ARG.  Overlapped, the matmul may be scheduled while the kernel before it
+ * in the stream still runs: it sets up and reads the weight arrays at once and waits for
+ * that kernel before it reads a_bf16 or writes c (the contract of the GEMVs' overlapped
+ * launch: the weight arrays must not be written by the kernel immediately before it). */
 Q4_API int q4gemm_run_ex(const void *codes, const void *scales_f16, const void *zeros_u4_or_null,
                   const void *a_bf16, float *c, int32_t M, int64_t N, int64_t K, int32_t group,
                   const q4_run_options_t *opts, void *stream);
@@ -301,8 +305,10 @@ Q4_API int q4gemv_device_status(void *stream);
  * entry points instead. */
 Q4_API int q4gemm_set_wait_timeout_ns(uint64_t ns);
 
-/* Overlapped launch of the M <= 2 GEMV kernels (programmatic dependent launch).
- * With enable != 0, every later q4gemv_run launch carries CUDA's programmatic
+/* Overlapped launch of the GEMV and matmul kernels (programmatic dependent launch).
+ * With enable != 0, every later launch by the entry points without options
+ * (q4gemv_run, q4gemv_fused_run, q4_0_gemv_run, q8_0_gemv_run, q4gemv_grouped_run,
+ * q4gemm_run; for the matmul, a_bf16 and c take the roles of x and y) carries CUDA's programmatic
  * stream serialisation attribute: the kernel may be scheduled while the kernel
  * before it in the stream is still running, and it starts streaming codes, scales
  * and zero points at once; before it reads x or writes y it waits (griddepcontrol.wait)

@@ -180,10 +180,13 @@ def test_per_call_options_are_checked(L):
     # an unknown flag or a nonzero reserved field is rejected before anything else
     assert L.q4gemv_run_ex(*ok, ctypes.byref(O(0x80, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
     assert L.q4gemv_run_ex(*ok, ctypes.byref(O(0, 1, 0)), None) == q4.Q4_ERR_INVALID_ARG
-    # the matmul takes only the wait bound
+    # the matmul takes the overlapped launch and the wait bound, not the exact-x kernel:
+    # with the overlapped flag the options pass and the argument checks run (a misaligned A)
     gm = (B0, B1, None, B3, B4, 128, 64, 64, 32)
     assert L.q4gemm_run_ex(*gm, ctypes.byref(O(q4.Q4_RUN_EXACT_X, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
-    assert L.q4gemm_run_ex(*gm, ctypes.byref(O(q4.Q4_RUN_OVERLAPPED, 0, 0)), None) == q4.Q4_ERR_INVALID_ARG
+    assert L.q4gemm_run_ex(B0, B1, None, B3 + 2, B4, 128, 64, 64, 32,
+                           ctypes.byref(O(q4.Q4_RUN_OVERLAPPED | q4.Q4_RUN_WAIT_TIMEOUT, 0, 5)), None) \
+        == q4.Q4_ERR_MISALIGNED
     # valid options, then the usual argument checks
     good = ctypes.byref(O(q4.Q4_RUN_OVERLAPPED | q4.Q4_RUN_EXACT_X | q4.Q4_RUN_WAIT_TIMEOUT, 0, 5))
     assert L.q4gemv_run_ex(B0, B1, None, B3, B4, 17, 64, 64, 32, good, None) == q4.Q4_ERR_UNSUPPORTED

@@ -1,4 +1,4 @@
-"""Overlapped (programmatic dependent) launch of the GEMV kernels.
+"""Overlapped (programmatic dependent) launch of the GEMV and matmul kernels.
 
 With the Q4_RUN_OVERLAPPED option of q4gemv_run_ex (or the process-wide
 q4gemv_set_overlapped_launch(1) for q4gemv_run) a GEMV may start streaming its
@@ -146,3 +146,52 @@ def test_dependent_chain_in_cuda_graph(torch):
             g.replay()
         torch.cuda.synchronize()
         ch.check(900 + rep)
+
+
+# The matmul (q4gemm_run_ex with Q4_RUN_OVERLAPPED): the split kernel (few tiles) and the
+# regular one (one and four 128-row halves of A per CTA)
+GEMM_SHAPES = [(128, 512, 2048, 32), (200, 1024, 1024, 64), (640, 2048, 1024, 128)]
+
+
+def _gemm_weights(torch, M, N, K, g):
+    w = synth.q4_weights(M + N + K, N, K, g, tag="gemm-overlap")
+    return w, (dev(w.codes, torch), dev(w.scales, torch), dev(w.zeros, torch))
+
+
+@pytest.mark.parametrize("M,N,K,g", GEMM_SHAPES)
+def test_matmul_reads_a_written_by_the_kernel_before_it(torch, M, N, K, g):
+    # the kernel right before the overlapped matmul converts A to bf16 (A held NaN until
+    # then): a read of A that did not wait would see NaN or the previous pass
+    w, dw = _gemm_weights(torch, M, N, K, g)
+    a32 = dev(synth.activations_f32(M + 1, M, K), torch)
+    a = torch.full((M, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    c = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for rep in range(2):
+        a.copy_(a32 * (1.0 + rep))         # a conversion kernel writes A
+        q4.q4gemm_run_ex(*dw, a, c, M, N, K, g, flags=q4.Q4_RUN_OVERLAPPED)
+        torch.cuda.synchronize()
+        a_bits = host(a.view(torch.int16)).view(np.uint16)
+        c_ref, bound = oracle.q4_gemm(w.codes, w.scales, w.zeros, a_bits, g)
+        err = np.abs(host(c).astype(np.float64) - c_ref.astype(np.float64))
+        assert np.all(err <= (2.0 ** -9 + 2e-6) * bound + 1e-6), f"pass {rep} M={M} N={N} K={K}"
+
+
+@pytest.mark.parametrize("M,N,K,g", GEMM_SHAPES)
+def test_matmul_writes_c_after_the_kernel_before_it_read_it(torch, M, N, K, g):
+    # the kernel right before the overlapped matmul reads C (a scaled copy); it must see
+    # C's old contents, and C must then hold the product
+    w, dw = _gemm_weights(torch, M, N, K, g)
+    a_bits = (synth.activations_f32(M + 2, M, K).view(np.uint32) >> 16).astype(np.uint16)
+    a = dev(a_bits, torch)
+    c = torch.full((M, N), 7.0, dtype=torch.float32, device="cuda")
+    seen = torch.empty_like(c)
+    torch.cuda.synchronize()
+    torch.mul(c, 2.0, out=seen)          # a kernel reads C
+    q4.q4gemm_run_ex(*dw, a, c, M, N, K, g, flags=q4.Q4_RUN_OVERLAPPED)
+    torch.cuda.synchronize()
+    assert np.all(host(seen) == 14.0), "the previous kernel saw C already overwritten"
+    c_ref, bound = oracle.q4_gemm(w.codes, w.scales, w.zeros, a_bits, g)
+    err = np.abs(host(c).astype(np.float64) - c_ref.astype(np.float64))
+    assert np.all(err <= (2.0 ** -9 + 2e-6) * bound + 1e-6)
+
