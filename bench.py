@@ -732,7 +732,8 @@ def run_prefill(args, torch, q4):
                     "frac_of_bf16_peak": round(tf / burst, 4), "peak": burst, "peak_source": src,
                     "us_p10_p90_min": [round(st["p10"], 3), round(st["p90"], 3), round(st["min"], 3)],
                     "t2n_over_tn": round(st["t2n_over_tn"], 3),
-                    "note": "a graph of back-to-back calls on one weight copy (W fits in L2), median of 5 replays"})
+                    "note": "a graph of back-to-back calls on one weight copy (W fits in L2), median of 5 replays; "
+                            + ("overlapped launch" if getattr(args, "overlap", 1) else "serialised launch")})
     return out
 
 
