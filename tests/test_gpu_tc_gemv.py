@@ -106,6 +106,17 @@ def test_side_data_loaded_one_value_at_a_time(torch, K, g, scale_off, zero_off):
         assert np.all(err <= FP16_REL * bound + 1e-6)
 
 
+@pytest.mark.parametrize("N,K,g,Ms", [(32768, 8192, 32, (4, 16)), (32768, 4096, 128, (8,))])
+def test_long_rows_on_256_row_tiles_split_over_clusters(torch, N, K, g, Ms):
+    # 128 tiles of 256 rows, each tile's K-blocks split over a cluster of 2 (as many CTAs
+    # as 256 tiles of 128 rows, at half the per-weight cost): sampled rows, both ends
+    w = synth.q4_weights(N + K + g, N, K, g, tag="tc-256")
+    rows = sorted(set(np.random.default_rng(N + K).choice(N, size=160, replace=False).tolist()) | {0, 255, 256, N - 1})
+    for M in Ms:
+        x = synth.activations_f32(M + K, M, K)
+        check(torch, w, x, f"256-row tiles N={N} K={K} g={g} M={M}", rows=rows)
+
+
 def test_few_rows_of_x_on_a_tall_matrix(torch):
     # M = 3 and 4 take the tensor cores only for N >= 65536
     N, K = 65600, 896
