@@ -578,17 +578,21 @@ static int tc_gemv_split(int64_t N, int K, int tm) {
     return S;
 }
 
-// Tile height: 256 rows (cheaper per weight) when that still gives two tiles per SM,
-// or when 256-row tiles (with their K split) launch at least as many CTAs as 128-row
-// ones; otherwise 128 rows (twice the tiles).  Measured on the decode and sweep shapes
-// (e.g. 32768 x 8192: 128 tiles of 256 rows over clusters of 2 against 256 unsplit
-// tiles of 128 rows, 7-15 % faster at M = 4..16).
+// Tile height: 256 rows (cheaper per weight) when that still gives two tiles per SM; or
+// when both heights need a K split and 256 rows launch at least as many CTAs; or when
+// 128-row tiles would run unsplit and 256-row tiles split over clusters launch as many
+// CTAs while keeping at least 32 K-blocks per CTA; otherwise 128 rows (twice the tiles).
+// Measured on the decode and sweep shapes: 32768 x 8192 at M = 4..16 is 7-15 % faster
+// as 128 tiles of 256 rows over clusters of 2 than as 256 unsplit 128-row tiles, while
+// 32768 x 896 and x 2048 (7 and 16 K-blocks per CTA once split) are 5-25 % slower.
 static int tc_gemv_tile_rows(int64_t N, int K) {
     const int64_t sms = device_info().sms;
     const int64_t t128 = (N + 127) / 128, t256 = (N + 255) / 256;
     const int s128 = tc_gemv_split(N, K, 128), s256 = tc_gemv_split(N, K, 256);
+    const int kblocks = (K + TK - 1) / TK;
     if (t256 >= 2 * sms) return 256;
-    if (t256 * s256 >= t128 * s128) return 256;
+    if (s128 > 1 && t256 * s256 >= t128 * s128) return 256;
+    if (s128 == 1 && t256 * s256 >= t128 && kblocks / s256 >= 32) return 256;
     return 128;
 }
 
