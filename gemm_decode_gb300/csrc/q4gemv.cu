@@ -92,6 +92,17 @@ int launch_q4gemv(const uint8_t *codes, const uint16_t *scales, const uint8_t *z
         return launch_q4gemv_stream(codes, scales, zeros, x, y, N, K, group, stream);
     if (!exact && stream2_applies(M, N, K, group, codes, scales, zeros))
         return launch_q4gemv_stream2(codes, scales, zeros, x, y, N, K, group, stream);
+    // M = 3 on wide, long matrices: rows 0 and 1 of x on the two-row streamed instances and
+    // row 2 on the one-row ones, two launches (8B LM head 109 us against 134 on the tensor
+    // cores, 14336 x 4096 17.8 against 20.5, 32768 x 8192 68 against 90; at about 8192 rows
+    // the two break even, and narrower matrices stay on the tensor cores)
+    if (!exact && M == 3 && N >= 12288 && stream2_applies(2, N, K, group, codes, scales, zeros) &&
+        stream_applies(1, N, K, group, codes, scales, zeros)) {
+        const int st = launch_q4gemv_stream2(codes, scales, zeros, x, y, N, K, group, stream);
+        if (st != Q4_OK) return st;
+        return launch_q4gemv_stream(codes, scales, zeros, x + 2 * static_cast<int64_t>(K), y + 2 * N, N, K, group,
+                                    stream);
+    }
     if (!exact && tc_gemv_applies(M, N, K, codes))
         return launch_q4gemv_tc(codes, scales, zeros, x, y, M, N, K, group, stream);
     if (!exact) {

@@ -42,7 +42,8 @@
  *   - CUDA-core float kernel (any call with Q4_RUN_EXACT_X; otherwise the shapes no
  *     faster kernel takes): each product (q - z) * s * x is formed exactly and rounded
  *     once, then summed in binary32; within the stated tolerance for every finite input.
- *   - dp4a kernels (M <= 2: the TMA-streamed, register-resident and grouped launches):
+ *   - dp4a kernels (M <= 2: the TMA-streamed, register-resident and grouped launches;
+ *     M = 3 on the streamed launches where they take it):
  *     x is held per 32-element chunk c as 24-bit integers under one power of two,
  *     2^(E_c - 1) <= max_{k in c} |x_k| < 2^E_c (E_c >= -100), and the dot products are
  *     exact in integers.  Per output
@@ -136,8 +137,9 @@ Q4_API int q4gemv_pack_info(int64_t N, int64_t K, int32_t group, q4gemv_pack_inf
  *   codes, scales_f16, zeros_u4_or_null : device, layout above
  *   x : device float [M][K], 16-byte aligned;  y : device float [M][N] (written, not
  *   accumulated)
- * The library picks the kernel by shape: a TMA-streamed dp4a kernel for M = 1 on long
- * matrices, the tcgen05 tensor-core GEMV for 3 <= M <= 16 on large ones (K split over a
+ * The library picks the kernel by shape: a TMA-streamed dp4a kernel for M = 1 and 2 on
+ * long matrices (and M = 3 with N >= 12288: rows 0-1 and row 2 as two streamed launches),
+ * the tcgen05 tensor-core GEMV for 3 <= M <= 16 on large ones (K split over a
  * thread-block cluster when tiles are few), a register-resident dp4a kernel for M <= 2,
  * and a general CUDA-core kernel (split-K over a cluster for long K / few rows) otherwise;
  * the accuracy each gives is stated at the top of this header.  Launches are overlapped

@@ -245,6 +245,20 @@ def test_streamed_kernel_two_rows(torch, K, g, N, symmetric):
     np.testing.assert_array_equal(y, run_gemv(torch, w, x))
 
 
+@pytest.mark.parametrize("K,g,N", [(4096, 128, 14336), (2048, 32, 12301), (14336, 64, 12289)])
+@pytest.mark.parametrize("symmetric", [False, True])
+def test_three_rows_as_two_streamed_launches(torch, K, g, N, symmetric):
+    # M = 3 with N >= 12288 on long matrices: rows 0 and 1 of x on the two-row streamed
+    # instances, row 2 on the one-row ones (x and y offset by two rows).  Every row of
+    # every row of x against the oracle; rows of x are independent.
+    w = synth.q4_weights(N + 3 * K + g, N, K, g, symmetric=symmetric, tag="three-rows")
+    x = synth.activations_f32(N + g + 3, 3, K)
+    y = run_gemv(torch, w, x)
+    y_ref, bound = oracle.q4_gemv_threaded(w.codes, w.scales, w.zeros, x, g, os.cpu_count() or 1)
+    assert_within_bound(y, y_ref, bound, f"three rows N={N} K={K} g={g}")
+    np.testing.assert_array_equal(y[2:3], run_gemv(torch, w, x[2:3]))   # row 2 = the one-row launch alone
+
+
 @pytest.mark.parametrize("K,g,N", [(896, 32, 9765), (896, 128, 9765), (2048, 64, 9777), (4096, 128, 4899),
                                    (4096, 64, 4899), (8192, 32, 4103), (16384, 32, 4099),
                                    (1152, 32, 9761), (14336, 128, 4101)])

@@ -1,6 +1,7 @@
 """The x encoding of the dp4a GEMV kernels as a stated, tested contract.
 
-The streamed (M = 1 and 2, long matrices), register-resident (M <= 2) and grouped
+The streamed (M = 1 and 2, long matrices; M = 3 as two launches on wide ones),
+register-resident (M <= 2) and grouped
 GEMV kernels hold each 32-element chunk c of a row of x as 24-bit integers
 under one shared power of two 2^E_c, 2^(E_c-1) <= max_{k in c} |x_k| < 2^E_c
 (E_c >= -100).  The library header states what that guarantees per output:
@@ -95,21 +96,21 @@ def outlier_x(rng, M, K, cols, factor, base=1.0):
 
 
 def adversarial_inputs(w, seed):
-    """(name, weights, x[2, K]) cases for one weight matrix."""
+    """(name, weights, x[3, K]) cases for one weight matrix."""
     rng = np.random.default_rng(seed)
     K = w.K
     cols = np.arange(K // 32) * 32 + rng.integers(0, 32, K // 32)   # one column per chunk
     wd = with_dead_columns(w, cols)
     out = []
     for e in (10, 15, 20):
-        out.append((f"outlier 2^{e} on dead columns", wd, outlier_x(rng, 2, K, cols, 2.0 ** e)))
-    out.append(("outlier 2^20, live columns", w, outlier_x(rng, 2, K, cols, 2.0 ** 20)))
-    out.append(("tiny rows 2^-40", w, (rng.standard_normal((2, K)) * 2.0 ** -40).astype(np.float32)))
-    sub = (rng.standard_normal((2, K)) * 1e-39).astype(np.float32)      # subnormal binary32
+        out.append((f"outlier 2^{e} on dead columns", wd, outlier_x(rng, 3, K, cols, 2.0 ** e)))
+    out.append(("outlier 2^20, live columns", w, outlier_x(rng, 3, K, cols, 2.0 ** 20)))
+    out.append(("tiny rows 2^-40", w, (rng.standard_normal((3, K)) * 2.0 ** -40).astype(np.float32)))
+    sub = (rng.standard_normal((3, K)) * 1e-39).astype(np.float32)      # subnormal binary32
     sub[:, ::7] = 0.0
     out.append(("subnormal rows", w, sub))
-    out.append(("huge rows 2^60", w, (rng.standard_normal((2, K)) * 2.0 ** 60).astype(np.float32)))
-    mixed = (rng.standard_normal((2, K)) * 2.0 ** -30).astype(np.float32)
+    out.append(("huge rows 2^60", w, (rng.standard_normal((3, K)) * 2.0 ** 60).astype(np.float32)))
+    mixed = (rng.standard_normal((3, K)) * 2.0 ** -30).astype(np.float32)
     mixed[:, cols[::3]] = 1.0e3
     out.append(("tiny chunks beside unit outliers", w, mixed))
     return out
@@ -130,7 +131,7 @@ def gemv(torch, w, x, ex_flags=None):
 # (N, K, g, symmetric, M): the streamed kernel (M = 1 and 2, long matrices), the register-
 # resident kernel (M <= 2, short matrices and small K)
 STREAMED = [(8192, 4096, 128, False, 1), (7680, 896, 32, False, 1), (4096, 2048, 64, True, 1),
-            (8192, 4096, 128, False, 2), (4101, 14336, 32, True, 2)]
+            (8192, 4096, 128, False, 2), (4101, 14336, 32, True, 2), (12288, 4096, 128, False, 3)]
 REGISTER_RESIDENT = [(1000, 896, 32, False, 1), (1000, 896, 32, False, 2), (300, 64, 32, False, 2),
                      (64, 4096, 128, True, 1), (777, 128, 64, False, 2)]
 
