@@ -899,7 +899,7 @@ PROFILE_CASES = {
     "lm_head": (151936, 896, 32, 1),
     "lm_head_8b": (128256, 4096, 128, 1),
     "down_8b": (4096, 14336, 128, 1),
-    "tc_m16": (32768, 4096, 128, 16),      # tensor-core GEMV, 128-row tiles, no K split
+    "tc_m16": (32768, 4096, 128, 16),      # tensor-core GEMV, 256-row tiles, K split over clusters of 2
     "tc_lm05_m8": (151936, 896, 32, 8),    # tensor-core GEMV, 256-row tiles (two MMAs per CTA)
     "tc_down8b_m8": (4096, 14336, 128, 8), # tensor-core GEMV, K split over 8-CTA clusters
 }
