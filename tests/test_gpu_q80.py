@@ -38,12 +38,13 @@ def run(torch, blocks, x):
 
 
 # On 152 SMs these reach every plan of the CUDA-core kernel (a warp takes 8 blocks of each
-# of its rows per step): 4 weight rows per warp with the blocks unsplit (40003 x 896;
-# 20001 x 608, whose 19 blocks leave a partial last step) or split over 4 or 8 warps
-# (4864 x 896, 4096 x 4096), 2 rows per warp at M = 5..8 split over 4 warps (4099 x 1056,
-# 33 blocks), one row per warp unsplit at M = 16 (9001 x 864) or split over 2, 4 or 8 warps
-# (3001 x 608, 2051 x 4096, 896 x 4864), ragged last CTAs, a single block per row (K = 32:
-# the lanes past it idle) and single rows.
+# of its rows per step): 4 weight rows per warp (M <= 4) with the blocks unsplit
+# (40003 x 896; 20001 x 608, whose 19 blocks leave a partial last step) or split over 4 or
+# 8 warps (4864 x 896, 4096 x 4096); 2 rows per warp (M > 4) split over 2 or 4 warps
+# (9001 x 864 at M = 16, 27 blocks; 4099 x 1056, 33 blocks); one row per warp unsplit
+# (77 x 32, 1 x 64) or split over 2, 4 or 8 warps (3001 x 608, 2051 x 4096, 896 x 4864,
+# 512 x 2048 at M = 16); ragged last CTAs, a single block per row (K = 32: the lanes past
+# it idle) and single rows.
 @pytest.mark.parametrize("M,N,K", [(1, 896, 896), (2, 4864, 896), (1, 896, 4864), (3, 1000, 2048), (4, 4096, 4096),
                                    (8, 300, 16384), (16, 512, 2048), (5, 77, 32), (1, 1, 64), (2, 33, 4864),
                                    (4, 40003, 896), (3, 20001, 608), (16, 9001, 864), (2, 2051, 4096),
